@@ -1,0 +1,102 @@
+"""CPU oracle for batched SPOTRF (lower, column-major, strided batch).
+
+TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` may import this package. The CUDA library never
+links, loads or calls it, and it never calls the CUDA library.
+
+The arithmetic lives in ``chol_ref.c`` (plain C, IEEE double, unblocked
+Cholesky-Crout); this module only compiles it with gcc into
+``oracle/_build/liboracle.so`` and marshals numpy arrays through ctypes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "chol_ref.c")
+_BUILD = os.path.join(_HERE, "_build")
+_SO = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle (gcc, -O2, no FMA contraction). Returns the .so path."""
+    with _lock:
+        if (not force and os.path.exists(_SO)
+                and os.path.getmtime(_SO) >= os.path.getmtime(_SRC)):
+            return _SO
+        os.makedirs(_BUILD, exist_ok=True)
+        tmp = _SO + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
+               "-pthread", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _SO)
+        return _SO
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        lib.oracle_potrf_one.restype = ctypes.c_int
+        lib.oracle_potrf_one.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_void_p, ctypes.c_int]
+        lib.oracle_potrf_batched.restype = ctypes.c_int
+        lib.oracle_potrf_batched.argtypes = [
+            ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
+            ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int]
+        _lib = lib
+    return _lib
+
+
+def default_threads() -> int:
+    return max(1, len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity")
+               else (os.cpu_count() or 1))
+
+
+def potrf_one(A: np.ndarray) -> tuple[np.ndarray, int]:
+    """Factor one dense matrix (only its lower triangle is used).
+
+    ``A`` is any n x n array; it is rounded to float32 first (the oracle's
+    input type). Returns (L as float64 n x n with L[i, j] = l_ij, info)."""
+    a32 = np.asfortranarray(np.asarray(A, dtype=np.float32))
+    n = a32.shape[0]
+    L = np.zeros((n, n), dtype=np.float64, order="F")
+    info = _load().oracle_potrf_one(a32.ctypes.data, n, max(1, n), L.ctypes.data, max(1, n))
+    return np.ascontiguousarray(L), int(info)
+
+
+def potrf_batched(buf: np.ndarray, n: int, lda: int, strideA: int, batch: int,
+                  indices: Optional[Sequence[int]] = None,
+                  nthreads: Optional[int] = None) -> tuple[np.ndarray, np.ndarray, int]:
+    """Factor matrices of a strided float32 batch.
+
+    ``buf`` is flat float32 with A_b(i, j) at ``buf[b*strideA + i + j*lda]``.
+    ``indices`` picks a subset of b (default: all). Returns (L, info, threads)
+    with L[t, i, j] = l_ij of the t-th picked matrix (float64) and info[t].
+    """
+    lib = _load()
+    buf = np.ascontiguousarray(buf, dtype=np.float32)
+    if indices is None:
+        src, sA, m = buf, strideA, batch
+    else:
+        idx = list(indices)
+        m = len(idx)
+        span = lda * n
+        src = np.empty(max(1, m * span), dtype=np.float32)
+        for t, b in enumerate(idx):
+            src[t * span:(t + 1) * span] = buf[b * strideA: b * strideA + span]
+        sA = span
+    L = np.zeros((m, n, n), dtype=np.float64)  # [t, j, i]: column-major per matrix
+    info = np.zeros(m, dtype=np.int32)
+    th = default_threads() if nthreads is None else nthreads
+    used = lib.oracle_potrf_batched(src.ctypes.data, n, lda, sA, m, L.ctypes.data,
+                                    n * n, info.ctypes.data, th)
+    return L.transpose(0, 2, 1), info, int(used)
