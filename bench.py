@@ -1,0 +1,516 @@
+#!/usr/bin/env python3
+"""Benchmark of batched SPOTRF (lower, FP32, column-major) on GB300.
+
+One step = one call of bl_spotrf_batched over one batch of a workload (every
+kernel the route launches), on a replica that no earlier step touched since
+the L2 was flushed. Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload n64] [--no-per-n] [--no-cpu-baseline]
+
+The headline workload is n=64, batch=1024 (A = G G^T/64 + 0.1 I); `per_n`
+adds the same measurement for every workload (n = 32, 64, 128, 256, 1024).
+Under torchrun (N > 1) every rank factors its own copy of the batch on its own
+GPU (independent replicas, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "batched SPOTRF matrices/s and GFLOP/s per n; achieved fraction of roofline"
+UNIT = "matrices/s"
+L2_FLUSH_BYTES = 512 << 20
+REPLICA_CAP_BYTES = 96 << 30
+
+# DRAM bytes (read + write) per launch of the dominant kernel from one ncu
+# capture, with the sha256 of the kernel's source file at capture time; a
+# changed source reports null. Filled from the summaries under profiles/.
+TRAFFIC = {
+    # workload: (source file, sha256 prefix, bytes per launch, summary file)
+}
+
+
+def peaks() -> dict:
+    p = {"hbm_gbs": 6684.5, "sm_max_mhz": 2070.0, "source": "fallback"}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        p.update(hbm_gbs=float(m["hbm_gbs"]), sm_max_mhz=float(m["sm_max_mhz"]),
+                 source="measured")
+    except Exception:
+        pass
+    return p
+
+
+def flops_per_matrix(n: int) -> float:
+    return n ** 3 / 3.0
+
+
+def alg_bytes_per_matrix(n: int) -> float:
+    # lower triangle read + lower triangle written, fp32
+    return 4.0 * n * (n + 1)
+
+
+def launches_per_call(n: int) -> int:
+    if n <= 128:
+        return 1
+    panels = (n + 127) // 128
+    return panels + 2 * (panels - 1)
+
+
+def dominant_kernel(n: int) -> str:
+    if n <= 32:
+        return "potrf_warp_kernel"
+    if n <= 128:
+        return "potrf_cta_kernel"
+    return "syrk_tile_kernel"
+
+
+def kernel_source(n: int) -> str:
+    d = os.path.join(ROOT, "matrix_dense_linear_gb300", "csrc")
+    if n <= 32:
+        return os.path.join(d, "potrf_warp.cu")
+    if n <= 128:
+        return os.path.join(d, "potrf_cta.cu")
+    return os.path.join(d, "potrf_blocked.cu")
+
+
+def traffic_for(name: str, n: int):
+    ent = TRAFFIC.get(name)
+    if not ent:
+        return None
+    src, sha, nbytes, _ = ent
+    with open(os.path.join(ROOT, src), "rb") as f:
+        cur = hashlib.sha256(f.read()).hexdigest()
+    return nbytes if cur.startswith(sha) else None
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms in the background."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.samples = []
+        self.proc = None
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return self
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        win = [p for (t, p) in self.samples if t0 - 0.25 <= t <= t1 + 0.25]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[1]) for p in win if num(p[1]) is not None]
+        mx = [num(p[2]) for p in win if num(p[2]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for p in win:
+            for nm, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        pw = [num(p[3]) for p in win if num(p[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(win),
+                "power_w_max": max(pw) if pw else None}
+
+
+def make_host_batch(name: str):
+    import synth
+    return synth.workload_batch(name, fill="mirror", include_info=False)
+
+
+class DeviceWorkload:
+    """Pristine device copy + replicas + the L2 flush buffer for one workload."""
+
+    def __init__(self, bt, steps: int, dev):
+        import torch
+        self.bt = bt
+        self.dev = dev
+        self.span = bt.buf.size
+        self.nbytes = self.span * 4
+        self.pristine = torch.from_numpy(bt.buf).to(dev)
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        want = max(steps, -(-2 * l2 // max(self.nbytes, 1)))
+        self.nrep = int(max(1, min(want, REPLICA_CAP_BYTES // max(self.nbytes, 1))))
+        self.rep = torch.empty((self.nrep, self.span), dtype=torch.float32, device=dev)
+        self.info = torch.zeros(bt.batch, dtype=torch.int32, device=dev)
+        self.flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def refresh(self, k=None):
+        rng = range(self.nrep) if k is None else [k]
+        for i in rng:
+            self.rep[i].copy_(self.pristine)
+
+    def flush_l2(self):
+        self.flush.fill_(1.0)
+
+    def call(self, i: int, stream) -> None:
+        import matrix_dense_linear_gb300 as bl
+        bt = self.bt
+        code = bl.spotrf_batched(self.rep[i].data_ptr(), bt.n, bt.lda, bt.strideA, bt.batch,
+                                 self.info, stream)
+        if code:
+            raise bl.BLError(code)
+
+
+def time_steps(w: DeviceWorkload, steps: int, barrier) -> float:
+    """Device time (ms) of exactly `steps` calls, each on a fresh replica; the
+    replicas are refreshed and the L2 flushed outside the timed intervals."""
+    import torch
+    st = torch.cuda.current_stream()
+    total = 0.0
+    done = 0
+    while done < steps:
+        chunk = min(w.nrep, steps - done)
+        w.refresh()
+        w.flush_l2()
+        torch.cuda.synchronize()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for i in range(chunk):
+            w.call(i, st.cuda_stream)
+        e1.record(st)
+        torch.cuda.synchronize()
+        barrier()
+        total += e0.elapsed_time(e1)
+        done += chunk
+    return total
+
+
+def soak(w: DeviceWorkload, seconds: float) -> None:
+    """Untimed calls for `seconds` (clock ramp and clock sampling under load)."""
+    import torch
+    st = torch.cuda.current_stream()
+    t0 = time.time()
+    i = 0
+    while time.time() - t0 < seconds:
+        k = i % w.nrep
+        w.refresh(k)
+        w.call(k, st.cuda_stream)
+        i += 1
+        if i % 16 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+
+
+def e2e_steps(w: DeviceWorkload, steps: int, warmup: int, barrier) -> dict:
+    """Same metric through the public host-buffer call: every step copies the
+    batch from pinned host memory, factors it, and copies matrices + info back."""
+    import torch
+
+    import matrix_dense_linear_gb300 as bl
+    bt = w.bt
+    host_in = torch.from_numpy(bt.buf).pin_memory()
+    host = torch.empty_like(host_in).pin_memory()
+    info_h = torch.zeros(bt.batch, dtype=torch.int32).pin_memory()
+    A_dev = w.rep[0]
+    for _ in range(warmup):
+        host.copy_(host_in)
+        bl.factor_host(host, bt.n, bt.lda, bt.strideA, bt.batch, info_h, A_dev, w.info)
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    total = 0.0
+    for _ in range(steps):
+        host.copy_(host_in)  # a fresh input each step, outside the timed interval
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        bl.factor_host(host, bt.n, bt.lda, bt.strideA, bt.batch, info_h, A_dev, w.info)
+        e1.record(st)
+        torch.cuda.synchronize()
+        total += e0.elapsed_time(e1)
+    assert not info_h.any().item(), "e2e run reported a failed factorization"
+    return {"ms": total, "h2d": bt.buf.nbytes, "d2h": bt.buf.nbytes + 4 * bt.batch}
+
+
+def oracle_rate(bt, seconds: float = 3.0, max_matrices: int | None = None) -> dict:
+    """The CPU oracle, as it stands, on the host cores: matrices/s on a bounded
+    sample (whole batch, or its first max_matrices), repeated >= `seconds`."""
+    import oracle
+    m = bt.batch if max_matrices is None else min(bt.batch, max_matrices)
+    idx = None if m == bt.batch else list(range(m))
+    th = oracle.default_threads()
+    t0 = time.perf_counter()
+    passes = 0
+    while True:
+        _, _, used = oracle.potrf_batched(bt.buf, bt.n, bt.lda, bt.strideA, bt.batch,
+                                          indices=idx, nthreads=th)
+        passes += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": passes * m / dt, "unit": UNIT, "cores": used, "kind": "oracle",
+            "sample": f"{passes} pass(es) over {m} of {bt.batch} matrices (n={bt.n}), "
+                      f"{dt:.1f} s on {used} host threads",
+            "gflops": passes * m * flops_per_matrix(bt.n) / dt / 1e9}
+
+
+def oracle_sample_size(n: int) -> int | None:
+    # about a second or more of double-precision work per pass on 16 cores
+    return {256: 512, 1024: 32}.get(n)
+
+
+def roofline_entry(name: str, n: int, batch: int, ms_per_call: float, pk: dict, sms: int,
+                   calls_per_launch_avg: float | None = None) -> dict:
+    fp32_peak = sms * 128 * 2 * pk["sm_max_mhz"] * 1e6 / 1e12  # TFLOP/s
+    t = ms_per_call / 1e3
+    bytes_ = alg_bytes_per_matrix(n) * batch
+    flops = flops_per_matrix(n) * batch
+    t_hbm = bytes_ / (pk["hbm_gbs"] * 1e9)
+    t_alu = flops / (fp32_peak * 1e12)
+    if t_hbm >= t_alu:
+        return {"bound": "hbm", "achieved": bytes_ / t / 1e9, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": (bytes_ / t / 1e9) / pk["hbm_gbs"],
+                "roof_ms": t_hbm * 1e3}
+    return {"bound": "alu", "achieved": flops / t / 1e12, "peak": fp32_peak,
+            "unit": "TFLOP/s", "frac": (flops / t / 1e12) / fp32_peak, "roof_ms": t_alu * 1e3}
+
+
+def run_ours(args, rank: int, world: int, barrier) -> dict | None:
+    import torch
+
+    import matrix_dense_linear_gb300 as bl
+    bl.library()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    pk = peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    import synth
+    w_desc = synth.WORKLOADS[args.workload]
+
+    bt = make_host_batch(args.workload)
+    w = DeviceWorkload(bt, args.steps, dev)
+    for i in range(args.warmup):
+        w.refresh(i % w.nrep)
+        w.call(i % w.nrep, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(dev.index).start() if rank == 0 else None
+    t_s0 = time.time()
+    soak(w, args.soak)
+    ms = time_steps(w, args.steps, barrier)
+    soak(w, 0.5)
+    t_s1 = time.time()
+    if sampler:
+        sampler.stop()
+    # max over ranks
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # check this run's output on its last replica (info only; parity is the tests')
+    info = w.info.cpu().numpy()
+    assert not info.any(), "benchmark factorization reported failures"
+
+    e2e = e2e_steps(w, args.steps, min(args.warmup, 3), barrier)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e["ms"]], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e["ms"] = float(t.item())
+
+    n, batch = bt.n, bt.batch
+    per_call = ms / args.steps
+    value = world * batch * args.steps / (ms / 1e3)
+    rf = roofline_entry(args.workload, n, batch, per_call, pk, sms)
+    nl = launches_per_call(n)
+    roof = {"bound": rf["bound"], "achieved": rf["achieved"], "peak": rf["peak"],
+            "unit": rf["unit"], "frac": rf["frac"], "traffic": traffic_for(args.workload, n),
+            "kernel": dominant_kernel(n), "peak_source": pk["source"],
+            "peak_note": ("HBM: measured copy bandwidth" if rf["bound"] == "hbm" else
+                          f"FP32: {sms} SMs x 128 FMA x 2 x {pk['sm_max_mhz']:.0f} MHz")}
+    if nl > 1:
+        roof["note"] = "multi-launch route: achieved is per call over all its launches"
+    if rank != 0:
+        return None
+
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": per_call, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "gflops": value * flops_per_matrix(n) / 1e9,
+        "config": {"workload": f"{args.workload}: n={n}, batch={batch}, lda={bt.lda}, "
+                               f"strideA={bt.strideA}, {w_desc.kind} SPD",
+                   "n": n, "batch": batch, "lda": bt.lda, "strideA": bt.strideA,
+                   "route": bl.route(n, batch),
+                   "l2": "flushed before each timed chunk; every step factors its own "
+                         "replica, untouched since the flush",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": roof,
+        "e2e": {"value": world * batch * args.steps / (e2e["ms"] / 1e3), "unit": UNIT,
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                "ms_per_step": e2e["ms"] / args.steps},
+        "gpu_launches": nl * args.steps,
+        "clocks": sampler.summary(t_s0, t_s1) if sampler else None,
+    }
+    if args.cpu_baseline and world == 1:
+        out["cpu_baseline"] = oracle_rate(bt, 3.0, oracle_sample_size(n))
+    del w
+    torch.cuda.empty_cache()
+
+    if args.per_n:
+        rows = []
+        for name in ["n32", "n64", "n128", "n256", "n1024"]:
+            if name == args.workload:
+                rows.append({"workload": name, "n": n, "batch": batch,
+                             "ms_per_call": per_call, "matrices_per_s": batch / (per_call / 1e3),
+                             "gflops": batch * flops_per_matrix(n) / (per_call / 1e3) / 1e9,
+                             "roofline": {k: rf[k] for k in ("bound", "frac", "roof_ms")},
+                             "launches_per_call": nl,
+                             "oracle_matrices_per_s": out.get("cpu_baseline", {}).get("value")})
+                continue
+            b2 = make_host_batch(name)
+            w2 = DeviceWorkload(b2, args.steps, dev)
+            for i in range(min(args.warmup, w2.nrep)):
+                w2.refresh(i)
+                w2.call(i, torch.cuda.current_stream().cuda_stream)
+            torch.cuda.synchronize()
+            ms2 = time_steps(w2, args.steps, lambda: None)
+            assert not w2.info.cpu().numpy().any()
+            pc = ms2 / args.steps
+            r2 = roofline_entry(name, b2.n, b2.batch, pc, pk, sms)
+            row = {"workload": name, "n": b2.n, "batch": b2.batch, "ms_per_call": pc,
+                   "matrices_per_s": b2.batch / (pc / 1e3),
+                   "gflops": b2.batch * flops_per_matrix(b2.n) / (pc / 1e3) / 1e9,
+                   "roofline": {k: r2[k] for k in ("bound", "frac", "roof_ms")},
+                   "launches_per_call": launches_per_call(b2.n)}
+            if args.cpu_baseline:
+                ob = oracle_rate(b2, 1.0, oracle_sample_size(b2.n))
+                row["oracle_matrices_per_s"] = ob["value"]
+                row["oracle_cores"] = ob["cores"]
+            rows.append(row)
+            del w2
+            torch.cuda.empty_cache()
+        out["per_n"] = rows
+    return out
+
+
+def run_reference(args) -> dict:
+    """The oracle as it stands, timed on the host cores, on the same workload:
+    each step is one pass over a bounded sample of the batch."""
+    import oracle
+    import synth
+    bt = make_host_batch(args.workload)
+    m = oracle_sample_size(bt.n) or bt.batch
+    idx = None if m == bt.batch else list(range(m))
+    th = oracle.default_threads()
+    for _ in range(args.warmup):
+        oracle.potrf_batched(bt.buf, bt.n, bt.lda, bt.strideA, bt.batch, indices=idx, nthreads=th)
+    t0 = time.perf_counter()
+    used = th
+    for _ in range(args.steps):
+        _, _, used = oracle.potrf_batched(bt.buf, bt.n, bt.lda, bt.strideA, bt.batch,
+                                          indices=idx, nthreads=th)
+    dt = time.perf_counter() - t0
+    value = args.steps * m / dt
+    sample = f"{m} of {bt.batch} matrices (n={bt.n}) per step on {used} host threads"
+    w_desc = synth.WORKLOADS[args.workload]
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{args.workload}: n={bt.n}, batch={bt.batch}, lda={bt.lda}, "
+                               f"strideA={bt.strideA}, {w_desc.kind} SPD",
+                   "n": bt.n, "batch": bt.batch, "parallelism": "host threads"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="n64", choices=["n32", "n64", "n128", "n256", "n1024"])
+    ap.add_argument("--soak", type=float, default=1.5, help="untimed seconds before timing")
+    ap.add_argument("--no-per-n", dest="per_n", action="store_false")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    barrier = lambda: None  # noqa: E731
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+        barrier = dist.barrier
+    out = run_ours(args, rank, world, barrier)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

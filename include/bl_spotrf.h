@@ -1,0 +1,120 @@
+/*
+ * bl_spotrf.h - batched single-precision Cholesky factorization (SPOTRF,
+ * uplo = 'L') for many small independent matrices on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation. For each b < batch, the symmetric positive definite matrix
+ * A_b = A + b*strideA (column-major, element (i, j) at A_b[i + j*lda]) is
+ * factored as A_b = L_b L_b^T with L_b lower triangular with a positive
+ * diagonal, and L_b overwrites the lower triangle of A_b in place:
+ *
+ *     d_j  = a_jj - sum_{k<j} l_jk^2,   l_jj = sqrt(d_j),
+ *     l_ij = (a_ij - sum_{k<j} l_ik l_jk) / l_jj          (i > j).
+ *
+ * This is the problem stated by the batched Cholesky leaderboard task of
+ * "kernelbot-cholesky-930185" (its problem statement and the chol_reg /
+ * chol_diag kernel comments; there row-major, a fresh output and a zeroed
+ * upper triangle) and the per-matrix factor of "BatchLAS perf_blackwell"
+ * (potrf rows of its routing table). Here the layout is the LAPACK one:
+ * column-major, strided batch, lower triangle written in place, everything
+ * else untouched.
+ *
+ * info[b] = 0 when every pivot d_j was > 0, else the 1-based index j+1 of the
+ * first pivot with !(d_j > 0) (a NaN pivot fails; +Inf passes). After a
+ * failure at k = info[b] only the leading (k-1) x (k-1) block of L_b is
+ * defined; the rest of that matrix's lower triangle is unspecified.
+ *
+ * All arithmetic is IEEE single precision (contractions into FMA allowed; the
+ * reciprocal square root of the pivot is the hardware approximation).
+ */
+#ifndef BL_SPOTRF_H
+#define BL_SPOTRF_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Largest n the library factors (argument check -7 above it). */
+#define BL_SPOTRF_MAX_N 4096
+
+/* Route numbers of bl_spotrf_batched_ex and bl_spotrf_route. */
+#define BL_ROUTE_AUTO 0
+#define BL_ROUTE_WARP 1     /* K1: one warp (or a 16/8-lane group) per matrix, n <= 32 */
+#define BL_ROUTE_CTA 2      /* K2: one thread block per matrix, shared-memory resident, n <= 128 */
+#define BL_ROUTE_BLOCKED 3  /* K3: right-looking blocked, 128-wide panels: diagonal factor,
+                               panel triangular solve, lower-only trailing update, any n */
+
+/*
+ * bl_spotrf_batched - factor a strided batch in place.
+ *
+ *   A        device pointer to matrix 0 (float, column-major). Only the lower
+ *            triangle (i >= j, i < n) of each matrix is read and written; the
+ *            strict upper triangle, the rows n..lda-1 of every column and the
+ *            memory between matrices are never read or written. Any alignment
+ *            of 4 bytes is accepted; 16-byte alignment of A, lda and strideA
+ *            lets the kernels use vector loads.
+ *   n        order of every matrix (n >= 0).
+ *   lda      leading dimension, lda >= max(1, n).
+ *   strideA  distance in floats between A_b and A_{b+1}; strideA >= lda*n
+ *            when batch > 1 (matrices may not overlap).
+ *   batch    number of matrices (batch >= 0).
+ *   info     device pointer to batch ints, written once per matrix (no
+ *            pre-fill needed).
+ *   stream   CUDA stream the work is enqueued on (0 = the legacy default).
+ *
+ * Ownership: the caller owns A and info (any device allocation, e.g. torch
+ * tensors). The library allocates nothing, keeps no per-call state, does not
+ * synchronize, and is reentrant and safe to call from several host threads
+ * and streams at once. Work on one (A, info) is ordered by `stream`.
+ *
+ * Returns 0 when the work was enqueued; a negative value -i when argument i is
+ * invalid (nothing is enqueued):
+ *   -1 A == NULL while n > 0 and batch > 0     -2 n < 0
+ *   -3 lda < max(1, n)                          -4 batch > 1 and strideA < lda*n
+ *   -5 batch < 0                                -6 info == NULL while batch > 0
+ *   -7 n > BL_SPOTRF_MAX_N
+ * Arguments are checked in the order -2, -5, -3, -4, -1, -6, -7. A positive
+ * value is the cudaError_t of a failed launch. Matrix-level failure (a matrix
+ * that is not positive definite) is reported only through info.
+ * Quick returns: batch == 0 enqueues nothing; n == 0 sets info[b] = 0 for all b.
+ */
+int bl_spotrf_batched(float *A, int n, int lda, int64_t strideA, int batch, int *info,
+                      cudaStream_t stream);
+
+/*
+ * bl_spotrf_batched_ex - as bl_spotrf_batched, with the kernel class forced
+ * (route = BL_ROUTE_*; BL_ROUTE_AUTO selects by n like bl_spotrf_batched).
+ * Returns -8 when the forced route cannot factor this n (WARP: n > 32;
+ * CTA: n > 128), after the checks above. For tests and measurement.
+ */
+int bl_spotrf_batched_ex(float *A, int n, int lda, int64_t strideA, int batch, int *info,
+                         cudaStream_t stream, int route);
+
+/*
+ * bl_spotrf_route - the route bl_spotrf_batched takes for (n, batch). Host
+ * only, needs no GPU. Returns BL_ROUTE_WARP/CTA/BLOCKED, or 0 when nothing
+ * would be launched (n <= 0 or batch <= 0).
+ */
+int bl_spotrf_route(int n, int batch);
+
+/*
+ * bl_spotrf_kernel_info - static resources of the kernel that `route` uses at
+ * order n, as the CUDA runtime reports them (registers per thread, local
+ * memory bytes per thread, static shared bytes, dynamic shared bytes the
+ * launch asks for, threads per block). Any output pointer may be NULL.
+ * Needs a CUDA device. Returns 0, -8 for a route that cannot run n, or a
+ * cudaError_t.
+ */
+int bl_spotrf_kernel_info(int route, int n, int *regs, int *local_bytes, int *static_smem,
+                          int *dynamic_smem, int *threads);
+
+/* Version string of the library ("bl_spotrf <major>.<minor> sm_103a"). */
+const char *bl_spotrf_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BL_SPOTRF_H */

@@ -1,0 +1,135 @@
+"""Batched single-precision Cholesky (SPOTRF, lower) on GB300: Python binding.
+
+A thin ctypes layer over the C-ABI library ``libbl_spotrf.so`` (declared in
+``include/bl_spotrf.h``). It only marshals arguments: every step of the
+factorization runs in the library's CUDA kernels. PyTorch is used for device
+memory and streams. If the library has not been built (see
+``matrix_dense_linear_gb300.build``) every call raises; there is no CPU path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+__all__ = ["ROUTE_AUTO", "ROUTE_WARP", "ROUTE_CTA", "ROUTE_BLOCKED", "MAX_N", "BLError",
+           "library", "library_path", "spotrf_batched", "spotrf_batched_ex", "route",
+           "kernel_info", "version", "factor", "factor_host"]
+
+ROUTE_AUTO, ROUTE_WARP, ROUTE_CTA, ROUTE_BLOCKED = 0, 1, 2, 3
+MAX_N = 4096
+_PKG = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_PKG, "libbl_spotrf.so")
+_lib = None
+
+# (name, restype, argtypes) of every symbol include/bl_spotrf.h declares
+_VP, _I, _I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+SYMBOLS = {
+    "bl_spotrf_batched": (_I, [_VP, _I, _I, _I64, _I, _VP, _VP]),
+    "bl_spotrf_batched_ex": (_I, [_VP, _I, _I, _I64, _I, _VP, _VP, _I]),
+    "bl_spotrf_route": (_I, [_I, _I]),
+    "bl_spotrf_kernel_info": (_I, [_I, _I, _VP, _VP, _VP, _VP, _VP]),
+    "bl_spotrf_version": (ctypes.c_char_p, []),
+}
+
+
+class BLError(RuntimeError):
+    """A nonzero status from the library (negative: bad argument; positive: CUDA error)."""
+
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        kind = f"argument {-code} invalid" if code < 0 else f"cudaError_t {code}"
+        super().__init__(f"bl_spotrf{(' ' + what) if what else ''}: status {code} ({kind})")
+
+
+def library() -> ctypes.CDLL:
+    """Load the C-ABI library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(library_path):
+            raise ImportError(
+                f"{library_path} is missing: build it with "
+                "`python -m matrix_dense_linear_gb300.build` (there is no CPU fallback)")
+        lib = ctypes.CDLL(library_path)
+        for name, (res, args) in SYMBOLS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _ptr(x) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def spotrf_batched(A, n: int, lda: int, strideA: int, batch: int, info, stream=None) -> int:
+    """bl_spotrf_batched: A and info are device tensors (or raw device pointers).
+    Returns the library status (0 = enqueued)."""
+    return library().bl_spotrf_batched(_ptr(A), n, lda, strideA, batch, _ptr(info),
+                                       _stream(stream))
+
+
+def spotrf_batched_ex(A, n: int, lda: int, strideA: int, batch: int, info, stream=None,
+                      route: int = ROUTE_AUTO) -> int:
+    """bl_spotrf_batched_ex: as spotrf_batched with the kernel class forced."""
+    return library().bl_spotrf_batched_ex(_ptr(A), n, lda, strideA, batch, _ptr(info),
+                                          _stream(stream), route)
+
+
+def route(n: int, batch: int) -> int:
+    """bl_spotrf_route: the kernel class chosen for (n, batch); needs no GPU."""
+    return library().bl_spotrf_route(n, batch)
+
+
+def kernel_info(route_: int, n: int) -> dict:
+    """bl_spotrf_kernel_info: registers, local bytes, shared bytes, threads."""
+    vals = [ctypes.c_int(0) for _ in range(5)]
+    code = library().bl_spotrf_kernel_info(route_, n, *[ctypes.byref(v) for v in vals])
+    if code:
+        raise BLError(code, "kernel_info")
+    keys = ["regs", "local_bytes", "static_smem", "dynamic_smem", "threads"]
+    return {k: v.value for k, v in zip(keys, vals)}
+
+
+def version() -> str:
+    return library().bl_spotrf_version().decode()
+
+
+def factor(A, n: int, lda: int, strideA: int, batch: int, info, stream=None,
+           route_: int = ROUTE_AUTO) -> None:
+    """Factor in place on the device; raises BLError on a nonzero status."""
+    code = spotrf_batched_ex(A, n, lda, strideA, batch, info, stream, route_)
+    if code:
+        raise BLError(code)
+
+
+def factor_host(A_host, n: int, lda: int, strideA: int, batch: int, info_host,
+                A_dev=None, info_dev=None, stream=None) -> None:
+    """Factor a batch that lives in (pinned) host memory: copy it to the device,
+    factor it there, copy the matrices and info back, all on one stream. The
+    device buffers are the caller's if given, else allocated by torch."""
+    import torch
+    st = torch.cuda.current_stream() if stream is None else stream
+    with torch.cuda.stream(st):
+        if A_dev is None:
+            A_dev = torch.empty_like(A_host, device="cuda")
+        if info_dev is None:
+            info_dev = torch.empty_like(info_host, device="cuda")
+        A_dev.copy_(A_host, non_blocking=True)
+        factor(A_dev, n, lda, strideA, batch, info_dev, st)
+        A_host.copy_(A_dev, non_blocking=True)
+        info_host.copy_(info_dev, non_blocking=True)

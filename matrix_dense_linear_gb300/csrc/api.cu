@@ -1,0 +1,125 @@
+// C-ABI of libbl_spotrf: argument checks, the size-keyed route selector and
+// the quick returns. Declarations and the contract are in include/bl_spotrf.h.
+#include <cstdio>
+#include <cstdlib>
+#include <mutex>
+
+#include "../../include/bl_spotrf.h"
+#include "bl_common.cuh"
+
+namespace {
+
+// Size thresholds of the selector. The pages route by order the same way
+// (one warp per matrix up to n = 32, one work-group per matrix in the middle,
+// blocked above: "BatchLAS perf_blackwell", potrf row of its routing table;
+// the size router of "kernelbot-cholesky-930185").
+constexpr int kWarpMaxN = 32;
+constexpr int kCtaMaxN = 128;
+
+bool trace_enabled()
+{
+    static std::once_flag once;
+    static bool on = false;
+    std::call_once(once, [] {
+        const char *v = std::getenv("BL_TRACE");
+        on = v && *v && *v != '0';
+    });
+    return on;
+}
+
+int check_args(const float *A, int n, int lda, int64_t strideA, int batch, const int *info)
+{
+    if (n < 0) return -2;
+    if (batch < 0) return -5;
+    if (lda < (n > 1 ? n : 1)) return -3;
+    if (batch > 1 && strideA < (int64_t)lda * n) return -4;
+    if (A == nullptr && n > 0 && batch > 0) return -1;
+    if (info == nullptr && batch > 0) return -6;
+    if (n > BL_SPOTRF_MAX_N) return -7;
+    return 0;
+}
+
+int route_for(int n)
+{
+    if (n <= kWarpMaxN) return BL_ROUTE_WARP;
+    if (n <= kCtaMaxN) return BL_ROUTE_CTA;
+    return BL_ROUTE_BLOCKED;
+}
+
+bool route_can_run(int route, int n)
+{
+    switch (route) {
+    case BL_ROUTE_WARP: return n <= kWarpMaxN;
+    case BL_ROUTE_CTA: return n <= kCtaMaxN;
+    case BL_ROUTE_BLOCKED: return true;
+    default: return false;
+    }
+}
+
+int run(float *A, int n, int lda, int64_t strideA, int batch, int *info, cudaStream_t stream,
+        int route)
+{
+    int e = check_args(A, n, lda, strideA, batch, info);
+    if (e) return e;
+    if (route == BL_ROUTE_AUTO) route = route_for(n);
+    if (!route_can_run(route, n)) return -8;
+    if (batch == 0) return 0;
+    if (n == 0) return (int)cudaMemsetAsync(info, 0, sizeof(int) * (size_t)batch, stream);
+    if (trace_enabled())
+        std::fprintf(stderr, "bl_spotrf: n=%d lda=%d strideA=%lld batch=%d route=%d\n", n, lda,
+                     (long long)strideA, batch, route);
+    switch (route) {
+    case BL_ROUTE_WARP: return bl::launch_warp(A, n, lda, strideA, batch, info, stream);
+    case BL_ROUTE_CTA:
+        return bl::launch_cta(A, n, lda, strideA, batch, info, stream, bl::InfoMode{-1});
+    default: return bl::launch_blocked(A, n, lda, strideA, batch, info, stream);
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+int bl_spotrf_batched(float *A, int n, int lda, int64_t strideA, int batch, int *info,
+                      cudaStream_t stream)
+{
+    return run(A, n, lda, strideA, batch, info, stream, BL_ROUTE_AUTO);
+}
+
+int bl_spotrf_batched_ex(float *A, int n, int lda, int64_t strideA, int batch, int *info,
+                         cudaStream_t stream, int route)
+{
+    if (route < BL_ROUTE_AUTO || route > BL_ROUTE_BLOCKED) return -8;
+    return run(A, n, lda, strideA, batch, info, stream, route);
+}
+
+int bl_spotrf_route(int n, int batch)
+{
+    if (n <= 0 || batch <= 0) return 0;
+    return route_for(n);
+}
+
+int bl_spotrf_kernel_info(int route, int n, int *regs, int *local_bytes, int *static_smem,
+                          int *dynamic_smem, int *threads)
+{
+    if (route == BL_ROUTE_AUTO) route = route_for(n);
+    if (n < 1 || !route_can_run(route, n)) return -8;
+    cudaFuncAttributes fa{};
+    int th = 0, dyn = 0, e;
+    switch (route) {
+    case BL_ROUTE_WARP: e = bl::attrs_warp(n, &fa, &th, &dyn); break;
+    case BL_ROUTE_CTA: e = bl::attrs_cta(n, &fa, &th, &dyn); break;
+    default: e = bl::attrs_blocked(n, &fa, &th, &dyn); break;
+    }
+    if (e) return e;
+    if (regs) *regs = fa.numRegs;
+    if (local_bytes) *local_bytes = (int)fa.localSizeBytes;
+    if (static_smem) *static_smem = (int)fa.sharedSizeBytes;
+    if (dynamic_smem) *dynamic_smem = dyn;
+    if (threads) *threads = th;
+    return 0;
+}
+
+const char *bl_spotrf_version(void) { return "bl_spotrf 0.1 sm_103a"; }
+
+}  // extern "C"

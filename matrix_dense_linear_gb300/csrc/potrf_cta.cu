@@ -1,0 +1,274 @@
+// K2: batched SPOTRF for n <= 128, one thread block per matrix, the lower
+// triangle resident in shared memory for the whole factorization.
+//
+// Storage. The padded order NP = 32*NB is split into NB block columns
+// ("panels") of 32 columns. Panel p keeps only its rows 32p .. NP-1, as a
+// column-major (NP-32p) x 32 rectangle with leading dimension NP-32p+4 (the
+// +4 keeps 16-byte alignment and shifts banks between columns). The whole
+// lower triangle then costs NP(NP+32)/2 floats: 43 KB at n = 128.
+//
+// Schedule (right-looking, one panel per step, after the inner-blocked
+// schedule of "kernelbot-cholesky-930185", chol_diag_b kernel comment: the
+// barriers, not the FMAs, are the critical path, so spend work to save them):
+//   1. warp 0 factors the 32 x 32 diagonal block alone, lane = row, with the
+//      same broadcast-column step as K1 (no block barrier inside);
+//   2. every thread solves one row of the panel below it against that block,
+//      P <- P L11^{-T}, reading L11's columns as 16-byte broadcasts
+//      (the trsm_panel kernel of the same page: one thread per row);
+//   3. every thread updates 4 x 4 tiles of the trailing LOWER triangle only,
+//      A22 <- A22 - L21 L21^T (the page's left-looking driver note measured a
+//      full-square trailing update as doubling the flops);
+// with one __syncthreads after each phase. Rows and columns n .. NP-1 are an
+// identity block. Entries above the diagonal inside a diagonal block of the
+// storage are scratch: they are never read into a lower result or stored.
+#include <mutex>
+
+#include "bl_common.cuh"
+
+namespace bl {
+namespace {
+
+constexpr int kPad = 4;
+
+template <int NB>
+struct CtaGeom {
+    static constexpr int NP = 32 * NB;
+    __host__ __device__ static constexpr int ld(int p) { return NP - 32 * p + kPad; }
+    __host__ __device__ static constexpr int off(int p) {
+        // sum_{q<p} 32 * ld(q)
+        return 32 * (p * (NP + kPad) - 32 * (p * (p - 1) / 2));
+    }
+    static constexpr int floats = off(NB);
+    static constexpr int bytes = floats * 4;
+};
+
+template <int NB>
+__device__ __forceinline__ float *elem_ptr(float *S, int i, int k)
+{
+    // address of element (i, k), i >= 32*(k/32), in the packed storage
+    using Gm = CtaGeom<NB>;
+    const int p = k >> 5;
+    return S + Gm::off(p) + (i - 32 * p) + (k - 32 * p) * Gm::ld(p);
+}
+
+// Step 1: factor the diagonal block of panel p in warp 0. P points at element
+// (c0, c0); ldp is the panel's leading dimension. Writes s_j = rsqrt(d_j) to
+// sinv and the first failing local pivot (c0 + j + 1) to *fail_out.
+__device__ __forceinline__ void factor_diag_block(float *P, int ldp, int lane, int c0, int n,
+                                                  float (*colbuf)[32], float *sinv,
+                                                  int *fail_out)
+{
+    float r[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) r[k] = P[lane + k * ldp];
+    int fail = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        if (c0 + j >= n) break;
+        float *cb = colbuf[j & 1];
+        cb[lane] = r[j];
+        __syncwarp();
+        const float d = cb[j];
+        if (!pivot_ok(d) && fail == 0) fail = c0 + j + 1;
+        const float s = rsqrt_approx(d);
+        const float lij = r[j] * s;
+        const float w = lij * s;
+        r[j] = (lane == j) ? sqrt_approx(d) : lij;
+        if (lane == j) sinv[j] = s;
+#pragma unroll
+        for (int q = (j + 1) / 4; q < 8; ++q) {
+            const float4 c4 = reinterpret_cast<const float4 *>(cb)[q];
+            const float cv[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int k = 4 * q + t;
+                if (k > j) r[k] = fmaf(-w, cv[t], r[k]);
+            }
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+        if (k <= lane) P[lane + k * ldp] = r[k];
+    if (lane == 0 && fail) *fail_out = fail;
+}
+
+// Step 2: row a (>= 32, panel coordinates) of panel p: x <- x L11^{-T}.
+__device__ __forceinline__ void trsm_row(float *P, int ldp, int a, const float *sinv)
+{
+    float x[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) x[k] = P[a + k * ldp];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        x[j] *= sinv[j];
+        const float *Lj = P + j * ldp;  // column j of L11, rows 0..31
+#pragma unroll
+        for (int q = (j + 1) / 4; q < 8; ++q) {
+            const float4 l4 = reinterpret_cast<const float4 *>(Lj)[q];
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int k = 4 * q + t;
+                if (k > j) x[k] = fmaf(-x[j], lv[t], x[k]);
+            }
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 32; ++k) P[a + k * ldp] = x[k];
+}
+
+// Step 3: one 4 x 4 tile (I, K), I >= K, of the trailing lower triangle that
+// starts at c1 = c0 + 32; L21 is panel p's rows c1.. .
+template <int NB>
+__device__ __forceinline__ void syrk_tile(float *S, const float *P, int ldp, int c0, int c1,
+                                          int I, int K)
+{
+    using Gm = CtaGeom<NB>;
+    const int gi = c1 + 4 * I, gk = c1 + 4 * K;
+    const int q = gk >> 5;
+    const int ldq = Gm::ld(q);
+    float *C = S + Gm::off(q) + (gi - 32 * q) + (gk - 32 * q) * ldq;
+    float acc[4][4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const float4 c4 = *reinterpret_cast<const float4 *>(C + b * ldq);
+        acc[b][0] = c4.x; acc[b][1] = c4.y; acc[b][2] = c4.z; acc[b][3] = c4.w;
+    }
+    const float *Li = P + (gi - c0);
+    const float *Lk = P + (gk - c0);
+#pragma unroll 8
+    for (int k = 0; k < 32; ++k) {
+        const float4 a4 = *reinterpret_cast<const float4 *>(Li + k * ldp);
+        const float4 b4 = *reinterpret_cast<const float4 *>(Lk + k * ldp);
+        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+        const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+#pragma unroll
+            for (int a = 0; a < 4; ++a) acc[b][a] = fmaf(-av[a], bv[b], acc[b][a]);
+    }
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+        *reinterpret_cast<float4 *>(C + b * ldq) =
+            make_float4(acc[b][0], acc[b][1], acc[b][2], acc[b][3]);
+}
+
+__device__ __forceinline__ void tri_index(int t, int &I, int &K)
+{
+    int i = (int)((sqrtf(8.0f * (float)t + 1.0f) - 1.0f) * 0.5f);
+    while ((i + 1) * (i + 2) / 2 <= t) ++i;
+    while (i * (i + 1) / 2 > t) --i;
+    I = i;
+    K = t - i * (i + 1) / 2;
+}
+
+template <int NB, int NT>
+__global__ void __launch_bounds__(NT)
+potrf_cta_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int batch,
+                 int *__restrict__ info, int info_off)
+{
+    using Gm = CtaGeom<NB>;
+    constexpr int NP = Gm::NP;
+    extern __shared__ __align__(16) float S[];
+    __shared__ __align__(16) float colbuf[2][32];
+    __shared__ __align__(16) float sinv[32];
+    __shared__ int sh_fail;
+
+    const int64_t mat = blockIdx.x;
+    if (info_off >= 0 && info[mat] != 0) return;  // failed at an earlier panel
+    float *__restrict__ Ab = A + mat * strideA;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) sh_fail = 0;
+
+    // load: column k by one warp, rows k .. NP-1 (identity beyond n)
+    for (int k = warp; k < NP; k += NT / 32) {
+        float *col = elem_ptr<NB>(S, 0, k);  // col[i] = element (i, k)
+        for (int i = k + lane; i < NP; i += 32) {
+            float v = (i == k) ? 1.0f : 0.0f;
+            if (i < n) v = Ab[i + (int64_t)k * lda];
+            col[i] = v;
+        }
+    }
+    __syncthreads();
+
+#pragma unroll 1
+    for (int p = 0; p < NB; ++p) {
+        const int c0 = 32 * p;
+        if (c0 >= n) break;
+        float *P = S + Gm::off(p);
+        const int ldp = Gm::ld(p);
+        if (warp == 0) factor_diag_block(P, ldp, lane, c0, n, colbuf, sinv, &sh_fail);
+        __syncthreads();
+        if (sh_fail) break;
+        const int c1 = c0 + 32;
+        if (c1 >= n) break;
+        for (int a = 32 + tid; a < NP - c0; a += NT) trsm_row(P, ldp, a, sinv);
+        __syncthreads();
+        const int T = (NP - c1) / 4;
+        const int ntiles = T * (T + 1) / 2;
+        for (int t = tid; t < ntiles; t += NT) {
+            int I, K;
+            tri_index(t, I, K);
+            if (c1 + 4 * K < n) syrk_tile<NB>(S, P, ldp, c0, c1, I, K);
+        }
+        __syncthreads();
+    }
+
+    // store the lower triangle, rows < n only
+    for (int k = warp; k < n; k += NT / 32) {
+        const float *col = elem_ptr<NB>(S, 0, k);
+        for (int i = k + lane; i < n; i += 32) Ab[i + (int64_t)k * lda] = col[i];
+    }
+    if (tid == 0) {
+        const int f = sh_fail;
+        if (info_off < 0) info[mat] = f;
+        else if (f) info[mat] = info_off + f;
+    }
+}
+
+template <int NB, int NT>
+int launch_nb(float *A, int n, int lda, int64_t strideA, int batch, int *info, cudaStream_t st,
+              int info_off)
+{
+    constexpr int bytes = CtaGeom<NB>::bytes;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(potrf_cta_kernel<NB, NT>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    });
+    if (attr_err != cudaSuccess) return (int)attr_err;
+    potrf_cta_kernel<NB, NT><<<(unsigned)batch, NT, bytes, st>>>(A, n, lda, strideA, batch, info,
+                                                                 info_off);
+    return (int)cudaGetLastError();
+}
+
+template <int NB, int NT>
+int attrs_nb(cudaFuncAttributes *fa, int *threads, int *dyn)
+{
+    *threads = NT;
+    *dyn = CtaGeom<NB>::bytes;
+    return (int)cudaFuncGetAttributes(fa, potrf_cta_kernel<NB, NT>);
+}
+
+}  // namespace
+
+int launch_cta(float *A, int n, int lda, int64_t strideA, int batch, int *info,
+               cudaStream_t stream, InfoMode mode)
+{
+    if (n <= 32) return launch_nb<1, 32>(A, n, lda, strideA, batch, info, stream, mode.off);
+    if (n <= 64) return launch_nb<2, 64>(A, n, lda, strideA, batch, info, stream, mode.off);
+    if (n <= 96) return launch_nb<3, 128>(A, n, lda, strideA, batch, info, stream, mode.off);
+    return launch_nb<4, 128>(A, n, lda, strideA, batch, info, stream, mode.off);
+}
+
+int attrs_cta(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem)
+{
+    if (n <= 32) return attrs_nb<1, 32>(fa, threads, dyn_smem);
+    if (n <= 64) return attrs_nb<2, 64>(fa, threads, dyn_smem);
+    if (n <= 96) return attrs_nb<3, 128>(fa, threads, dyn_smem);
+    return attrs_nb<4, 128>(fa, threads, dyn_smem);
+}
+
+}  // namespace bl

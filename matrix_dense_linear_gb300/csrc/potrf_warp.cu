@@ -1,0 +1,119 @@
+// K1: batched SPOTRF for n <= 32, one group of N lanes per matrix (N = 32, 16
+// or 8, so one warp factors 1, 2 or 4 matrices), the matrix in registers.
+//
+// Lane `row` of a group holds row `row` of its matrix, r[k] = a(row, k). The
+// factorization is right-looking: at column j every lane publishes its current
+// r[j] to a warp-private shared buffer, one __syncwarp, and every lane reads
+// the pivot d_j and the column below it back as 16-byte broadcast loads. The
+// pages measured this broadcast against shuffle chains and found the shuffles
+// stalled on the MIO queue ("kernelbot-cholesky-930185", exp_s6 header, "THE
+// SECOND FIX: n=32's SHUFFLES"); the buffer is double-buffered so no second
+// sync is needed before the next column overwrites it.
+//
+// Per column, with s = rsqrt(d_j) and c_i = r[j] of lane i:
+//   l_ij = c_i * s,  and for k > j:  r[k] -= (l_ij * s) * c_k      (= l_ij l_kj)
+// so the broadcast column is read unscaled and no lane has to wait for another
+// lane's scaling (one pre-scaled factor per lane instead of per entry).
+//
+// Rows and columns n .. N-1 of the register tile are an identity block, so the
+// same unrolled code factors any n <= N. Lanes compute the whole row including
+// the strict upper triangle of the register tile: values there are never read
+// into a lower-triangle result and never stored.
+#include "bl_common.cuh"
+
+namespace bl {
+namespace {
+
+constexpr int kWarpsPerBlock = 4;
+
+template <int N>
+__global__ void __launch_bounds__(32 * kWarpsPerBlock)
+potrf_warp_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int batch,
+                  int *__restrict__ info)
+{
+    constexpr int G = 32 / N;  // matrices per warp
+    __shared__ __align__(16) float colbuf[kWarpsPerBlock][2][32];
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int grp = lane / N;
+    const int row = lane - grp * N;
+    const int64_t mat = ((int64_t)blockIdx.x * kWarpsPerBlock + warp) * G + grp;
+    const bool valid = mat < batch;
+    const bool live = valid && row < n;
+    float *__restrict__ Ab = A + (valid ? mat * strideA : 0);
+
+    float r[N];
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+        float v = (row == k) ? 1.0f : 0.0f;
+        if (live && k <= row) v = Ab[row + (int64_t)k * lda];
+        r[k] = v;
+    }
+
+    int fail = 0;
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+        if (j >= n) break;  // same n for every lane: uniform
+        float *cb = colbuf[warp][j & 1];
+        cb[lane] = r[j];
+        __syncwarp();
+        const float *col = cb + grp * N;
+        const float d = col[j];
+        if (!pivot_ok(d) && fail == 0) fail = j + 1;
+        const float s = rsqrt_approx(d);
+        const float lij = r[j] * s;
+        const float w = lij * s;
+        r[j] = (row == j) ? sqrt_approx(d) : lij;
+        // columns j+1 .. N-1 of the broadcast column, read 4 at a time
+#pragma unroll
+        for (int q = (j + 1) / 4; q < N / 4; ++q) {
+            const float4 c4 = reinterpret_cast<const float4 *>(col)[q];
+            const float cv[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int k = 4 * q + t;
+                if (k > j) r[k] = fmaf(-w, cv[t], r[k]);
+            }
+        }
+    }
+
+#pragma unroll
+    for (int k = 0; k < N; ++k)
+        if (live && k <= row) Ab[row + (int64_t)k * lda] = r[k];
+    if (valid && row == 0) info[mat] = fail;
+}
+
+template <int N>
+int launch_n(float *A, int n, int lda, int64_t strideA, int batch, int *info, cudaStream_t st)
+{
+    constexpr int G = 32 / N;
+    const int64_t per_block = (int64_t)kWarpsPerBlock * G;
+    const int64_t blocks = (batch + per_block - 1) / per_block;
+    potrf_warp_kernel<N><<<(unsigned)blocks, 32 * kWarpsPerBlock, 0, st>>>(A, n, lda, strideA,
+                                                                           batch, info);
+    return (int)cudaGetLastError();
+}
+
+}  // namespace
+
+int launch_warp(float *A, int n, int lda, int64_t strideA, int batch, int *info,
+                cudaStream_t stream)
+{
+    if (n <= 8) return launch_n<8>(A, n, lda, strideA, batch, info, stream);
+    if (n <= 16) return launch_n<16>(A, n, lda, strideA, batch, info, stream);
+    return launch_n<32>(A, n, lda, strideA, batch, info, stream);
+}
+
+int attrs_warp(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem)
+{
+    cudaError_t e;
+    if (n <= 8) e = cudaFuncGetAttributes(fa, potrf_warp_kernel<8>);
+    else if (n <= 16) e = cudaFuncGetAttributes(fa, potrf_warp_kernel<16>);
+    else e = cudaFuncGetAttributes(fa, potrf_warp_kernel<32>);
+    *threads = 32 * kWarpsPerBlock;
+    *dyn_smem = 0;
+    return (int)e;
+}
+
+}  // namespace bl

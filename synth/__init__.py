@@ -205,14 +205,19 @@ class Batch:
 
 def pack(mats: Callable[[int], np.ndarray] | np.ndarray, n: int, batch: int, *,
          lda: Optional[int] = None, strideA: Optional[int] = None,
-         fill: str = "mirror", pad_value: float = 0.0, offset: int = 0) -> Batch:
+         fill: str = "mirror", pad_value: float = 0.0, offset: int = 0,
+         workers: Optional[int] = None) -> Batch:
     """Round each matrix once to float32 and lay the batch out column-major.
 
     ``mats`` is an array (batch, n, n) or a function b -> n x n float64 matrix.
     Only the lower triangle of each matrix is used; ``fill`` says what goes
     everywhere else (see the module docstring). ``offset`` floats of fill are
-    put in front of matrix 0 (to misalign the base address).
+    put in front of matrix 0 (to misalign the base address). Matrices are made
+    on ``workers`` threads (default: one per core); each writes its own slot.
     """
+    import concurrent.futures as cf
+    import os
+
     lda = n if lda is None else lda
     strideA = lda * n if strideA is None else strideA
     size = offset + buffer_size(n, lda, strideA, batch)
@@ -224,15 +229,25 @@ def pack(mats: Callable[[int], np.ndarray] | np.ndarray, n: int, batch: int, *,
     core = buf[offset:]
     v = strided_view(core, n, lda, strideA, batch)
     tri = np.tril(np.ones((n, n), dtype=bool))
-    for b in range(batch):
+
+    def one(b: int) -> None:
         m = mats(b) if callable(mats) else mats[b]
         m32 = np.asarray(m).astype(F32)
-        low = np.where(tri, m32, F32(0))
         if fill == "mirror":
-            blk = low + np.tril(low, -1).T
+            if not np.array_equal(m32, m32.T):
+                low = np.where(tri, m32, F32(0))
+                m32 = low + np.tril(low, -1).T
+            v[b] = m32
         else:
-            blk = np.where(tri, m32, outside)
-        v[b] = blk
+            v[b] = np.where(tri, m32, outside)
+
+    nw = workers if workers is not None else min(32, os.cpu_count() or 1)
+    if nw <= 1 or batch < 4:
+        for b in range(batch):
+            one(b)
+    else:
+        with cf.ThreadPoolExecutor(max_workers=nw) as ex:
+            list(ex.map(one, range(batch)))
     out = Batch(core, n, lda, strideA, batch, fill)
     out.base = buf  # type: ignore[attr-defined]
     return out

@@ -1,0 +1,117 @@
+"""The C-ABI library builds, loads and exports what include/*.h declares; the
+host-side logic (argument checks, quick returns, route selection) works without
+a GPU; every kernel compiles with no stack frame and no spills (CPU only)."""
+from __future__ import annotations
+
+import glob
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+pytestmark = pytest.mark.skipif(
+    shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"),
+    reason="nvcc not available")
+
+
+@pytest.fixture(scope="module")
+def bl():
+    from matrix_dense_linear_gb300 import build
+    build.build()
+    import matrix_dense_linear_gb300 as bl
+    bl.library()
+    return bl
+
+
+def _declared_functions() -> set[str]:
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names.update(re.findall(r"\b(bl_\w+)\s*\(", text))
+    return names
+
+
+def test_every_declared_symbol_is_exported(bl):
+    declared = _declared_functions()
+    assert "bl_spotrf_batched" in declared and "bl_spotrf_batched_ex" in declared
+    lib = bl.library()
+    for name in declared:
+        assert hasattr(lib, name), f"{name} declared but not exported"
+    assert declared == set(bl.SYMBOLS), "binding and header disagree"
+
+
+def test_version(bl):
+    assert bl.version().startswith("bl_spotrf ") and "sm_103a" in bl.version()
+
+
+@pytest.mark.parametrize("args,code", [
+    # (A, n, lda, strideA, batch, info) -> status; no call below reaches the GPU
+    ((8, -1, 1, 1, 1, 8), -2),
+    ((8, 4, 4, 16, -1, 8), -5),
+    ((8, 4, 3, 16, 2, 8), -3),
+    ((8, 0, 0, 0, 1, 8), -3),
+    ((8, 4, 4, 15, 2, 8), -4),
+    ((8, 4, 4, -16, 2, 8), -4),
+    ((None, 4, 4, 16, 2, 8), -1),
+    ((8, 4, 4, 16, 2, None), -6),
+    ((8, 4097, 4097, 4097 * 4097, 2, 8), -7),
+    ((None, 4, 4, 16, 0, None), 0),   # batch == 0: nothing to do
+])
+def test_argument_checks(bl, args, code):
+    A, n, lda, sA, batch, info = args
+    lib = bl.library()
+    if code is None:
+        return
+    assert lib.bl_spotrf_batched(A, n, lda, sA, batch, info, None) == code
+    assert lib.bl_spotrf_batched_ex(A, n, lda, sA, batch, info, None, 0) == code
+
+
+def test_check_order(bl):
+    lib = bl.library()
+    # n < 0 wins over everything; then batch < 0; then lda
+    assert lib.bl_spotrf_batched(None, -1, 0, 0, -1, None, None) == -2
+    assert lib.bl_spotrf_batched(None, 4, 0, 0, -1, None, None) == -5
+    assert lib.bl_spotrf_batched(None, 4, 1, 0, 2, None, None) == -3
+    assert lib.bl_spotrf_batched(None, 4, 4, 1, 2, None, None) == -4
+
+
+def test_forced_route_that_cannot_run(bl):
+    lib = bl.library()
+    assert lib.bl_spotrf_batched_ex(8, 33, 33, 33 * 33, 1, 8, None, bl.ROUTE_WARP) == -8
+    assert lib.bl_spotrf_batched_ex(8, 129, 129, 129 * 129, 1, 8, None, bl.ROUTE_CTA) == -8
+    assert lib.bl_spotrf_batched_ex(8, 4, 4, 16, 1, 8, None, 9) == -8
+    assert lib.bl_spotrf_batched_ex(8, 4, 4, 16, 1, 8, None, -1) == -8
+    # argument errors come first
+    assert lib.bl_spotrf_batched_ex(8, 33, 32, 33 * 33, 1, 8, None, bl.ROUTE_WARP) == -3
+
+
+def test_route_selection(bl):
+    assert bl.route(0, 5) == 0 and bl.route(5, 0) == 0
+    for n in (1, 8, 9, 16, 17, 32):
+        assert bl.route(n, 1024) == bl.ROUTE_WARP
+    for n in (33, 64, 65, 128):
+        assert bl.route(n, 1024) == bl.ROUTE_CTA
+    for n in (129, 256, 1024, 4096):
+        assert bl.route(n, 512) == bl.ROUTE_BLOCKED
+
+
+def test_no_stack_no_spill(bl):
+    from matrix_dense_linear_gb300 import build
+    rep = build.ptxas_report()
+    funcs = re.findall(r"Function properties for (\S+)\n\s*(\d+) bytes stack frame, "
+                       r"(\d+) bytes spill stores, (\d+) bytes spill loads", rep)
+    assert len(funcs) >= 6, rep[:2000]
+    for name, stack, st, ld in funcs:
+        assert (int(stack), int(st), int(ld)) == (0, 0, 0), f"{name}: stack/spill {stack}/{st}/{ld}"
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    import matrix_dense_linear_gb300 as bl
+    monkeypatch.setattr(bl, "library_path", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(bl, "_lib", None)
+    with pytest.raises(ImportError):
+        bl.library()
