@@ -74,6 +74,8 @@ def launches_per_call(n: int) -> int:
 def dominant_kernel(n: int) -> str:
     if n <= 32:
         return "potrf_warp_kernel"
+    if n <= 64:
+        return "potrf_warp64_kernel"
     if n <= 128:
         return "potrf_cta_kernel"
     return "syrk_tile_kernel"
@@ -81,7 +83,7 @@ def dominant_kernel(n: int) -> str:
 
 def kernel_source(n: int) -> str:
     d = os.path.join(ROOT, "matrix_dense_linear_gb300", "csrc")
-    if n <= 32:
+    if n <= 64:
         return os.path.join(d, "potrf_warp.cu")
     if n <= 128:
         return os.path.join(d, "potrf_cta.cu")
@@ -164,9 +166,9 @@ class ClockSampler:
                 "power_w_max": max(pw) if pw else None}
 
 
-def make_host_batch(name: str):
+def make_host_batch(name: str, batch: int | None = None):
     import synth
-    return synth.workload_batch(name, fill="mirror", include_info=False)
+    return synth.workload_batch(name, fill="mirror", include_info=False, batch=batch)
 
 
 class DeviceWorkload:
@@ -203,15 +205,25 @@ class DeviceWorkload:
             raise bl.BLError(code)
 
 
-def time_steps(w: DeviceWorkload, steps: int, barrier) -> float:
+def time_steps(w: DeviceWorkload, steps: int, barrier, graph: bool = True) -> float:
     """Device time (ms) of exactly `steps` calls, each on a fresh replica; the
-    replicas are refreshed and the L2 flushed outside the timed intervals."""
+    replicas are refreshed and the L2 flushed outside the timed intervals.
+    With `graph`, the calls of a chunk are captured once into a CUDA graph and
+    the graph's replay is timed (device time without host launch overhead);
+    otherwise the calls are launched one by one from Python."""
     import torch
     st = torch.cuda.current_stream()
     total = 0.0
     done = 0
     while done < steps:
         chunk = min(w.nrep, steps - done)
+        g = None
+        if graph:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                cs = torch.cuda.current_stream().cuda_stream
+                for i in range(chunk):
+                    w.call(i, cs)
         w.refresh()
         w.flush_l2()
         torch.cuda.synchronize()
@@ -219,13 +231,17 @@ def time_steps(w: DeviceWorkload, steps: int, barrier) -> float:
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(st)
-        for i in range(chunk):
-            w.call(i, st.cuda_stream)
+        if g is not None:
+            g.replay()
+        else:
+            for i in range(chunk):
+                w.call(i, st.cuda_stream)
         e1.record(st)
         torch.cuda.synchronize()
         barrier()
         total += e0.elapsed_time(e1)
         done += chunk
+        del g
     return total
 
 
@@ -331,7 +347,7 @@ def run_ours(args, rank: int, world: int, barrier) -> dict | None:
     import synth
     w_desc = synth.WORKLOADS[args.workload]
 
-    bt = make_host_batch(args.workload)
+    bt = make_host_batch(args.workload, args.batch)
     w = DeviceWorkload(bt, args.steps, dev)
     for i in range(args.warmup):
         w.refresh(i % w.nrep)
@@ -342,6 +358,7 @@ def run_ours(args, rank: int, world: int, barrier) -> dict | None:
     t_s0 = time.time()
     soak(w, args.soak)
     ms = time_steps(w, args.steps, barrier)
+    ms_direct = time_steps(w, args.steps, barrier, graph=False)
     soak(w, 0.5)
     t_s1 = time.time()
     if sampler:
@@ -382,6 +399,7 @@ def run_ours(args, rank: int, world: int, barrier) -> dict | None:
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": per_call, "higher_is_better": True,
+        "ms_per_step_direct_launch": ms_direct / args.steps,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "gflops": value * flops_per_matrix(n) / 1e9,
         "config": {"workload": f"{args.workload}: n={n}, batch={batch}, lda={bt.lda}, "
@@ -390,6 +408,7 @@ def run_ours(args, rank: int, world: int, barrier) -> dict | None:
                    "route": bl.route(n, batch),
                    "l2": "flushed before each timed chunk; every step factors its own "
                          "replica, untouched since the flush",
+                   "timing": "CUDA events around the replay of a CUDA graph of the K calls",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roof,
         "e2e": {"value": world * batch * args.steps / (e2e["ms"] / 1e3), "unit": UNIT,
@@ -445,7 +464,7 @@ def run_reference(args) -> dict:
     each step is one pass over a bounded sample of the batch."""
     import oracle
     import synth
-    bt = make_host_batch(args.workload)
+    bt = make_host_batch(args.workload, args.batch)
     m = oracle_sample_size(bt.n) or bt.batch
     idx = None if m == bt.batch else list(range(m))
     th = oracle.default_threads()
@@ -482,6 +501,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="n64", choices=["n32", "n64", "n128", "n256", "n1024"])
     ap.add_argument("--soak", type=float, default=1.5, help="untimed seconds before timing")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="factor only the first B matrices of the workload (profiling)")
     ap.add_argument("--no-per-n", dest="per_n", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     args = ap.parse_args()

@@ -41,7 +41,7 @@ extern "C" {
 
 /* Route numbers of bl_spotrf_batched_ex and bl_spotrf_route. */
 #define BL_ROUTE_AUTO 0
-#define BL_ROUTE_WARP 1     /* K1: one warp (or a 16/8-lane group) per matrix, n <= 32 */
+#define BL_ROUTE_WARP 1     /* K1: one warp (or a 16/8-lane group) per matrix, n <= 64 */
 #define BL_ROUTE_CTA 2      /* K2: one thread block per matrix, shared-memory resident, n <= 128 */
 #define BL_ROUTE_BLOCKED 3  /* K3: right-looking blocked, 128-wide panels: diagonal factor,
                                panel triangular solve, lower-only trailing update, any n */
@@ -86,7 +86,7 @@ int bl_spotrf_batched(float *A, int n, int lda, int64_t strideA, int batch, int 
 /*
  * bl_spotrf_batched_ex - as bl_spotrf_batched, with the kernel class forced
  * (route = BL_ROUTE_*; BL_ROUTE_AUTO selects by n like bl_spotrf_batched).
- * Returns -8 when the forced route cannot factor this n (WARP: n > 32;
+ * Returns -8 when the forced route cannot factor this n (WARP: n > 64;
  * CTA: n > 128), after the checks above. For tests and measurement.
  */
 int bl_spotrf_batched_ex(float *A, int n, int lda, int64_t strideA, int batch, int *info,

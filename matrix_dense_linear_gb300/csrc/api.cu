@@ -13,7 +13,7 @@ namespace {
 // (one warp per matrix up to n = 32, one work-group per matrix in the middle,
 // blocked above: "BatchLAS perf_blackwell", potrf row of its routing table;
 // the size router of "kernelbot-cholesky-930185").
-constexpr int kWarpMaxN = 32;
+constexpr int kWarpMaxN = 64;
 constexpr int kCtaMaxN = 128;
 
 bool trace_enabled()

@@ -4,9 +4,9 @@
 //   potf2  the 128 x 128 diagonal block A11 is factored in place by K2
 //          (potrf_cta.cu) in its sub-block mode;
 //   trsm   L21 = A21 L11^{-T} for the rows below it (one thread per row,
-//          32-column blocks, L11 staged in shared memory);
+//          32-column blocks, L11 packed in shared memory);
 //   syrk   A22 <- A22 - L21 L21^T on the trailing LOWER triangle only, in
-//          64 x 64 tiles (only tiles on or below the diagonal are launched).
+//          128 x 128 tiles (only tiles on or below the diagonal are launched).
 // This is the blocked right-looking schedule of "BatchLAS perf_blackwell"
 // (potrf Blocked nb/W rows: nb = 128 won above n = 512) and of the blocked
 // driver on "kernelbot-cholesky-930185", whose measured defect (a full-square
@@ -23,16 +23,32 @@ namespace {
 
 constexpr int kNb = 128;          // panel width
 constexpr int kTrsmRows = 128;    // rows per TRSM block (one per thread)
-constexpr int kLdL = kNb + 4;     // shared leading dimension of L11
-constexpr int kTile = 64;         // SYRK output tile
-constexpr int kKc = 32;           // SYRK k-chunk staged in shared memory
+constexpr int kTile = 128;        // SYRK output tile
+constexpr int kKc = 16;           // SYRK k-slice staged in shared memory
 
-// L21 (rows c0+128 .. n-1, columns c0 .. c0+127) <- A21 L11^{-T}.
-__global__ void __launch_bounds__(kTrsmRows)
+// L11 in shared memory, packed by 32-column blocks: block b keeps rows
+// 32b .. 127 of its 32 columns, column-major with leading dimension 128 - 32b.
+__host__ __device__ constexpr int l11_off(int b) { return 32 * (128 * b - 32 * (b * (b - 1) / 2)); }
+constexpr int kL11Floats = l11_off(4);  // 10240 floats, 40 KB
+
+__device__ __forceinline__ const float *l11_col(const float *Ls, int k)
+{
+    // pointer p with p[i] = L11(i, k) for i >= 32*(k/32)
+    const int b = k >> 5;
+    return Ls + l11_off(b) + (k - 32 * b) * (128 - 32 * b) - 32 * b;
+}
+
+// L21 (rows c0+128 .. n-1, columns c0 .. c0+127) <- A21 L11^{-T}, one thread
+// per row (the trsm_panel kernel of "kernelbot-cholesky-930185": row in
+// registers, L11 broadcast from shared memory), in four 32-column blocks:
+// block jb first subtracts the row's already solved blocks kb < jb (reloaded
+// from memory, the next one prefetched while the current one is applied),
+// then solves against L11's diagonal block jb.
+__global__ void __launch_bounds__(kTrsmRows, 3)
 trsm_panel_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
                   const int *__restrict__ info)
 {
-    extern __shared__ __align__(16) float Ls[];  // [kNb][kLdL]: Ls[i + j*kLdL] = L11(i, j)
+    __shared__ __align__(16) float Ls[kL11Floats];
     __shared__ float rinv[kNb];
     const int64_t mat = blockIdx.x;
     if (info[mat] != 0) return;
@@ -41,10 +57,14 @@ trsm_panel_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
 
-    for (int j = warp; j < kNb; j += kTrsmRows / 32)
-        for (int i = j + lane; i < kNb; i += 32) Ls[i + j * kLdL] = L11[i + (int64_t)j * lda];
+    for (int j = warp; j < kNb; j += kTrsmRows / 32) {
+        float *dst = const_cast<float *>(l11_col(Ls, j));
+        for (int i = j + lane; i < kNb; i += 32) cp_async4(dst + i, L11 + i + (int64_t)j * lda);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
     __syncthreads();
-    if (tid < kNb) rinv[tid] = 1.0f / Ls[tid + tid * kLdL];
+    if (tid < kNb) rinv[tid] = 1.0f / l11_col(Ls, tid)[tid];
     __syncthreads();
 
     const int r0 = c0 + kNb;
@@ -54,28 +74,45 @@ trsm_panel_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0
 
 #pragma unroll 1
     for (int jb = 0; jb < kNb / 32; ++jb) {
-        float x[32];
+        float x[32], xp[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) x[c] = X[(int64_t)(32 * jb + c) * lda];
-        // subtract the solved columns 0 .. 32*jb-1
-#pragma unroll 1
-        for (int k = 0; k < 32 * jb; ++k) {
-            const float xk = X[(int64_t)k * lda];
-            const float *Lrow = Ls + 32 * jb + k * kLdL;  // L11(32jb + c, k), c = 0..31
+        if (jb > 0) {
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float4 l4 = reinterpret_cast<const float4 *>(Lrow)[q];
-                x[4 * q + 0] = fmaf(-xk, l4.x, x[4 * q + 0]);
-                x[4 * q + 1] = fmaf(-xk, l4.y, x[4 * q + 1]);
-                x[4 * q + 2] = fmaf(-xk, l4.z, x[4 * q + 2]);
-                x[4 * q + 3] = fmaf(-xk, l4.w, x[4 * q + 3]);
+            for (int c = 0; c < 32; ++c) xp[c] = X[(int64_t)c * lda];
+        }
+#pragma unroll 1
+        for (int kb = 0; kb < jb; ++kb) {
+            float xn[32];
+            if (kb + 1 < jb) {
+#pragma unroll
+                for (int c = 0; c < 32; ++c) xn[c] = X[(int64_t)(32 * (kb + 1) + c) * lda];
+            }
+#pragma unroll
+            for (int kk = 0; kk < 32; ++kk) {
+                // L11(32jb + c, 32kb + kk), c = 0..31
+                const float *Lrow = l11_col(Ls, 32 * kb + kk) + 32 * jb;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float4 l4 = reinterpret_cast<const float4 *>(Lrow)[q];
+                    x[4 * q + 0] = fmaf(-xp[kk], l4.x, x[4 * q + 0]);
+                    x[4 * q + 1] = fmaf(-xp[kk], l4.y, x[4 * q + 1]);
+                    x[4 * q + 2] = fmaf(-xp[kk], l4.z, x[4 * q + 2]);
+                    x[4 * q + 3] = fmaf(-xp[kk], l4.w, x[4 * q + 3]);
+                }
+            }
+            if (kb + 1 < jb) {
+#pragma unroll
+                for (int c = 0; c < 32; ++c) xp[c] = xn[c];
             }
         }
         // solve against the 32 x 32 diagonal block of L11
+        const float *Ld = l11_col(Ls, 32 * jb) + 32 * jb;  // Ld[c + j*ld] = L11(32jb+c, 32jb+j)
+        const int ldd = 128 - 32 * jb;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
             x[j] *= rinv[32 * jb + j];
-            const float *Lj = Ls + 32 * jb + (32 * jb + j) * kLdL;
+            const float *Lj = Ld + j * ldd;
 #pragma unroll
             for (int q = (j + 1) / 4; q < 8; ++q) {
                 const float4 l4 = reinterpret_cast<const float4 *>(Lj)[q];
@@ -92,14 +129,49 @@ trsm_panel_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0
     }
 }
 
-// A22 <- A22 - L21 L21^T on one 64 x 64 tile (I, K), I >= K, of the trailing
-// lower triangle (rows/cols c1 .. n-1, c1 = c0 + 128); L21 = columns c0.. .
+// A22 <- A22 - L21 L21^T on one 128 x 128 tile (I, K), I >= K, of the
+// trailing lower triangle (rows/cols c1 .. n-1, c1 = c0 + 128); L21 is the
+// panel's columns c0 .. c0+127. A register-tiled FP32 GEMM: 256 threads, 8 x 8
+// outputs each (rows 4ty+{0..3} and 64+4ty+{0..3}, columns likewise with tx),
+// the k dimension staged 16 at a time in double-buffered shared memory by
+// asynchronous copies, so the next slice loads while this one is multiplied.
+// The register tile follows the 128 x 128 x 8 macro tile with 8 x 8 per thread
+// of "BatchLAS perf_gemm" (register_128x128 section). Only tiles on or below
+// the diagonal are launched; diagonal tiles mask their upper half at the store.
+__device__ __forceinline__ void syrk_stage(float (*As)[kTile + 4], float (*Bs)[kTile + 4],
+                                           const float *Li, const float *Lk, int lda, int kc,
+                                           int mi, int mk, bool vec, int tid)
+{
+    // rows [0, mi) of the I operand and [0, mk) of the K operand exist; the
+    // rest of the 128 rows are zero-filled
+    if (vec) {
+#pragma unroll
+        for (int e = 0; e < (kKc * kTile / 4) / 256; ++e) {
+            const int idx = tid + 256 * e;       // float4 index in the 16 x 128 slice
+            const int r = 4 * (idx & (kTile / 4 - 1)), k = idx / (kTile / 4);
+            const int64_t o = (int64_t)(kc + k) * lda + r;
+            const int bi = 4 * max(0, min(4, mi - r)), bk = 4 * max(0, min(4, mk - r));
+            cp_async16_zfill(&As[k][r], Li + (bi ? o : 0), bi);
+            cp_async16_zfill(&Bs[k][r], Lk + (bk ? o : 0), bk);
+        }
+    } else {
+#pragma unroll 4
+        for (int e = 0; e < (kKc * kTile) / 256; ++e) {
+            const int idx = tid + 256 * e;
+            const int r = idx & (kTile - 1), k = idx / kTile;
+            const int64_t o = (int64_t)(kc + k) * lda + r;
+            cp_async4_zfill(&As[k][r], Li + (r < mi ? o : 0), r < mi ? 4 : 0);
+            cp_async4_zfill(&Bs[k][r], Lk + (r < mk ? o : 0), r < mk ? 4 : 0);
+        }
+    }
+}
+
 __global__ void __launch_bounds__(256)
 syrk_tile_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
                  const int *__restrict__ info)
 {
-    __shared__ __align__(16) float As[kKc][kTile + 4];
-    __shared__ __align__(16) float Bs[kKc][kTile + 4];
+    __shared__ __align__(16) float As[2][kKc][kTile + 4];
+    __shared__ __align__(16) float Bs[2][kKc][kTile + 4];
     const int64_t mat = blockIdx.x;
     if (info[mat] != 0) return;
     int I, K;
@@ -117,66 +189,83 @@ syrk_tile_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     const int ri = I * kTile, rk = K * kTile;  // tile origin, trailing coordinates
     const float *Li = Ab + c1 + ri + (int64_t)c0 * lda;  // L21 rows ri.., column c0
     const float *Lk = Ab + c1 + rk + (int64_t)c0 * lda;
+    const int mi = m - ri, mk = m - rk;
+    const bool vec = ((reinterpret_cast<uintptr_t>(Li) & 15) == 0) &&
+                     ((reinterpret_cast<uintptr_t>(Lk) & 15) == 0) && ((lda & 3) == 0);
     const int tid = threadIdx.x;
-    const int tx = tid & 15, ty = tid >> 4;  // 16 x 16 threads, 4 x 4 each
+    // ty (rows) fastest: a warp's 16 row groups of one column are contiguous
+    const int ty = tid & 15, tx = tid >> 4;
 
-    float acc[4][4] = {};
+    float acc[8][8];
+#pragma unroll
+    for (int a = 0; a < 8; ++a)
+#pragma unroll
+        for (int b = 0; b < 8; ++b) acc[a][b] = 0.0f;
+
+    syrk_stage(As[0], Bs[0], Li, Lk, lda, 0, mi, mk, vec, tid);
+    cp_async_commit();
 #pragma unroll 1
-    for (int kc = 0; kc < kNb; kc += kKc) {
-        // stage L21[ri .. ri+63, kc .. kc+31] and L21[rk .., ..]: 2048 floats each
-#pragma unroll
-        for (int e = 0; e < (kKc * kTile) / 256; ++e) {
-            const int idx = tid + 256 * e;
-            const int r = idx & (kTile - 1), k = idx >> 6;
-            const int64_t o = (int64_t)(kc + k) * lda + r;
-            As[k][r] = (ri + r < m) ? Li[o] : 0.0f;
-            Bs[k][r] = (rk + r < m) ? Lk[o] : 0.0f;
-        }
+    for (int c = 0; c < kNb / kKc; ++c) {
+        if (c + 1 < kNb / kKc)
+            syrk_stage(As[(c + 1) & 1], Bs[(c + 1) & 1], Li, Lk, lda, (c + 1) * kKc, mi, mk,
+                       vec, tid);
+        cp_async_commit();
+        cp_async_wait<1>();
         __syncthreads();
-#pragma unroll 8
+        const float(*as)[kTile + 4] = As[c & 1];
+        const float(*bs)[kTile + 4] = Bs[c & 1];
+#pragma unroll
         for (int k = 0; k < kKc; ++k) {
-            const float4 a4 = *reinterpret_cast<const float4 *>(&As[k][4 * ty]);
-            const float4 b4 = *reinterpret_cast<const float4 *>(&Bs[k][4 * tx]);
-            const float av[4] = {a4.x, a4.y, a4.z, a4.w};
-            const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
+            const float4 a0 = *reinterpret_cast<const float4 *>(&as[k][4 * ty]);
+            const float4 a1 = *reinterpret_cast<const float4 *>(&as[k][64 + 4 * ty]);
+            const float4 b0 = *reinterpret_cast<const float4 *>(&bs[k][4 * tx]);
+            const float4 b1 = *reinterpret_cast<const float4 *>(&bs[k][64 + 4 * tx]);
+            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-            for (int a = 0; a < 4; ++a)
+            for (int a = 0; a < 8; ++a)
 #pragma unroll
-                for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(av[a], bv[b], acc[a][b]);
+                for (int b = 0; b < 8; ++b) acc[a][b] = fmaf(av[a], bv[b], acc[a][b]);
         }
         __syncthreads();
     }
+
     float *C = Ab + c1 + (int64_t)c1 * lda;
+    const bool full = vec && ((reinterpret_cast<uintptr_t>(C) & 15) == 0) && I != K &&
+                      ri + kTile <= m && rk + kTile <= m;
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-        const int gc = rk + 4 * tx + b;
-        if (gc >= m) continue;
+    for (int bh = 0; bh < 2; ++bh)
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
-            const int gr = ri + 4 * ty + a;
-            if (gr < m && gr >= gc) {
-                float *p = C + gr + (int64_t)gc * lda;
-                *p = *p - acc[a][b];
+        for (int b = 0; b < 4; ++b) {
+            const int gc = rk + 64 * bh + 4 * tx + b;
+#pragma unroll
+            for (int ah = 0; ah < 2; ++ah) {
+                const int gr0 = ri + 64 * ah + 4 * ty;
+                float *p = C + gr0 + (int64_t)gc * lda;
+                if (full) {
+                    float4 v = *reinterpret_cast<float4 *>(p);
+                    v.x -= acc[4 * ah + 0][4 * bh + b];
+                    v.y -= acc[4 * ah + 1][4 * bh + b];
+                    v.z -= acc[4 * ah + 2][4 * bh + b];
+                    v.w -= acc[4 * ah + 3][4 * bh + b];
+                    *reinterpret_cast<float4 *>(p) = v;
+                } else if (gc < m) {
+#pragma unroll
+                    for (int a = 0; a < 4; ++a) {
+                        const int gr = gr0 + a;
+                        if (gr < m && gr >= gc) p[a] -= acc[4 * ah + a][4 * bh + b];
+                    }
+                }
             }
         }
-    }
 }
 
-std::once_flag g_trsm_once;
-cudaError_t g_trsm_attr = cudaSuccess;
-constexpr int kTrsmSmem = kNb * kLdL * 4;
 
 }  // namespace
 
 int launch_blocked(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                    cudaStream_t stream)
 {
-    std::call_once(g_trsm_once, [] {
-        g_trsm_attr = cudaFuncSetAttribute(trsm_panel_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           kTrsmSmem);
-    });
-    if (g_trsm_attr != cudaSuccess) return (int)g_trsm_attr;
     for (int c0 = 0; c0 < n; c0 += kNb) {
         const int nb = n - c0 < kNb ? n - c0 : kNb;
         int e = launch_cta(A + c0 + (int64_t)c0 * lda, nb, lda, strideA, batch, info, stream,
@@ -185,7 +274,7 @@ int launch_blocked(float *A, int n, int lda, int64_t strideA, int batch, int *in
         const int m = n - c0 - nb;
         if (m <= 0) break;
         dim3 gt((unsigned)batch, (unsigned)((m + kTrsmRows - 1) / kTrsmRows));
-        trsm_panel_kernel<<<gt, kTrsmRows, kTrsmSmem, stream>>>(A, n, lda, strideA, c0, info);
+        trsm_panel_kernel<<<gt, kTrsmRows, 0, stream>>>(A, n, lda, strideA, c0, info);
         if ((e = (int)cudaGetLastError())) return e;
         const int T = (m + kTile - 1) / kTile;
         dim3 gs((unsigned)batch, (unsigned)(T * (T + 1) / 2));

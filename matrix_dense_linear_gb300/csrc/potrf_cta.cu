@@ -17,7 +17,9 @@
 //      (the trsm_panel kernel of the same page: one thread per row);
 //   3. every thread updates 4 x 4 tiles of the trailing LOWER triangle only,
 //      A22 <- A22 - L21 L21^T (the page's left-looking driver note measured a
-//      full-square trailing update as doubling the flops);
+//      full-square trailing update as doubling the flops): first the next
+//      panel's columns, then (look-ahead) warp 0 factors the next diagonal
+//      block while the other warps update the remaining columns;
 // with one __syncthreads after each phase. Rows and columns n .. NP-1 are an
 // identity block. Entries above the diagonal inside a diagonal block of the
 // storage are scratch: they are never read into a lower result or stored.
@@ -162,6 +164,88 @@ __device__ __forceinline__ void tri_index(int t, int &I, int &K)
     K = t - i * (i + 1) / 2;
 }
 
+// Copy columns [k0, k1) of the lower triangle (rows k .. n-1) into the
+// packed storage; rows n .. NP-1 of those columns get the identity block.
+template <int NB, int NT>
+__device__ __forceinline__ void load_columns(float *S, const float *Ab, int n, int lda, int k0,
+                                             int k1, bool vec, int warp, int lane)
+{
+    constexpr int NP = CtaGeom<NB>::NP;
+    for (int k = k0 + warp; k < k1; k += NT / 32) {
+        float *col = elem_ptr<NB>(S, 0, k);  // col[i] = element (i, k)
+        const float *g = Ab + (int64_t)k * lda;
+        const int lo = k, hi = k < n ? n : k;  // rows [lo, hi) come from memory
+        int qa = hi, qb = hi;                   // rows [qa, qb) by 16-byte copies
+        if (vec) {
+            qa = (lo + 3) & ~3;
+            qb = hi & ~3;
+            if (qb < qa) qa = qb = hi;
+        }
+        for (int q = qa + 4 * lane; q < qb; q += 128) cp_async16(col + q, g + q);
+        for (int i = lo + lane; i < hi; i += 32)
+            if (i < qa || i >= qb) cp_async4(col + i, g + i);
+        for (int i = hi + lane; i < NP; i += 32) col[i] = (i == k) ? 1.0f : 0.0f;
+    }
+}
+
+// Store the lower triangle (rows < n) back, 16 bytes at a time where aligned.
+template <int NB, int NT>
+__device__ __forceinline__ void store_columns(const float *S, float *Ab, int n, int lda,
+                                              bool vec, int warp, int lane)
+{
+    for (int k = warp; k < n; k += NT / 32) {
+        const float *col = elem_ptr<NB>(const_cast<float *>(S), 0, k);
+        float *g = Ab + (int64_t)k * lda;
+        int qa = n, qb = n;
+        if (vec) {
+            qa = (k + 3) & ~3;
+            qb = n & ~3;
+            if (qb < qa) qa = qb = n;
+        }
+        for (int q = qa + 4 * lane; q < qb; q += 128)
+            *reinterpret_cast<float4 *>(g + q) = *reinterpret_cast<const float4 *>(col + q);
+        for (int i = k + lane; i < n; i += 32)
+            if (i < qa || i >= qb) g[i] = col[i];
+    }
+}
+
+// The same two copies for the common exact case n = NP with 16-byte aligned
+// columns: column j's rows j .. NP-1 are its 0-3 leading rows (4-byte copies
+// by lanes 0..2) and whole quads from ceil4(j) on (one 16-byte copy per lane;
+// NP <= 128 is at most 32 quads). No identity block, no ragged tail.
+template <int NB, int NT>
+__device__ __forceinline__ void load_columns_full(float *S, const float *Ab, int lda, int k0,
+                                                  int k1, int warp, int lane)
+{
+    constexpr int NP = CtaGeom<NB>::NP;
+#pragma unroll 4
+    for (int k = k0 + warp; k < k1; k += NT / 32) {
+        float *col = elem_ptr<NB>(S, 0, k);
+        const float *g = Ab + (int64_t)k * lda;
+        const int q0 = (k + 3) & ~3;
+        const int q = q0 + 4 * lane;
+        if (q < NP) cp_async16(col + q, g + q);
+        if (k + lane < q0) cp_async4(col + k + lane, g + k + lane);
+    }
+}
+
+template <int NB, int NT>
+__device__ __forceinline__ void store_columns_full(const float *S, float *Ab, int lda, int warp,
+                                                   int lane)
+{
+    constexpr int NP = CtaGeom<NB>::NP;
+#pragma unroll 4
+    for (int k = warp; k < NP; k += NT / 32) {
+        const float *col = elem_ptr<NB>(const_cast<float *>(S), 0, k);
+        float *g = Ab + (int64_t)k * lda;
+        const int q0 = (k + 3) & ~3;
+        const int q = q0 + 4 * lane;
+        if (q < NP)
+            *reinterpret_cast<float4 *>(g + q) = *reinterpret_cast<const float4 *>(col + q);
+        if (k + lane < q0) g[k + lane] = col[k + lane];
+    }
+}
+
 template <int NB, int NT>
 __global__ void __launch_bounds__(NT)
 potrf_cta_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int batch,
@@ -181,45 +265,73 @@ potrf_cta_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int bat
     const int warp = tid >> 5, lane = tid & 31;
     if (tid == 0) sh_fail = 0;
 
-    // load: column k by one warp, rows k .. NP-1 (identity beyond n)
-    for (int k = warp; k < NP; k += NT / 32) {
-        float *col = elem_ptr<NB>(S, 0, k);  // col[i] = element (i, k)
-        for (int i = k + lane; i < NP; i += 32) {
-            float v = (i == k) ? 1.0f : 0.0f;
-            if (i < n) v = Ab[i + (int64_t)k * lda];
-            col[i] = v;
-        }
+    // Load. Column k is copied by one warp straight into shared memory with
+    // asynchronous copies, 16 bytes at a time where both sides are aligned
+    // (A, lda and strideA multiples of 4 floats) and 4 bytes at the ragged
+    // ends, so every copy of the matrix is in flight at once. Panel 0 is the
+    // first copy group: it is factored while the rest is still arriving.
+    // Rows n .. NP-1 are an identity block written directly.
+    const bool vec = ((reinterpret_cast<uintptr_t>(A) & 15) == 0) && ((lda & 3) == 0) &&
+                     ((strideA & 3) == 0);
+    const bool full = vec && n == NP;
+    if (full) {
+        load_columns_full<NB, NT>(S, Ab, lda, 0, 32, warp, lane);
+        cp_async_commit();
+        load_columns_full<NB, NT>(S, Ab, lda, 32, NP, warp, lane);
+        cp_async_commit();
+    } else {
+        load_columns<NB, NT>(S, Ab, n, lda, 0, 32, vec, warp, lane);
+        cp_async_commit();
+        load_columns<NB, NT>(S, Ab, n, lda, 32, NP, vec, warp, lane);
+        cp_async_commit();
     }
+    cp_async_wait<1>();
     __syncthreads();
 
+    // Panel 0's diagonal block, then per panel p (look-ahead): the panel solve
+    // of p; the trailing update of the next panel's 32 columns; then warp 0
+    // factors the next diagonal block while the other warps update the rest
+    // of the trailing triangle (columns the next panel solve does not read).
+    if (warp == 0) factor_diag_block(S, Gm::ld(0), lane, 0, n, colbuf, sinv, &sh_fail);
+    __syncthreads();
 #pragma unroll 1
-    for (int p = 0; p < NB; ++p) {
+    for (int p = 0; p < NB && !sh_fail; ++p) {
         const int c0 = 32 * p;
-        if (c0 >= n) break;
-        float *P = S + Gm::off(p);
-        const int ldp = Gm::ld(p);
-        if (warp == 0) factor_diag_block(P, ldp, lane, c0, n, colbuf, sinv, &sh_fail);
-        __syncthreads();
-        if (sh_fail) break;
         const int c1 = c0 + 32;
         if (c1 >= n) break;
+        float *P = S + Gm::off(p);
+        const int ldp = Gm::ld(p);
         for (int a = 32 + tid; a < NP - c0; a += NT) trsm_row(P, ldp, a, sinv);
+        if (p == 0) cp_async_wait<0>();  // the trailing columns have arrived
         __syncthreads();
+        // 4 x 4 tiles of the trailing triangle (rows/cols from c1), T per side;
+        // consecutive threads take consecutive tile rows of one tile column
         const int T = (NP - c1) / 4;
-        const int ntiles = T * (T + 1) / 2;
-        for (int t = tid; t < ntiles; t += NT) {
-            int I, K;
-            tri_index(t, I, K);
-            if (c1 + 4 * K < n) syrk_tile<NB>(S, P, ldp, c0, c1, I, K);
+        // the next panel's columns: tile columns 0..7, every tile row below
+        for (int t = tid; t < 8 * T; t += NT) {
+            const int K = t / T, I = t - K * T;
+            if (I >= K) syrk_tile<NB>(S, P, ldp, c0, c1, I, K);
+        }
+        __syncthreads();
+        if (warp == 0) {
+            factor_diag_block(S + Gm::off(p + 1), Gm::ld(p + 1), lane, c1, n, colbuf, sinv,
+                              &sh_fail);
+        } else {
+            const int T2 = T - 8;  // tile columns 8 .. T-1, column-major order
+            for (int t = tid - 32; t < T2 * (T2 + 1) / 2; t += NT - 32) {
+                int a, b;
+                tri_index(t, a, b);
+                const int I = 8 + (T2 - 1 - b), K = 8 + (T2 - 1 - a);
+                if (c1 + 4 * K < n) syrk_tile<NB>(S, P, ldp, c0, c1, I, K);
+            }
         }
         __syncthreads();
     }
 
-    // store the lower triangle, rows < n only
-    for (int k = warp; k < n; k += NT / 32) {
-        const float *col = elem_ptr<NB>(S, 0, k);
-        for (int i = k + lane; i < n; i += 32) Ab[i + (int64_t)k * lda] = col[i];
-    }
+    cp_async_wait<0>();  // a failed panel 0 leaves the loop before the first wait
+    __syncthreads();
+    if (full) store_columns_full<NB, NT>(S, Ab, lda, warp, lane);
+    else store_columns<NB, NT>(S, Ab, n, lda, vec, warp, lane);
     if (tid == 0) {
         const int f = sh_fail;
         if (info_off < 0) info[mat] = f;

@@ -1,5 +1,6 @@
-// K1: batched SPOTRF for n <= 32, one group of N lanes per matrix (N = 32, 16
-// or 8, so one warp factors 1, 2 or 4 matrices), the matrix in registers.
+// K1: batched SPOTRF for n <= 64, the matrix in the registers of one warp: for
+// n <= 32 a group of N lanes per matrix (N = 32, 16 or 8, so one warp factors
+// 1, 2 or 4 matrices); for 33 <= n <= 64 one warp per matrix, two rows a lane.
 //
 // Lane `row` of a group holds row `row` of its matrix, r[k] = a(row, k). The
 // factorization is right-looking: at column j every lane publishes its current
@@ -24,7 +25,7 @@
 namespace bl {
 namespace {
 
-constexpr int kWarpsPerBlock = 4;
+constexpr int kWarpsPerBlock = 1;  // one warp per block: blocks spread evenly over the SMs
 
 template <int N>
 __global__ void __launch_bounds__(32 * kWarpsPerBlock)
@@ -51,7 +52,7 @@ potrf_warp_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int ba
         r[k] = v;
     }
 
-    int fail = 0;
+    float dm = 1.0f;  // this lane's pivot
 #pragma unroll
     for (int j = 0; j < N; ++j) {
         if (j >= n) break;  // same n for every lane: uniform
@@ -60,11 +61,11 @@ potrf_warp_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int ba
         __syncwarp();
         const float *col = cb + grp * N;
         const float d = col[j];
-        if (!pivot_ok(d) && fail == 0) fail = j + 1;
         const float s = rsqrt_approx(d);
         const float lij = r[j] * s;
         const float w = lij * s;
-        r[j] = (row == j) ? sqrt_approx(d) : lij;
+        r[j] = lij;
+        dm = (row == j) ? d : dm;
         // columns j+1 .. N-1 of the broadcast column, read 4 at a time
 #pragma unroll
         for (int q = (j + 1) / 4; q < N / 4; ++q) {
@@ -81,7 +82,97 @@ potrf_warp_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int ba
 #pragma unroll
     for (int k = 0; k < N; ++k)
         if (live && k <= row) Ab[row + (int64_t)k * lda] = r[k];
-    if (valid && row == 0) info[mat] = fail;
+    // the diagonal from the lane's own pivot (sqrt(+Inf) = +Inf, like the
+    // definition); info = the group's lowest row whose pivot failed
+    if (live) Ab[row + (int64_t)row * lda] = sqrt_approx(dm);
+    const unsigned bad = __ballot_sync(0xffffffffu, live && !pivot_ok(dm));
+    constexpr unsigned kGroupMask = (N == 32) ? 0xffffffffu : ((1u << (N & 31)) - 1u);
+    const unsigned mine = (bad >> (grp * N)) & kGroupMask;
+    if (valid && row == 0) info[mat] = mine ? __ffs(mine) : 0;
+}
+
+// n = 33 .. 64: one warp per matrix, lane i holds rows i (ra[k],
+// k < 32) and i + 32 (rb[k], k < 64). Same column step as above; rows 0..31
+// are finished after column 31, so from then on only rb is updated (a
+// compile-time split, since the column loop is unrolled). The pivot test and
+// the diagonal's square root are taken once at the end from each lane's own
+// pivot (info by a warp ballot: the lowest failing row).
+__global__ void __launch_bounds__(32 * kWarpsPerBlock)
+potrf_warp64_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int batch,
+                    int *__restrict__ info)
+{
+    __shared__ __align__(16) float colbuf[kWarpsPerBlock][2][64];
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int64_t mat = (int64_t)blockIdx.x * kWarpsPerBlock + warp;
+    const bool valid = mat < batch;
+    const int rowa = lane, rowb = lane + 32;
+    const bool livea = valid && rowa < n, liveb = valid && rowb < n;
+    float *__restrict__ Ab = A + (valid ? mat * strideA : 0);
+
+    float ra[32], rb[64];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+        float v = (rowa == k) ? 1.0f : 0.0f;
+        if (livea && k <= rowa) v = Ab[rowa + (int64_t)k * lda];
+        ra[k] = v;
+    }
+#pragma unroll
+    for (int k = 0; k < 64; ++k) {
+        float v = (rowb == k) ? 1.0f : 0.0f;
+        if (liveb && k <= rowb) v = Ab[rowb + (int64_t)k * lda];
+        rb[k] = v;
+    }
+
+    float da = 1.0f, db = 1.0f;  // this lane's two pivots
+#pragma unroll
+    for (int j = 0; j < 64; ++j) {
+        if (j >= n) break;
+        float *cb = colbuf[warp][j & 1];
+        if (j < 32) cb[lane] = ra[j];
+        cb[lane + 32] = rb[j];
+        __syncwarp();
+        const float d = cb[j];
+        const float s = rsqrt_approx(d);
+        float wa = 0.0f;
+        if (j < 32) {
+            const float la = ra[j] * s;
+            wa = la * s;
+            ra[j] = la;
+            da = (rowa == j) ? d : da;
+        }
+        const float lb = rb[j] * s;
+        const float wb = lb * s;
+        rb[j] = lb;
+        db = (rowb == j) ? d : db;
+#pragma unroll
+        for (int q = (j + 1) / 4; q < 16; ++q) {
+            const float4 c4 = reinterpret_cast<const float4 *>(cb)[q];
+            const float cv[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int k = 4 * q + t;
+                if (k > j) {
+                    if (j < 32 && k < 32) ra[k] = fmaf(-wa, cv[t], ra[k]);
+                    rb[k] = fmaf(-wb, cv[t], rb[k]);
+                }
+            }
+        }
+    }
+
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+        if (livea && k <= rowa) Ab[rowa + (int64_t)k * lda] = ra[k];
+#pragma unroll
+    for (int k = 0; k < 64; ++k)
+        if (liveb && k <= rowb) Ab[rowb + (int64_t)k * lda] = rb[k];
+    // diagonal entries from the pivots (sqrt(+Inf) = +Inf, like the definition)
+    if (livea) Ab[rowa + (int64_t)rowa * lda] = sqrt_approx(da);
+    if (liveb) Ab[rowb + (int64_t)rowb * lda] = sqrt_approx(db);
+    const unsigned fa = __ballot_sync(0xffffffffu, livea && !pivot_ok(da));
+    const unsigned fb = __ballot_sync(0xffffffffu, liveb && !pivot_ok(db));
+    if (valid && lane == 0) info[mat] = fa ? __ffs(fa) : (fb ? 32 + __ffs(fb) : 0);
 }
 
 template <int N>
@@ -95,6 +186,14 @@ int launch_n(float *A, int n, int lda, int64_t strideA, int batch, int *info, cu
     return (int)cudaGetLastError();
 }
 
+int launch_64(float *A, int n, int lda, int64_t strideA, int batch, int *info, cudaStream_t st)
+{
+    const int64_t blocks = (batch + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    potrf_warp64_kernel<<<(unsigned)blocks, 32 * kWarpsPerBlock, 0, st>>>(A, n, lda, strideA,
+                                                                          batch, info);
+    return (int)cudaGetLastError();
+}
+
 }  // namespace
 
 int launch_warp(float *A, int n, int lda, int64_t strideA, int batch, int *info,
@@ -102,7 +201,8 @@ int launch_warp(float *A, int n, int lda, int64_t strideA, int batch, int *info,
 {
     if (n <= 8) return launch_n<8>(A, n, lda, strideA, batch, info, stream);
     if (n <= 16) return launch_n<16>(A, n, lda, strideA, batch, info, stream);
-    return launch_n<32>(A, n, lda, strideA, batch, info, stream);
+    if (n <= 32) return launch_n<32>(A, n, lda, strideA, batch, info, stream);
+    return launch_64(A, n, lda, strideA, batch, info, stream);
 }
 
 int attrs_warp(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem)
@@ -110,7 +210,8 @@ int attrs_warp(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem)
     cudaError_t e;
     if (n <= 8) e = cudaFuncGetAttributes(fa, potrf_warp_kernel<8>);
     else if (n <= 16) e = cudaFuncGetAttributes(fa, potrf_warp_kernel<16>);
-    else e = cudaFuncGetAttributes(fa, potrf_warp_kernel<32>);
+    else if (n <= 32) e = cudaFuncGetAttributes(fa, potrf_warp_kernel<32>);
+    else e = cudaFuncGetAttributes(fa, potrf_warp64_kernel);
     *threads = 32 * kWarpsPerBlock;
     *dyn_smem = 0;
     return (int)e;

@@ -81,19 +81,19 @@ def test_check_order(bl):
 
 def test_forced_route_that_cannot_run(bl):
     lib = bl.library()
-    assert lib.bl_spotrf_batched_ex(8, 33, 33, 33 * 33, 1, 8, None, bl.ROUTE_WARP) == -8
+    assert lib.bl_spotrf_batched_ex(8, 65, 65, 65 * 65, 1, 8, None, bl.ROUTE_WARP) == -8
     assert lib.bl_spotrf_batched_ex(8, 129, 129, 129 * 129, 1, 8, None, bl.ROUTE_CTA) == -8
     assert lib.bl_spotrf_batched_ex(8, 4, 4, 16, 1, 8, None, 9) == -8
     assert lib.bl_spotrf_batched_ex(8, 4, 4, 16, 1, 8, None, -1) == -8
     # argument errors come first
-    assert lib.bl_spotrf_batched_ex(8, 33, 32, 33 * 33, 1, 8, None, bl.ROUTE_WARP) == -3
+    assert lib.bl_spotrf_batched_ex(8, 65, 64, 65 * 65, 1, 8, None, bl.ROUTE_WARP) == -3
 
 
 def test_route_selection(bl):
     assert bl.route(0, 5) == 0 and bl.route(5, 0) == 0
-    for n in (1, 8, 9, 16, 17, 32):
+    for n in (1, 8, 9, 16, 17, 32, 33, 64):
         assert bl.route(n, 1024) == bl.ROUTE_WARP
-    for n in (33, 64, 65, 128):
+    for n in (65, 100, 128):
         assert bl.route(n, 1024) == bl.ROUTE_CTA
     for n in (129, 256, 1024, 4096):
         assert bl.route(n, 512) == bl.ROUTE_BLOCKED

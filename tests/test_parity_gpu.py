@@ -20,7 +20,7 @@ WARP, CTA, BLOCKED = 1, 2, 3
 
 def _routes(n):
     r = [0, BLOCKED]
-    if n <= 32:
+    if n <= 64:
         r.append(WARP)
     if n <= 128:
         r.append(CTA)
@@ -122,7 +122,7 @@ def test_batch_position_invariance_and_determinism(n):
                               np.tril(np.array(gv[b])).view(np.uint32))
 
 
-@pytest.mark.parametrize("n", [17, 32, 100, 128])
+@pytest.mark.parametrize("n", [17, 32, 48, 64, 100, 128])
 def test_routes_agree(n):
     bt = _gram_batch(n, 6, 700 + n, fill="nan")
     outs = [run_gpu(bt, r)[0] for r in _routes(n)]
@@ -154,8 +154,8 @@ def test_nondefault_stream():
     compare(bt, out, info, what="stream")
 
 
-@pytest.mark.parametrize("route,n", [(1, 8), (1, 16), (1, 32), (2, 32), (2, 64), (2, 96),
-                                     (2, 128), (3, 256)])
+@pytest.mark.parametrize("route,n", [(1, 8), (1, 16), (1, 32), (1, 64), (2, 32), (2, 64),
+                                     (2, 96), (2, 128), (3, 256)])
 def test_kernels_use_no_local_memory(route, n):
     import matrix_dense_linear_gb300 as bl
     ki = bl.kernel_info(route, n)
