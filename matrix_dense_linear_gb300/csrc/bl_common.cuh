@@ -73,6 +73,10 @@ int launch_cta(float *A, int n, int lda, int64_t strideA, int batch, int *info,
 int launch_blocked(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                    cudaStream_t stream);
 
+int launch_syrk_tc(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
+                   cudaStream_t stream);
+int attrs_syrk_tc(cudaFuncAttributes *fa);
+
 int attrs_warp(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem);
 int attrs_cta(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem);
 int attrs_blocked(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem);

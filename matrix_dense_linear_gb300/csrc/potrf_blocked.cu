@@ -276,21 +276,27 @@ int launch_blocked(float *A, int n, int lda, int64_t strideA, int batch, int *in
         dim3 gt((unsigned)batch, (unsigned)((m + kTrsmRows - 1) / kTrsmRows));
         trsm_panel_kernel<<<gt, kTrsmRows, 0, stream>>>(A, n, lda, strideA, c0, info);
         if ((e = (int)cudaGetLastError())) return e;
-        const int T = (m + kTile - 1) / kTile;
-        dim3 gs((unsigned)batch, (unsigned)(T * (T + 1) / 2));
-        syrk_tile_kernel<<<gs, 256, 0, stream>>>(A, n, lda, strideA, c0, info);
-        if ((e = (int)cudaGetLastError())) return e;
+        // tensor cores (3xTF32) when the panels are 16-byte aligned, else FP32
+        e = launch_syrk_tc(A, n, lda, strideA, batch, info, c0, stream);
+        if (e == 1) {
+            const int T = (m + kTile - 1) / kTile;
+            dim3 gs((unsigned)batch, (unsigned)(T * (T + 1) / 2));
+            syrk_tile_kernel<<<gs, 256, 0, stream>>>(A, n, lda, strideA, c0, info);
+            e = (int)cudaGetLastError();
+        }
+        if (e) return e;
     }
     return 0;
 }
 
 int attrs_blocked(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem)
 {
-    // the dominant kernel of the blocked path is the trailing update
+    // the dominant kernel of the blocked path is the trailing update (the
+    // tensor-core one for aligned panels)
     (void)n;
     *threads = 256;
     *dyn_smem = 0;
-    return (int)cudaFuncGetAttributes(fa, syrk_tile_kernel);
+    return attrs_syrk_tc(fa);
 }
 
 }  // namespace bl

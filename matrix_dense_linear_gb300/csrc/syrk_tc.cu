@@ -1,0 +1,236 @@
+// Trailing update of the blocked path on the tensor cores:
+//     A22 <- A22 - L21 L21^T     (lower triangle, 128 x 128 output tiles, K = 128)
+// with an error-compensated "3xTF32" split of the FP32 operands: each operand
+// x = hi + lo with hi exact in TF32 and lo the FP32 remainder, and
+//     L_I L_K^T ~= hi_I hi_K^T + hi_I lo_K^T + lo_I hi_K^T
+// (the lo*lo term is below FP32 rounding). This is the trailing update the
+// left-looking and blocked drivers of "kernelbot-cholesky-930185" ran through
+// cuBLAS with TF32 (its notes record plain TF32 failing the reconstruction
+// budget at n = 256); here it is a tcgen05 kernel of our own with the
+// compensated split, the accumulator in tensor memory.
+//
+// One block (256 threads) per output tile (I, K), I >= K. The k dimension goes
+// through shared memory 16 columns at a time, double-buffered: every thread
+// loads a 4 x 4 block of one operand (4 columns x 4 rows, 16-byte loads along
+// the contiguous rows), splits it and writes it K-major (row r: k..k+3) into
+// the hi and lo tiles; thread 0 then issues 2 k-steps x 3 products of
+// tcgen05.mma (M = N = 128, K = 8) and commits them to the buffer's mbarrier,
+// which the stagers wait on before reusing the buffer. The next slice's global
+// loads are in flight while the current one is written. The epilogue reads the
+// accumulator back from tensor memory (warp w: rows 32(w%4).., columns
+// 64(w/4)..) and subtracts it from A22 in place, lower triangle only.
+//
+// Every wait is bounded (about a second); a block that gives up marks the
+// matrix with info = -1 and still releases its tensor memory.
+#include <mutex>
+
+#include "bl_common.cuh"
+#include "tc_sm100.cuh"
+
+namespace bl {
+namespace {
+
+constexpr int kNbTc = 128;                 // panel width = GEMM k
+constexpr int kKs = 16;                    // k columns per shared-memory slice
+constexpr int kSlices = kNbTc / kKs;       // 8
+constexpr uint32_t kLbo = 128;             // K-adjacent core matrices
+constexpr uint32_t kSbo = (kKs / 4) * 128 + 16;  // row-group stride, +16 B: no bank conflicts
+constexpr uint32_t kTileBytes = 16 * kSbo;  // 128 rows
+constexpr uint32_t kStageBytes = 4 * kTileBytes;  // A hi, A lo, B hi, B lo
+constexpr int kSmemBytes = 2 * kStageBytes;
+constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at 2 GHz
+
+__device__ __forceinline__ uint32_t core_off(int r, int kq)
+{
+    // byte offset of (row r, k = 4kq .. 4kq+3) in a K-major no-swizzle tile
+    return (uint32_t)(r >> 3) * kSbo + (uint32_t)kq * kLbo + (uint32_t)(r & 7) * 16;
+}
+
+__global__ void __launch_bounds__(256, 2)
+syrk_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
+               int *__restrict__ info)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ uint32_t tmem_base;
+    __shared__ __align__(8) uint64_t mbar[2];
+    __shared__ int sh_err;
+
+    const int64_t mat = blockIdx.x;
+    if (info[mat] != 0) return;
+    int I, K;
+    {
+        const int t = blockIdx.y;
+        int i = (int)((sqrtf(8.0f * (float)t + 1.0f) - 1.0f) * 0.5f);
+        while ((i + 1) * (i + 2) / 2 <= t) ++i;
+        while (i * (i + 1) / 2 > t) --i;
+        I = i;
+        K = t - i * (i + 1) / 2;
+    }
+    float *__restrict__ Ab = A + mat * strideA;
+    const int c1 = c0 + kNbTc;
+    const int m = n - c1;
+    const int ri = I * 128, rk = K * 128;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    // this thread stages one 4 x 4 block of one operand per slice
+    const int op = tid >> 7;            // 0: rows ri.. (A side), 1: rows rk.. (B side)
+    const int rq = tid & 31;            // row quad: rows 4rq .. 4rq+3
+    const int kq = (tid >> 5) & 3;      // k quad within the slice
+    const int rbase = op ? rk : ri;
+    const int mrows = m - rbase;        // rows of this operand that exist
+    const float *src = Ab + c1 + rbase + 4 * rq + (int64_t)(c0 + 4 * kq) * lda;
+    const int valid_rows = max(0, min(4, mrows - 4 * rq));
+
+    if (tid == 0) {
+        sh_err = 0;
+        tc::mbar_init(&mbar[0], 1);
+        tc::mbar_init(&mbar[1], 1);
+        tc::fence_mbar_init();
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(&tmem_base, 128);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = tmem_base;
+    const uint32_t sbase = tc::smem_u32(smem);
+    constexpr uint32_t idesc = tc::idesc_tf32(128, 128);
+
+    float4 cur[4], nxt[4];
+    auto load_slice = [&](int s, float4 (&v)[4]) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const float *p = src + (int64_t)(s * kKs + c) * lda;
+            if (valid_rows == 4) {
+                v[c] = *reinterpret_cast<const float4 *>(p);
+            } else {
+                v[c].x = valid_rows > 0 ? p[0] : 0.0f;
+                v[c].y = valid_rows > 1 ? p[1] : 0.0f;
+                v[c].z = valid_rows > 2 ? p[2] : 0.0f;
+                v[c].w = 0.0f;
+            }
+        }
+    };
+    load_slice(0, cur);
+
+    bool ok = true;
+    int issued = 0;  // slices whose MMAs thread 0 has issued (same in every thread)
+#pragma unroll 1
+    for (int s = 0; s < kSlices; ++s) {
+        const int b = s & 1;
+        if (s + 1 < kSlices) load_slice(s + 1, nxt);
+        if (s >= 2 && !tc::mbar_wait(&mbar[b], ((s - 2) >> 1) & 1, kWaitCycles)) ok = false;
+        // transpose the 4 x 4 block to K-major rows, split into hi and lo
+        uint8_t *st = smem + b * kStageBytes + (op ? 2 : 0) * kTileBytes;
+        const float cv[4][4] = {{cur[0].x, cur[0].y, cur[0].z, cur[0].w},
+                                {cur[1].x, cur[1].y, cur[1].z, cur[1].w},
+                                {cur[2].x, cur[2].y, cur[2].z, cur[2].w},
+                                {cur[3].x, cur[3].y, cur[3].z, cur[3].w}};  // [k][row]
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float h[4], l[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tc::split_tf32(cv[c][i], h[c], l[c]);
+            const uint32_t off = core_off(4 * rq + i, kq);
+            *reinterpret_cast<float4 *>(st + off) = make_float4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<float4 *>(st + kTileBytes + off) = make_float4(l[0], l[1], l[2], l[3]);
+        }
+        tc::fence_async_smem();
+        if (!ok) sh_err = 1;
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+        if (sh_err) { ok = false; break; }
+        if (tid == 0) {
+            const uint32_t a_hi = sbase + b * kStageBytes, a_lo = a_hi + kTileBytes;
+            const uint32_t b_hi = a_hi + 2 * kTileBytes, b_lo = a_hi + 3 * kTileBytes;
+#pragma unroll
+            for (int ks = 0; ks < kKs / 8; ++ks) {
+                const uint32_t ko = ks * 2 * kLbo;
+                const uint32_t acc0 = (s > 0 || ks > 0) ? 1u : 0u;
+                tc::mma_tf32(tmem, tc::smem_desc(a_hi + ko, kLbo, kSbo),
+                             tc::smem_desc(b_hi + ko, kLbo, kSbo), idesc, acc0);
+                tc::mma_tf32(tmem, tc::smem_desc(a_hi + ko, kLbo, kSbo),
+                             tc::smem_desc(b_lo + ko, kLbo, kSbo), idesc, 1u);
+                tc::mma_tf32(tmem, tc::smem_desc(a_lo + ko, kLbo, kSbo),
+                             tc::smem_desc(b_hi + ko, kLbo, kSbo), idesc, 1u);
+            }
+            tc::mma_commit(&mbar[b]);
+        }
+        ++issued;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) cur[c] = nxt[c];
+    }
+
+    // all MMAs issued before the last commit are complete once it arrives; the
+    // outcome is made block-uniform (tcgen05.ld is a warp-collective)
+    const int last = issued - 1;
+    if (ok && !tc::mbar_wait(&mbar[last & 1], (last >> 1) & 1, kWaitCycles)) ok = false;
+    if (!ok) sh_err = 1;
+    __syncthreads();
+    ok = sh_err == 0;
+    tc::fence_after_sync();
+
+    if (ok) {
+        const int q = warp & 3, h = warp >> 2;
+        const int r = 32 * q + lane;  // tile row
+        const int gr = ri + r;        // trailing row
+        float *Crow = Ab + c1 + gr + (int64_t)c1 * lda;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+            float v[16];
+            tc::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + 64 * h + 16 * c, v);
+            const int gc0 = rk + 64 * h + 16 * c;
+            if (gr < m) {
+                float old[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int gc = gc0 + j;
+                    old[j] = (gc < m && gr >= gc) ? Crow[(int64_t)gc * lda] : 0.0f;
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int gc = gc0 + j;
+                    if (gc < m && gr >= gc) Crow[(int64_t)gc * lda] = old[j] - v[j];
+                }
+            }
+        }
+    } else if (tid == 0) {
+        info[mat] = -1;
+        // let anything still in flight drain (bounded) before releasing TMEM
+        if (last >= 0) tc::mbar_wait(&mbar[last & 1], (last >> 1) & 1, kWaitCycles);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, 128);
+}
+
+std::once_flag g_tc_once;
+cudaError_t g_tc_attr = cudaSuccess;
+
+}  // namespace
+
+// Returns 0 and launches when the tensor-core path applies (16-byte aligned
+// panels), 1 when the caller must use the FP32 path, or a cudaError_t.
+int launch_syrk_tc(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
+                   cudaStream_t stream)
+{
+    if (((reinterpret_cast<uintptr_t>(A) & 15) != 0) || (lda & 3) || (strideA & 3)) return 1;
+    std::call_once(g_tc_once, [] {
+        g_tc_attr = cudaFuncSetAttribute(syrk_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemBytes);
+    });
+    if (g_tc_attr != cudaSuccess) return (int)g_tc_attr;
+    const int m = n - c0 - kNbTc;
+    const int T = (m + 127) / 128;
+    dim3 grid((unsigned)batch, (unsigned)(T * (T + 1) / 2));
+    syrk_tc_kernel<<<grid, 256, kSmemBytes, stream>>>(A, n, lda, strideA, c0, info);
+    return (int)cudaGetLastError();
+}
+
+int attrs_syrk_tc(cudaFuncAttributes *fa) { return (int)cudaFuncGetAttributes(fa, syrk_tc_kernel); }
+
+}  // namespace bl
