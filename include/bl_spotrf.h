@@ -22,6 +22,9 @@
  * first pivot with !(d_j > 0) (a NaN pivot fails; +Inf passes). After a
  * failure at k = info[b] only the leading (k-1) x (k-1) block of L_b is
  * defined; the rest of that matrix's lower triangle is unspecified.
+ * info[b] = -1 reports an internal error: a bounded wait inside a
+ * tensor-core kernel gave up (about a second) and matrix b's result is not
+ * valid. It does not occur in normal operation.
  *
  * All arithmetic is IEEE single precision (contractions into FMA allowed; the
  * reciprocal square root of the pivot is the hardware approximation).
@@ -45,6 +48,8 @@ extern "C" {
 #define BL_ROUTE_CTA 2      /* K2: one thread block per matrix, shared-memory resident, n <= 128 */
 #define BL_ROUTE_BLOCKED 3  /* K3: right-looking blocked, 128-wide panels: diagonal factor,
                                panel triangular solve, lower-only trailing update, any n */
+#define BL_ROUTE_TMEM 4     /* K2t: one thread block per matrix, the matrix resident in tensor
+                               memory, trailing updates on the tensor cores, n <= 128 */
 
 /*
  * bl_spotrf_batched - factor a strided batch in place.
@@ -87,7 +92,7 @@ int bl_spotrf_batched(float *A, int n, int lda, int64_t strideA, int batch, int 
  * bl_spotrf_batched_ex - as bl_spotrf_batched, with the kernel class forced
  * (route = BL_ROUTE_*; BL_ROUTE_AUTO selects by n like bl_spotrf_batched).
  * Returns -8 when the forced route cannot factor this n (WARP: n > 64;
- * CTA: n > 128), after the checks above. For tests and measurement.
+ * CTA or TMEM: n > 128), after the checks above. For tests and measurement.
  */
 int bl_spotrf_batched_ex(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                          cudaStream_t stream, int route);

@@ -12,11 +12,12 @@ import ctypes
 import os
 from typing import Optional
 
-__all__ = ["ROUTE_AUTO", "ROUTE_WARP", "ROUTE_CTA", "ROUTE_BLOCKED", "MAX_N", "BLError",
+__all__ = ["ROUTE_AUTO", "ROUTE_WARP", "ROUTE_CTA", "ROUTE_BLOCKED", "ROUTE_TMEM", "MAX_N",
+           "BLError",
            "library", "library_path", "spotrf_batched", "spotrf_batched_ex", "route",
            "kernel_info", "version", "factor", "factor_host"]
 
-ROUTE_AUTO, ROUTE_WARP, ROUTE_CTA, ROUTE_BLOCKED = 0, 1, 2, 3
+ROUTE_AUTO, ROUTE_WARP, ROUTE_CTA, ROUTE_BLOCKED, ROUTE_TMEM = 0, 1, 2, 3, 4
 MAX_N = 4096
 _PKG = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_PKG, "libbl_spotrf.so")

@@ -12,7 +12,10 @@ namespace {
 // Size thresholds of the selector. The pages route by order the same way
 // (one warp per matrix up to n = 32, one work-group per matrix in the middle,
 // blocked above: "BatchLAS perf_blackwell", potrf row of its routing table;
-// the size router of "kernelbot-cholesky-930185").
+// the size router of "kernelbot-cholesky-930185"). Measured on GB300: the
+// register-resident warp kernel wins up to n = 64; for 65..128 the shared-
+// memory block kernel (K2) beats the tensor-memory one (K2t, reachable as a
+// forced route) at 1024 matrices of n = 128 (about 70 us against 89 us).
 constexpr int kWarpMaxN = 64;
 constexpr int kCtaMaxN = 128;
 
@@ -51,6 +54,7 @@ bool route_can_run(int route, int n)
     switch (route) {
     case BL_ROUTE_WARP: return n <= kWarpMaxN;
     case BL_ROUTE_CTA: return n <= kCtaMaxN;
+    case BL_ROUTE_TMEM: return n <= kCtaMaxN;
     case BL_ROUTE_BLOCKED: return true;
     default: return false;
     }
@@ -72,6 +76,8 @@ int run(float *A, int n, int lda, int64_t strideA, int batch, int *info, cudaStr
     case BL_ROUTE_WARP: return bl::launch_warp(A, n, lda, strideA, batch, info, stream);
     case BL_ROUTE_CTA:
         return bl::launch_cta(A, n, lda, strideA, batch, info, stream, bl::InfoMode{-1});
+    case BL_ROUTE_TMEM:
+        return bl::launch_tmem(A, n, lda, strideA, batch, info, stream, bl::InfoMode{-1});
     default: return bl::launch_blocked(A, n, lda, strideA, batch, info, stream);
     }
 }
@@ -89,7 +95,7 @@ int bl_spotrf_batched(float *A, int n, int lda, int64_t strideA, int batch, int 
 int bl_spotrf_batched_ex(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                          cudaStream_t stream, int route)
 {
-    if (route < BL_ROUTE_AUTO || route > BL_ROUTE_BLOCKED) return -8;
+    if (route < BL_ROUTE_AUTO || route > BL_ROUTE_TMEM) return -8;
     return run(A, n, lda, strideA, batch, info, stream, route);
 }
 
@@ -109,6 +115,7 @@ int bl_spotrf_kernel_info(int route, int n, int *regs, int *local_bytes, int *st
     switch (route) {
     case BL_ROUTE_WARP: e = bl::attrs_warp(n, &fa, &th, &dyn); break;
     case BL_ROUTE_CTA: e = bl::attrs_cta(n, &fa, &th, &dyn); break;
+    case BL_ROUTE_TMEM: e = bl::attrs_tmem(n, &fa, &th, &dyn); break;
     default: e = bl::attrs_blocked(n, &fa, &th, &dyn); break;
     }
     if (e) return e;

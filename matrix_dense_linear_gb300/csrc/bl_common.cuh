@@ -70,6 +70,8 @@ int launch_warp(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                 cudaStream_t stream);
 int launch_cta(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                cudaStream_t stream, InfoMode mode);
+int launch_tmem(float *A, int n, int lda, int64_t strideA, int batch, int *info,
+                cudaStream_t stream, InfoMode mode);
 int launch_blocked(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                    cudaStream_t stream);
 
@@ -79,6 +81,7 @@ int attrs_syrk_tc(cudaFuncAttributes *fa);
 
 int attrs_warp(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem);
 int attrs_cta(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem);
+int attrs_tmem(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem);
 int attrs_blocked(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem);
 
 }  // namespace bl

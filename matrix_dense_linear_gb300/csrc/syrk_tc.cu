@@ -98,7 +98,7 @@ syrk_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     const uint32_t sbase = tc::smem_u32(smem);
     constexpr uint32_t idesc = tc::idesc_tf32(128, 128);
 
-    float4 cur[4], nxt[4];
+    float4 cur[4], nxt[4], nxt2[4];
     auto load_slice = [&](int s, float4 (&v)[4]) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -114,13 +114,14 @@ syrk_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
         }
     };
     load_slice(0, cur);
+    load_slice(1, nxt);
 
     bool ok = true;
     int issued = 0;  // slices whose MMAs thread 0 has issued (same in every thread)
 #pragma unroll 1
     for (int s = 0; s < kSlices; ++s) {
         const int b = s & 1;
-        if (s + 1 < kSlices) load_slice(s + 1, nxt);
+        if (s + 2 < kSlices) load_slice(s + 2, nxt2);  // two slices in flight
         if (s >= 2 && !tc::mbar_wait(&mbar[b], ((s - 2) >> 1) & 1, kWaitCycles)) ok = false;
         // transpose the 4 x 4 block to K-major rows, split into hi and lo
         uint8_t *st = smem + b * kStageBytes + (op ? 2 : 0) * kTileBytes;
@@ -161,7 +162,24 @@ syrk_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
         }
         ++issued;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) cur[c] = nxt[c];
+        for (int c = 0; c < 4; ++c) {
+            cur[c] = nxt[c];
+            nxt[c] = nxt2[c];
+        }
+    }
+
+    // this thread's 64 entries of A22 (its tile row, its column half) are
+    // loaded while the last MMAs run
+    const int q = warp & 3, h = warp >> 2;
+    const int r = 32 * q + lane;  // tile row
+    const int gr = ri + r;        // trailing row
+    const int gcb = rk + 64 * h;  // first trailing column of this half
+    float *Crow = Ab + c1 + gr + (int64_t)c1 * lda;
+    float old[32];  // the first two 16-column chunks; the other two follow
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const int gc = gcb + j;
+        old[j] = (gr < m && gc < m && gr >= gc) ? Crow[(int64_t)gc * lda] : 0.0f;
     }
 
     // all MMAs issued before the last commit are complete once it arrives; the
@@ -174,26 +192,24 @@ syrk_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     tc::fence_after_sync();
 
     if (ok) {
-        const int q = warp & 3, h = warp >> 2;
-        const int r = 32 * q + lane;  // tile row
-        const int gr = ri + r;        // trailing row
-        float *Crow = Ab + c1 + gr + (int64_t)c1 * lda;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-            float v[16];
-            tc::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + 64 * h + 16 * c, v);
-            const int gc0 = rk + 64 * h + 16 * c;
-            if (gr < m) {
-                float old[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int gc = gc0 + j;
-                    old[j] = (gc < m && gr >= gc) ? Crow[(int64_t)gc * lda] : 0.0f;
+        for (int half = 0; half < 2; ++half) {
+            if (half == 1) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int gc = gcb + 32 + j;
+                    old[j] = (gr < m && gc < m && gr >= gc) ? Crow[(int64_t)gc * lda] : 0.0f;
                 }
+            }
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                float v[16];
+                tc::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + 64 * h + 32 * half + 16 * c, v);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const int gc = gc0 + j;
-                    if (gc < m && gr >= gc) Crow[(int64_t)gc * lda] = old[j] - v[j];
+                    const int gc = gcb + 32 * half + 16 * c + j;
+                    if (gr < m && gc < m && gr >= gc)
+                        Crow[(int64_t)gc * lda] = old[16 * c + j] - v[j];
                 }
             }
         }

@@ -107,16 +107,26 @@ __device__ __forceinline__ bool mbar_test(uint64_t *mbar, uint32_t parity)
         : "=r"(ok) : "r"(smem_u32(mbar)), "r"(parity) : "memory");
     return ok != 0;
 }
+// One potentially blocking probe: the hardware suspends the thread until the
+// phase completes or its own short time limit passes.
+__device__ __forceinline__ bool mbar_try(uint64_t *mbar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok) : "r"(smem_u32(mbar)), "r"(parity) : "memory");
+    return ok != 0;
+}
 // Wait for the phase with the given parity to complete, giving up after about
 // max_cycles SM cycles (returns false then). Never an unbounded spin.
 __device__ __forceinline__ bool mbar_wait(uint64_t *mbar, uint32_t parity, long long max_cycles)
 {
     if (mbar_test(mbar, parity)) return true;
     const long long t0 = clock64();
-    while (!mbar_test(mbar, parity)) {
+    while (!mbar_try(mbar, parity))
         if (clock64() - t0 > max_cycles) return false;
-        __nanosleep(32);
-    }
     return true;
 }
 
@@ -158,6 +168,29 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
         : "memory");
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 32 lanes x 32 columns of 32-bit values into tensor memory (the inverse of
+// tmem_ld32), waiting until the stores are done.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
+        "tcgen05.wait::st.sync.aligned;"
+        ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])),
+          "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])),
+          "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+          "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
+          "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
+          "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])),
+          "r"(__float_as_uint(v[17])), "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])),
+          "r"(__float_as_uint(v[20])), "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])),
+          "r"(__float_as_uint(v[23])), "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])),
+          "r"(__float_as_uint(v[26])), "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])),
+          "r"(__float_as_uint(v[29])), "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        : "memory");
 }
 
 // Split x into a tf32-exact high part (sign, exponent, top 10 mantissa bits)
