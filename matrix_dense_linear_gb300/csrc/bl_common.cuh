@@ -55,6 +55,34 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Programmatic dependent launch. Kernels launched with launch_pdl may start
+// while the previous kernel in the stream is still running; they call
+// pdl_wait() before their first access to global memory (it returns once the
+// previous grid has completed and its writes are visible) and pdl_trigger()
+// to let the next kernel start launching early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                      cudaStream_t stream, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return (int)cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // info handling of one launch over a strided batch.
 //   info_off < 0 : the launch factors whole matrices and writes info[b]
 //                  unconditionally (0 or the failing pivot).
@@ -78,6 +106,8 @@ int launch_blocked(float *A, int n, int lda, int64_t strideA, int batch, int *in
 int launch_syrk_tc(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
                    cudaStream_t stream);
 int attrs_syrk_tc(cudaFuncAttributes *fa);
+int launch_trsm_tc(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
+                   cudaStream_t stream);
 
 int attrs_warp(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem);
 int attrs_cta(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem);

@@ -273,9 +273,14 @@ int launch_blocked(float *A, int n, int lda, int64_t strideA, int batch, int *in
         if (e) return e;
         const int m = n - c0 - nb;
         if (m <= 0) break;
-        dim3 gt((unsigned)batch, (unsigned)((m + kTrsmRows - 1) / kTrsmRows));
-        trsm_panel_kernel<<<gt, kTrsmRows, 0, stream>>>(A, n, lda, strideA, c0, info);
-        if ((e = (int)cudaGetLastError())) return e;
+        // block updates of the panel solve on the tensor cores when aligned
+        e = launch_trsm_tc(A, n, lda, strideA, batch, info, c0, stream);
+        if (e == 1) {
+            dim3 gt((unsigned)batch, (unsigned)((m + kTrsmRows - 1) / kTrsmRows));
+            trsm_panel_kernel<<<gt, kTrsmRows, 0, stream>>>(A, n, lda, strideA, c0, info);
+            e = (int)cudaGetLastError();
+        }
+        if (e) return e;
         // tensor cores (3xTF32) when the panels are 16-byte aligned, else FP32
         e = launch_syrk_tc(A, n, lda, strideA, batch, info, c0, stream);
         if (e == 1) {

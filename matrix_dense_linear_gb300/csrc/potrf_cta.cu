@@ -259,6 +259,8 @@ potrf_cta_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int bat
     __shared__ int sh_fail;
 
     const int64_t mat = blockIdx.x;
+    pdl_wait();
+    pdl_trigger();
     if (info_off >= 0 && info[mat] != 0) return;  // failed at an earlier panel
     float *__restrict__ Ab = A + mat * strideA;
     const int tid = threadIdx.x;
@@ -351,9 +353,8 @@ int launch_nb(float *A, int n, int lda, int64_t strideA, int batch, int *info, c
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     });
     if (attr_err != cudaSuccess) return (int)attr_err;
-    potrf_cta_kernel<NB, NT><<<(unsigned)batch, NT, bytes, st>>>(A, n, lda, strideA, batch, info,
-                                                                 info_off);
-    return (int)cudaGetLastError();
+    return launch_pdl(potrf_cta_kernel<NB, NT>, dim3((unsigned)batch), dim3(NT), (size_t)bytes,
+                      st, A, n, lda, strideA, batch, info, info_off);
 }
 
 template <int NB, int NT>

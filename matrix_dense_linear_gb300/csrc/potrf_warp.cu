@@ -43,6 +43,8 @@ potrf_warp_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int ba
     const bool valid = mat < batch;
     const bool live = valid && row < n;
     float *__restrict__ Ab = A + (valid ? mat * strideA : 0);
+    pdl_wait();
+    pdl_trigger();
 
     float r[N];
 #pragma unroll
@@ -110,6 +112,8 @@ potrf_warp64_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int 
     const int rowa = lane, rowb = lane + 32;
     const bool livea = valid && rowa < n, liveb = valid && rowb < n;
     float *__restrict__ Ab = A + (valid ? mat * strideA : 0);
+    pdl_wait();
+    pdl_trigger();
 
     float ra[32], rb[64];
 #pragma unroll
@@ -181,17 +185,15 @@ int launch_n(float *A, int n, int lda, int64_t strideA, int batch, int *info, cu
     constexpr int G = 32 / N;
     const int64_t per_block = (int64_t)kWarpsPerBlock * G;
     const int64_t blocks = (batch + per_block - 1) / per_block;
-    potrf_warp_kernel<N><<<(unsigned)blocks, 32 * kWarpsPerBlock, 0, st>>>(A, n, lda, strideA,
-                                                                           batch, info);
-    return (int)cudaGetLastError();
+    return launch_pdl(potrf_warp_kernel<N>, dim3((unsigned)blocks), dim3(32 * kWarpsPerBlock), 0,
+                      st, A, n, lda, strideA, batch, info);
 }
 
 int launch_64(float *A, int n, int lda, int64_t strideA, int batch, int *info, cudaStream_t st)
 {
     const int64_t blocks = (batch + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    potrf_warp64_kernel<<<(unsigned)blocks, 32 * kWarpsPerBlock, 0, st>>>(A, n, lda, strideA,
-                                                                          batch, info);
-    return (int)cudaGetLastError();
+    return launch_pdl(potrf_warp64_kernel, dim3((unsigned)blocks), dim3(32 * kWarpsPerBlock), 0,
+                      st, A, n, lda, strideA, batch, info);
 }
 
 }  // namespace

@@ -191,7 +191,25 @@ syrk_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     ok = sh_err == 0;
     tc::fence_after_sync();
 
-    if (ok) {
+    const bool full = I != K && ri + 128 <= m && rk + 128 <= m;
+    if (ok && full) {  // whole off-diagonal tile: no masks
+        float *Cr = Crow + (int64_t)gcb * lda;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            if (half == 1) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) old[j] = Cr[(int64_t)(32 + j) * lda];
+            }
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                float v[16];
+                tc::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + 64 * h + 32 * half + 16 * c, v);
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    Cr[(int64_t)(32 * half + 16 * c + j) * lda] = old[16 * c + j] - v[j];
+            }
+        }
+    } else if (ok) {
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             if (half == 1) {

@@ -1,0 +1,243 @@
+// Panel solve of the blocked path with the tensor cores doing the block updates:
+//     L21 = A21 L11^{-T}      (A21: the rows below the 128 x 128 diagonal block)
+// as a blocked forward substitution over four 32-column blocks j:
+//     X_j = (A_j - sum_{i<j} X_i L_ji^T) L_jj^{-T}.
+// One block of 128 threads takes 128 rows. Tensor memory holds -(A21 rows)
+// (lane = row, column = panel column). For j = 0..3 every thread reads its
+// row's 32 columns of block j back, solves them against the 32 x 32 diagonal
+// block L_jj with the reciprocal-root scaling of K2 (one row per thread, the
+// trsm_panel kernel of "kernelbot-cholesky-930185"), stores the finished X_j
+// and stages it (3xTF32 split, K-major) as the A operand of one group of
+// tcgen05.mma that adds X_j L_{k,j}^T to every later column block k > j in
+// tensor memory. Three quarters of the flops run on the tensor cores; only the
+// 32-column triangular solves stay on the FP32 pipes.
+//
+// Needs 16-byte aligned panels (the caller falls back to the FP32 kernel
+// otherwise). Every wait is bounded; a block that gives up marks info = -1.
+#include <mutex>
+
+#include "bl_common.cuh"
+#include "tc_sm100.cuh"
+
+namespace bl {
+namespace {
+
+constexpr uint32_t kLbo = 128;
+constexpr uint32_t kSbo = 8 * 128 + 16;          // K = 32 per row group, +16 B (banks)
+constexpr uint32_t kXTile = 16 * kSbo;           // 128 rows
+// rows of L_{k,j} (k > j) for block j, and the byte offset of its hi/lo pair
+__host__ __device__ constexpr uint32_t lt_rows(int j) { return 96u - 32u * (uint32_t)j; }
+__host__ __device__ constexpr uint32_t lt_off(int j)
+{
+    return j == 0 ? 0u : (j == 1 ? 12u * kSbo * 2u : 20u * kSbo * 2u);
+}
+constexpr uint32_t kLtBytes = (12 + 8 + 4) * kSbo * 2;
+constexpr uint32_t kOffX = 0;
+constexpr uint32_t kOffLt = 2 * kXTile;
+constexpr uint32_t kOffLd = kOffLt + kLtBytes;   // diagonal blocks, 4 x 32 x 32 floats
+constexpr uint32_t kOffRinv = kOffLd + 4 * 32 * 32 * 4;
+constexpr int kSmemBytes = (int)(kOffRinv + 128 * 4);
+constexpr long long kWaitCycles = 2000000000LL;
+
+__device__ __forceinline__ uint32_t core_off(int r, int q)
+{
+    return (uint32_t)(r >> 3) * kSbo + (uint32_t)q * kLbo + (uint32_t)(r & 7) * 16;
+}
+
+__global__ void __launch_bounds__(128, 2)
+trsm_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
+               int *__restrict__ info)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ uint32_t tmem_base;
+    __shared__ __align__(8) uint64_t mbar;
+    __shared__ int sh_err;
+
+    const int64_t mat = blockIdx.x;
+    if (info[mat] != 0) return;
+    float *__restrict__ Ab = A + mat * strideA;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int R = c0 + 128 + (int)blockIdx.y * 128 + tid;  // this thread's row
+    const bool live = R < n;
+    const float *L11 = Ab + c0 + (int64_t)c0 * lda;         // L11(i, k) = L11[i + k*lda]
+    float *Ld = reinterpret_cast<float *>(smem + kOffLd);    // Ld[j*1024 + t*32 + k] = L(32j+k, 32j+t)
+    float *rinv = reinterpret_cast<float *>(smem + kOffRinv);
+
+    if (tid == 0) {
+        sh_err = 0;
+        tc::mbar_init(&mbar, 1);
+        tc::fence_mbar_init();
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(&tmem_base, 128);
+        tc::tmem_relinquish();
+    }
+
+    // diagonal blocks of L11 (lower part) by asynchronous copies
+    for (int col = warp; col < 128; col += 4) {
+        const int j = col >> 5, t = col & 31;
+        for (int k = t + lane; k < 32; k += 32)
+            cp_async4(Ld + j * 1024 + t * 32 + k, L11 + (32 * j + k) + (int64_t)col * lda);
+    }
+    cp_async_commit();
+
+    // off-diagonal row blocks L_{k,j} (k > j) as K-major hi/lo tiles: 4 x 4
+    // blocks (rows i..i+3, columns 4q..4q+3 of block j), 16-byte loads
+#pragma unroll 1
+    for (int b = tid; b < (24 + 16 + 8) * 8; b += 128) {
+        const int j = b < 192 ? 0 : (b < 320 ? 1 : 2);
+        const int bb = b - (j == 0 ? 0 : (j == 1 ? 192 : 320));
+        // row quads fastest: a warp's loads are 16-byte runs of one column and
+        // its stores land in distinct banks
+        const int nrq = (int)lt_rows(j) / 4;
+        const int rq = bb % nrq, q = bb / nrq;  // row quad within L_{.,j}, k quad
+        const int i0 = 32 * (j + 1) + 4 * rq;  // L11 row
+        float4 v[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            v[c] = *reinterpret_cast<const float4 *>(L11 + i0 + (int64_t)(32 * j + 4 * q + c) * lda);
+        const float cv[4][4] = {{v[0].x, v[0].y, v[0].z, v[0].w},
+                                {v[1].x, v[1].y, v[1].z, v[1].w},
+                                {v[2].x, v[2].y, v[2].z, v[2].w},
+                                {v[3].x, v[3].y, v[3].z, v[3].w}};  // [k][row]
+        uint8_t *hi = smem + kOffLt + lt_off(j);
+        uint8_t *lo = hi + lt_rows(j) / 8 * kSbo;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float h[4], l[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tc::split_tf32(cv[c][i], h[c], l[c]);
+            const uint32_t off = core_off(4 * rq + i, q);
+            *reinterpret_cast<float4 *>(hi + off) = make_float4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<float4 *>(lo + off) = make_float4(l[0], l[1], l[2], l[3]);
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = tmem_base;
+    const uint32_t tlane = tmem + ((uint32_t)(32 * warp) << 16);
+
+    // -A21 rows into tensor memory (two 32-column chunks in flight)
+    {
+        const float *g = Ab + R + (int64_t)c0 * lda;
+        float v0[32], v1[32];
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                v0[c] = live ? -g[(int64_t)(64 * h + c) * lda] : 0.0f;
+                v1[c] = live ? -g[(int64_t)(64 * h + 32 + c) * lda] : 0.0f;
+            }
+            tc::tmem_st32(tlane + 64 * h, v0);
+            tc::tmem_st32(tlane + 64 * h + 32, v1);
+        }
+    }
+    cp_async_wait<0>();
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    rinv[tid] = 1.0f / Ld[(tid >> 5) * 1024 + (tid & 31) * 33];
+    __syncthreads();
+
+    const uint32_t sbase = tc::smem_u32(smem);
+#pragma unroll 1
+    for (int j = 0; j < 4; ++j) {
+        if (j > 0) {
+            if (tid == 0 && !tc::mbar_wait(&mbar, (j - 1) & 1, kWaitCycles)) sh_err = 1;
+            tc::fence_before_sync();
+            __syncthreads();
+            if (sh_err) break;
+            tc::fence_after_sync();
+        }
+        float x[32];
+        tc::tmem_ld32(tlane + 32 * j, x);
+        const float *Lj = Ld + j * 1024;
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+            x[t] = -x[t] * rinv[32 * j + t];
+            const float *Lt = Lj + t * 32;
+#pragma unroll
+            for (int q = (t + 1) / 4; q < 8; ++q) {
+                const float4 l4 = reinterpret_cast<const float4 *>(Lt)[q];
+                const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int k = 4 * q + u;
+                    if (k > t) x[k] = fmaf(x[t], lv[u], x[k]);  // x[k] holds -(...)
+                }
+            }
+        }
+        if (live) {
+            float *out = Ab + R + (int64_t)(c0 + 32 * j) * lda;
+#pragma unroll
+            for (int t = 0; t < 32; ++t) out[(int64_t)t * lda] = x[t];
+        }
+        if (j == 3) break;
+        // X_j as the A operand (K-major, hi/lo)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            float h[4], l[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) tc::split_tf32(x[4 * q + u], h[u], l[u]);
+            const uint32_t off = core_off(tid, q);
+            *reinterpret_cast<float4 *>(smem + kOffX + off) = make_float4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<float4 *>(smem + kOffX + kXTile + off) =
+                make_float4(l[0], l[1], l[2], l[3]);
+        }
+        tc::fence_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+        if (tid == 0) {
+            // -A[:, 32(j+1):] += X_j L_{k,j}^T   (M = 128, N = 96 - 32j, K = 32)
+            const uint32_t N = lt_rows(j);
+            const uint32_t idesc = tc::idesc_tf32(128, N);
+            const uint32_t xh = sbase + kOffX, xl = xh + kXTile;
+            const uint32_t bh = sbase + kOffLt + lt_off(j), bl = bh + N / 8 * kSbo;
+            const uint32_t d = tmem + 32 * (j + 1);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                const uint32_t ko = ks * 2 * kLbo;
+                tc::mma_tf32(d, tc::smem_desc(xh + ko, kLbo, kSbo),
+                             tc::smem_desc(bh + ko, kLbo, kSbo), idesc, 1u);
+                tc::mma_tf32(d, tc::smem_desc(xh + ko, kLbo, kSbo),
+                             tc::smem_desc(bl + ko, kLbo, kSbo), idesc, 1u);
+                tc::mma_tf32(d, tc::smem_desc(xl + ko, kLbo, kSbo),
+                             tc::smem_desc(bh + ko, kLbo, kSbo), idesc, 1u);
+            }
+            tc::mma_commit(&mbar);
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, 128);
+    if (tid == 0 && sh_err) info[mat] = -1;
+}
+
+std::once_flag g_once;
+cudaError_t g_attr = cudaSuccess;
+
+}  // namespace
+
+// Returns 0 after launching, 1 when the caller must use the FP32 kernel
+// (unaligned panels), or a cudaError_t.
+int launch_trsm_tc(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
+                   cudaStream_t stream)
+{
+    if (((reinterpret_cast<uintptr_t>(A) & 15) != 0) || (lda & 3) || (strideA & 3)) return 1;
+    std::call_once(g_once, [] {
+        g_attr = cudaFuncSetAttribute(trsm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      kSmemBytes);
+    });
+    if (g_attr != cudaSuccess) return (int)g_attr;
+    const int m = n - c0 - 128;
+    dim3 grid((unsigned)batch, (unsigned)((m + 127) / 128));
+    trsm_tc_kernel<<<grid, 128, kSmemBytes, stream>>>(A, n, lda, strideA, c0, info);
+    return (int)cudaGetLastError();
+}
+
+}  // namespace bl
