@@ -10,15 +10,17 @@
 // Schedule (right-looking, one panel per step, after the inner-blocked
 // schedule of "kernelbot-cholesky-930185", chol_diag_b kernel comment: the
 // barriers, not the FMAs, are the critical path, so spend work to save them):
-//   1. warp 0 factors the 32 x 32 diagonal block alone, lane = row, with the
-//      same broadcast-column step as K1 (no block barrier inside);
+//   1. one warp factors the 32 x 32 diagonal block alone, lane = row, with the
+//      same broadcast-column step as K1 (no block barrier inside); which warp
+//      rotates with the panel and the block index, so the serial factors of
+//      co-resident blocks spread over the SM's four sub-partitions;
 //   2. every thread solves one row of the panel below it against that block,
 //      P <- P L11^{-T}, reading L11's columns as 16-byte broadcasts
 //      (the trsm_panel kernel of the same page: one thread per row);
 //   3. every thread updates 4 x 4 tiles of the trailing LOWER triangle only,
 //      A22 <- A22 - L21 L21^T (the page's left-looking driver note measured a
 //      full-square trailing update as doubling the flops): first the next
-//      panel's columns, then (look-ahead) warp 0 factors the next diagonal
+//      panel's columns, then (look-ahead) one warp factors the next diagonal
 //      block while the other warps update the remaining columns;
 // with one __syncthreads after each phase. Rows and columns n .. NP-1 are an
 // identity block. Entries above the diagonal inside a diagonal block of the
@@ -294,7 +296,13 @@ potrf_cta_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int bat
     // of p; the trailing update of the next panel's 32 columns; then warp 0
     // factors the next diagonal block while the other warps update the rest
     // of the trailing triangle (columns the next panel solve does not read).
-    if (warp == 0) factor_diag_block(S, Gm::ld(0), lane, 0, n, colbuf, sinv, &sh_fail);
+    // The warp that factors a diagonal block rotates with the panel and the
+    // block index: a warp runs on SM sub-partition (warp % 4), and a fixed
+    // choice would queue the serial factor of every co-resident block on the
+    // same sub-partition.
+    constexpr int NW = NT / 32;
+    const int rot = (int)(blockIdx.x % NW);
+    if (warp == rot) factor_diag_block(S, Gm::ld(0), lane, 0, n, colbuf, sinv, &sh_fail);
     __syncthreads();
 #pragma unroll 1
     for (int p = 0; p < NB && !sh_fail; ++p) {
@@ -315,12 +323,14 @@ potrf_cta_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int bat
             if (I >= K) syrk_tile<NB>(S, P, ldp, c0, c1, I, K);
         }
         __syncthreads();
-        if (warp == 0) {
+        const int dw = (p + 1 + rot) % NW;
+        if (warp == dw) {
             factor_diag_block(S + Gm::off(p + 1), Gm::ld(p + 1), lane, c1, n, colbuf, sinv,
                               &sh_fail);
         } else {
             const int T2 = T - 8;  // tile columns 8 .. T-1, column-major order
-            for (int t = tid - 32; t < T2 * (T2 + 1) / 2; t += NT - 32) {
+            const int rank = (warp - dw - 1 + NW) % NW;  // among the other warps
+            for (int t = 32 * rank + lane; t < T2 * (T2 + 1) / 2; t += NT - 32) {
                 int a, b;
                 tri_index(t, a, b);
                 const int I = 8 + (T2 - 1 - b), K = 8 + (T2 - 1 - a);

@@ -47,30 +47,14 @@ __device__ __forceinline__ uint32_t core_off(int r, int q)
 // The lower triangle is first copied into shared memory in the packed panel
 // layout of K2 (panel p keeps rows 32p .. 127 of its 32 columns, column-major,
 // leading dimension 128 - 32p; 40 KB), every copy in flight at once.
-__device__ __forceinline__ int pk_off(int r, int k)
-{
-    const int p = k >> 5;
-    return 32 * (p * 128 - 32 * (p * (p - 1) / 2)) + (r - 32 * p) + (k - 32 * p) * (128 - 32 * p);
-}
-
-// 32 entries of row `row`, columns col0 .. col0+31, negated, from the packed
-// copy (lower triangle of A; identity beyond n).
-__device__ __forceinline__ void row_chunk(const float *S, int n, int row, int col0, float (&v)[32])
-{
-#pragma unroll
-    for (int c = 0; c < 32; ++c) {
-        const int col = col0 + c;
-        float x = (row == col) ? -1.0f : 0.0f;
-        if (row < n && col <= row) x = -S[pk_off(row, col)];
-        v[c] = x;
-    }
-}
+__host__ __device__ constexpr int pk_base(int p) { return 32 * (p * 128 - 32 * (p * (p - 1) / 2)); }
+__host__ __device__ constexpr int pk_ld(int p) { return 128 - 32 * p; }
 
 __global__ void __launch_bounds__(128, 4)
 potrf_tmem_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int batch,
                   int *__restrict__ info, int info_off)
 {
-    extern __shared__ __align__(128) uint8_t smem[];      // operand tiles: hi, lo
+    extern __shared__ __align__(128) uint8_t smem[];      // packed copy, then operand tiles
     __shared__ __align__(16) float Ls[32 * 32];            // Ls[j*32 + k] = L(c0+k, c0+j)
     __shared__ __align__(16) float colbuf[2][32];
     __shared__ __align__(16) float sinv[32];
@@ -82,8 +66,19 @@ potrf_tmem_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int ba
     if (info_off >= 0 && info[mat] != 0) return;  // failed at an earlier panel
     float *__restrict__ Ab = A + mat * strideA;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int row = tid;
     const int NB = (n + 31) >> 5;
+    // Row and column blocks are rotated against the TMEM lane quarters and
+    // column blocks by rot: matrix block b lives in quarter / column block
+    // (b + rot) % 4. Warp w (which may only address lane quarter w, and runs
+    // on SM sub-partition w) therefore holds matrix row block (w - rot) % 4,
+    // and the warp that factors panel p changes from block to block, so the
+    // serial diagonal factors of co-resident blocks do not queue on one
+    // sub-partition. The operand tile rows follow the TMEM lanes, so both MMA
+    // operands see the same permutation.
+    const int rot = (int)(blockIdx.x & 3);
+    const int rb = (warp - rot) & 3;   // this warp's matrix row block
+    const int row = 32 * rb + lane;    // this thread's matrix row
+    auto tcol = [rot](int b) { return 32 * ((b + rot) & 3); };  // TMEM column of block b
 
     if (tid == 0) {
         sh_fail = 0;
@@ -96,41 +91,61 @@ potrf_tmem_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int ba
         tc::tmem_alloc(&tmem_base, 128);
         tc::tmem_relinquish();
     }
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    const uint32_t tmem = tmem_base;
-    const uint32_t tlane = tmem + ((uint32_t)(32 * warp) << 16);
 
     // -A into TMEM: copy the lower triangle into shared memory (column k by
-    // one warp), then warp w moves its rows' chunks 0 .. w into TMEM
+    // one warp; 16-byte copies when aligned), then every thread moves its
+    // row's chunks (column blocks 0 .. rb) into TMEM
     {
         float *S = reinterpret_cast<float *>(smem);
+        const bool vec = ((reinterpret_cast<uintptr_t>(Ab) & 15) == 0) && ((lda & 3) == 0);
         for (int k = warp; k < n; k += 4) {
+            const int pk = k >> 5;
+            float *col = S + pk_base(pk) + (k - 32 * pk) * pk_ld(pk) - 32 * pk;  // col[r]
             const float *g = Ab + (int64_t)k * lda;
-            for (int r = k + lane; r < n; r += 32) cp_async4(S + pk_off(r, k), g + r);
+            int qa = n, qb = n;
+            if (vec) {
+                qa = (k + 3) & ~3;
+                qb = n & ~3;
+                if (qb < qa) qa = qb = n;
+            }
+            for (int q = qa + 4 * lane; q < qb; q += 128) cp_async16(col + q, g + q);
+            for (int r = k + lane; r < n; r += 32)
+                if (r < qa || r >= qb) cp_async4(col + r, g + r);
         }
         cp_async_commit();
         cp_async_wait<0>();
+        tc::fence_before_sync();
         __syncthreads();
-        const int nch = min(warp, NB - 1) + 1;
+        tc::fence_after_sync();
+        const uint32_t tlane0 = tmem_base + ((uint32_t)(32 * warp) << 16);
+        const int nch = min(rb, NB - 1) + 1;
 #pragma unroll 1
         for (int j = 0; j < nch; ++j) {
+            const float *src = S + pk_base(j) + (row - 32 * j);  // element (row, 32j + c)
+            const int ldj = pk_ld(j);
             float v[32];
-            row_chunk(S, n, row, 32 * j, v);
-            tc::tmem_st32(tlane + 32 * j, v);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const int col = 32 * j + c;
+                float x = (row == col) ? -1.0f : 0.0f;
+                if (row < n && col <= row) x = -src[c * ldj];
+                v[c] = x;
+            }
+            tc::tmem_st32(tlane0 + tcol(j), v);
         }
     }
     tc::fence_before_sync();
     __syncthreads();  // the shared copy is dead from here on (operand tiles reuse it)
     tc::fence_after_sync();
+    const uint32_t tmem = tmem_base;
+    const uint32_t tlane = tmem + ((uint32_t)(32 * warp) << 16);
 
-    // Trailing update of panel p in two MMA groups: group 0 updates the next
-    // panel's 32 columns and is committed to mbar[0] (the next panel waits only
-    // for it), group 1 the columns after those, committed to mbar[1] (waited
-    // for only before the operand tile is overwritten) - so the next diagonal
-    // factor runs while the bulk of the update is still on the tensor cores.
-    // One thread waits on an mbarrier; the others sleep at the block barrier.
+    // Trailing update of panel p: group 0 (mbar[0]) updates the next panel's
+    // 32 columns, which the next panel waits for; group 1 (mbar[1]) the
+    // columns after those, waited for only before the operand tile is
+    // overwritten - the next diagonal factor runs while it is still on the
+    // tensor cores. One MMA chain of N = 32 per column block. One thread waits
+    // on an mbarrier; the others sleep at the block barrier.
     const uint32_t sbase = tc::smem_u32(smem);
     int n0 = 0, n1 = 0;  // commits to mbar[0] / mbar[1] so far (same in every thread)
 #pragma unroll 1
@@ -144,12 +159,12 @@ potrf_tmem_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int ba
             tc::fence_after_sync();
         }
         float x[32];
-        if (warp >= p) {
-            tc::tmem_ld32(tlane + c0, x);
+        if (rb >= p) {
+            tc::tmem_ld32(tlane + tcol(p), x);
 #pragma unroll
             for (int k = 0; k < 32; ++k) x[k] = -x[k];
         }
-        if (warp == p) {
+        if (rb == p) {
             // diagonal block: lane = row c0 + lane, columns c0 .. c0+31
             float dm = 1.0f;
 #pragma unroll
@@ -179,19 +194,18 @@ potrf_tmem_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int ba
             for (int j = 0; j < 32; ++j)
                 if (j < lane) Ls[j * 32 + lane] = x[j];
             sinv[lane] = rsqrt_approx(dm);
-            const int r = c0 + lane;
-            if (r < n) {
+            if (row < n) {
 #pragma unroll
                 for (int k = 0; k < 32; ++k)
-                    if (k < lane) Ab[r + (int64_t)(c0 + k) * lda] = x[k];
-                Ab[r + (int64_t)r * lda] = sqrt_approx(dm);
+                    if (k < lane) Ab[row + (int64_t)(c0 + k) * lda] = x[k];
+                Ab[row + (int64_t)row * lda] = sqrt_approx(dm);
             }
-            const unsigned bad = __ballot_sync(0xffffffffu, r < n && !pivot_ok(dm));
+            const unsigned bad = __ballot_sync(0xffffffffu, row < n && !pivot_ok(dm));
             if (lane == 0 && bad) sh_fail = c0 + __ffs(bad);
         }
         __syncthreads();
         if (sh_fail) break;
-        if (warp > p) {
+        if (rb > p) {
             // x <- x L_pp^{-T}
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
@@ -220,16 +234,17 @@ potrf_tmem_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int ba
             __syncthreads();
             if (sh_err) break;
         }
-        // operand tile: rows > c0+31 carry L21 (split hi / lo), the rest zeros
+        // operand tile (row = TMEM lane): rows of blocks > p carry L21 split hi /
+        // lo, the rest zeros
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             float h[4], l[4];
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
-                if (warp > p) tc::split_tf32(x[4 * q + t], h[t], l[t]);
+                if (rb > p) tc::split_tf32(x[4 * q + t], h[t], l[t]);
                 else h[t] = l[t] = 0.0f;
             }
-            const uint32_t off = core_off(row, q);
+            const uint32_t off = core_off(tid, q);
             *reinterpret_cast<float4 *>(smem + off) = make_float4(h[0], h[1], h[2], h[3]);
             *reinterpret_cast<float4 *>(smem + kTileBytes + off) =
                 make_float4(l[0], l[1], l[2], l[3]);
@@ -238,32 +253,31 @@ potrf_tmem_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int ba
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
-        // -S[:, c:c+N] += L21 L21[c:c+N, :]^T  (M = 128 rows)
-        const int nrest = 128 - c1 - 32;
+        // -S[:, block b] += L21 L21[block b, :]^T for b = p+1 .. NB-1 (M = 128, N = 32)
+        const bool rest = p + 2 < NB;
         if (tid == 0) {
             const uint32_t a_hi = sbase, a_lo = sbase + kTileBytes;
+            const uint32_t idesc = tc::idesc_tf32(128, 32);
 #pragma unroll 1
-            for (int g = 0; g < 2; ++g) {
-                const int c = g == 0 ? c1 : c1 + 32;
-                const uint32_t N = g == 0 ? 32u : (uint32_t)nrest;
-                if (N == 0) break;
-                const uint32_t idesc = tc::idesc_tf32(128, N);
-                const uint32_t boff = (uint32_t)(c >> 3) * kSbo;
+            for (int b = p + 1; b < NB; ++b) {
+                const uint32_t tc_b = (uint32_t)tcol(b);
+                const uint32_t boff = (tc_b >> 3) * kSbo;  // tile rows of row block b
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
                     const uint32_t ko = ks * 2 * kLbo;
-                    tc::mma_tf32(tmem + c, tc::smem_desc(a_hi + ko, kLbo, kSbo),
+                    tc::mma_tf32(tmem + tc_b, tc::smem_desc(a_hi + ko, kLbo, kSbo),
                                  tc::smem_desc(a_hi + boff + ko, kLbo, kSbo), idesc, 1u);
-                    tc::mma_tf32(tmem + c, tc::smem_desc(a_hi + ko, kLbo, kSbo),
+                    tc::mma_tf32(tmem + tc_b, tc::smem_desc(a_hi + ko, kLbo, kSbo),
                                  tc::smem_desc(a_lo + boff + ko, kLbo, kSbo), idesc, 1u);
-                    tc::mma_tf32(tmem + c, tc::smem_desc(a_lo + ko, kLbo, kSbo),
+                    tc::mma_tf32(tmem + tc_b, tc::smem_desc(a_lo + ko, kLbo, kSbo),
                                  tc::smem_desc(a_hi + boff + ko, kLbo, kSbo), idesc, 1u);
                 }
-                tc::mma_commit(&mbar[g]);
+                if (b == p + 1) tc::mma_commit(&mbar[0]);
             }
+            if (rest) tc::mma_commit(&mbar[1]);
         }
         ++n0;
-        if (nrest > 0) ++n1;
+        if (rest) ++n1;
     }
 
     tc::fence_before_sync();
