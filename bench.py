@@ -40,6 +40,8 @@ REPLICA_CAP_BYTES = 96 << 30
 # changed source reports null. Filled from the summaries under profiles/.
 TRAFFIC = {
     # workload: (source file, sha256 prefix, bytes per launch, summary file)
+    "n64": ("matrix_dense_linear_gb300/csrc/potrf_warp.cu", "5e9bb36d30360aee", 12665088,
+            "profiles/potrf_warp64_n64_b1024.md"),
 }
 
 
