@@ -28,11 +28,13 @@
 #include <mutex>
 
 #include "bl_common.cuh"
+#include "tc_sm100.cuh"
 
 namespace bl {
 namespace {
 
 constexpr int kPad = 4;
+constexpr long long kWaitCycles = 2000000000LL;  // ~1 s
 
 template <int NB>
 struct CtaGeom {
@@ -55,9 +57,16 @@ __device__ __forceinline__ float *elem_ptr(float *S, int i, int k)
     return S + Gm::off(p) + (i - 32 * p) + (k - 32 * p) * Gm::ld(p);
 }
 
-// Step 1: factor the diagonal block of panel p in warp 0. P points at element
-// (c0, c0); ldp is the panel's leading dimension. Writes s_j = rsqrt(d_j) to
-// sinv and the first failing local pivot (c0 + j + 1) to *fail_out.
+// Step 1: factor the diagonal block of panel p in one warp, lane = row, with
+// the broadcast-column step of K1. P points at element (c0, c0); ldp is the
+// panel's leading dimension. Per column j every lane publishes r[j] to a
+// warp-private buffer, one __syncwarp, and reads the pivot d_j and the column
+// below it back as 16-byte broadcasts (from the quad holding d_j on); then
+// l = r[j] rsqrt(d_j) and r[k] -= (l rsqrt(d_j)) c_k for k > j. Lane j keeps
+// its pivot; at the end every lane writes s = rsqrt(d) of its column to sinv
+// and the first pivot with !(d > 0) is reported as c0 + j + 1 in *fail_out.
+// The diagonal entry l_jj = d_j rsqrt(d_j) is the square root of the pivot.
+// Columns from n on (the identity block) are left as they are.
 __device__ __forceinline__ void factor_diag_block(float *P, int ldp, int lane, int c0, int n,
                                                   float (*colbuf)[32], float *sinv,
                                                   int *fail_out)
@@ -65,35 +74,38 @@ __device__ __forceinline__ void factor_diag_block(float *P, int ldp, int lane, i
     float r[32];
 #pragma unroll
     for (int k = 0; k < 32; ++k) r[k] = P[lane + k * ldp];
-    int fail = 0;
+    float my_d = 1.0f;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
         if (c0 + j >= n) break;
         float *cb = colbuf[j & 1];
         cb[lane] = r[j];
         __syncwarp();
-        const float d = cb[j];
-        if (!pivot_ok(d) && fail == 0) fail = c0 + j + 1;
+        const float4 f4 = reinterpret_cast<const float4 *>(cb)[j / 4];
+        const float fv[4] = {f4.x, f4.y, f4.z, f4.w};
+        const float d = fv[j % 4];
+        my_d = (lane == j) ? d : my_d;
         const float s = rsqrt_approx(d);
         const float lij = r[j] * s;
         const float w = lij * s;
-        r[j] = (lane == j) ? sqrt_approx(d) : lij;
-        if (lane == j) sinv[j] = s;
+        r[j] = lij;
 #pragma unroll
-        for (int q = (j + 1) / 4; q < 8; ++q) {
+        for (int t = j % 4 + 1; t < 4; ++t) r[4 * (j / 4) + t] = fmaf(-w, fv[t], r[4 * (j / 4) + t]);
+#pragma unroll
+        for (int q = j / 4 + 1; q < 8; ++q) {
             const float4 c4 = reinterpret_cast<const float4 *>(cb)[q];
-            const float cv[4] = {c4.x, c4.y, c4.z, c4.w};
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                const int k = 4 * q + t;
-                if (k > j) r[k] = fmaf(-w, cv[t], r[k]);
-            }
+            r[4 * q] = fmaf(-w, c4.x, r[4 * q]);
+            r[4 * q + 1] = fmaf(-w, c4.y, r[4 * q + 1]);
+            r[4 * q + 2] = fmaf(-w, c4.z, r[4 * q + 2]);
+            r[4 * q + 3] = fmaf(-w, c4.w, r[4 * q + 3]);
         }
     }
 #pragma unroll
     for (int k = 0; k < 32; ++k)
         if (k <= lane) P[lane + k * ldp] = r[k];
-    if (lane == 0 && fail) *fail_out = fail;
+    sinv[lane] = rsqrt_approx(my_d);
+    const unsigned bad = __ballot_sync(0xffffffffu, !pivot_ok(my_d));
+    if (lane == 0 && bad) *fail_out = c0 + __ffs(bad);
 }
 
 // Step 2: row a (>= 32, panel coordinates) of panel p: x <- x L11^{-T}.
@@ -102,9 +114,11 @@ __device__ __forceinline__ void trsm_row(float *P, int ldp, int a, const float *
     float x[32];
 #pragma unroll
     for (int k = 0; k < 32; ++k) x[k] = P[a + k * ldp];
+    float4 s4;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
-        x[j] *= sinv[j];
+        if (j % 4 == 0) s4 = reinterpret_cast<const float4 *>(sinv)[j / 4];
+        x[j] *= (j % 4 == 0) ? s4.x : (j % 4 == 1) ? s4.y : (j % 4 == 2) ? s4.z : s4.w;
         const float *Lj = P + j * ldp;  // column j of L11, rows 0..31
 #pragma unroll
         for (int q = (j + 1) / 4; q < 8; ++q) {
@@ -212,44 +226,55 @@ __device__ __forceinline__ void store_columns(const float *S, float *Ab, int n, 
 }
 
 // The same two copies for the common exact case n = NP with 16-byte aligned
-// columns: column j's rows j .. NP-1 are its 0-3 leading rows (4-byte copies
-// by lanes 0..2) and whole quads from ceil4(j) on (one 16-byte copy per lane;
-// NP <= 128 is at most 32 quads). No identity block, no ragged tail.
-template <int NB, int NT>
-__device__ __forceinline__ void load_columns_full(float *S, const float *Ab, int lda, int k0,
-                                                  int k1, int warp, int lane)
+// columns, by the bulk-copy engine: thread k moves column k, rows ceil4(k) ..
+// NP-1 as one bulk copy (16-byte aligned on both sides) and its 0-3 leading
+// rows k .. ceil4(k)-1 with plain loads and stores. Loads complete on mbar[0]
+// (columns 0..31, arrival count 32) and mbar[1] (the rest, NP-32).
+template <int NB>
+__device__ __forceinline__ void bulk_load_full(float *S, const float *Ab, int lda, int tid,
+                                               uint64_t *mbar)
 {
     constexpr int NP = CtaGeom<NB>::NP;
-#pragma unroll 4
-    for (int k = k0 + warp; k < k1; k += NT / 32) {
-        float *col = elem_ptr<NB>(S, 0, k);
-        const float *g = Ab + (int64_t)k * lda;
-        const int q0 = (k + 3) & ~3;
-        const int q = q0 + 4 * lane;
-        if (q < NP) cp_async16(col + q, g + q);
-        if (k + lane < q0) cp_async4(col + k + lane, g + k + lane);
-    }
+    if (tid >= NP) return;
+    const int k = tid, q0 = (k + 3) & ~3;
+    const float *g = Ab + (int64_t)k * lda;
+    float *col = elem_ptr<NB>(S, 0, k);  // col[i] = element (i, k)
+    uint64_t *bar = mbar + (k < 32 ? 0 : 1);
+    const uint32_t bytes = 4u * (uint32_t)(NP - q0);
+    tc::mbar_arrive_expect_tx(bar, bytes);
+    if (bytes) tc::bulk_g2s(col + q0, g + q0, bytes, bar);
+    const int m = q0 - k;  // 0..3 leading rows (q0 <= NP)
+    if (m > 0) col[k] = g[k];
+    if (m > 1) col[k + 1] = g[k + 1];
+    if (m > 2) col[k + 2] = g[k + 2];
 }
 
-template <int NB, int NT>
-__device__ __forceinline__ void store_columns_full(const float *S, float *Ab, int lda, int warp,
-                                                   int lane)
+template <int NB>
+__device__ __forceinline__ void bulk_store_full(const float *S, float *Ab, int lda, int tid)
 {
     constexpr int NP = CtaGeom<NB>::NP;
-#pragma unroll 4
-    for (int k = warp; k < NP; k += NT / 32) {
-        const float *col = elem_ptr<NB>(const_cast<float *>(S), 0, k);
-        float *g = Ab + (int64_t)k * lda;
-        const int q0 = (k + 3) & ~3;
-        const int q = q0 + 4 * lane;
-        if (q < NP)
-            *reinterpret_cast<float4 *>(g + q) = *reinterpret_cast<const float4 *>(col + q);
-        if (k + lane < q0) g[k + lane] = col[k + lane];
+    if (tid >= NP) return;
+    const int k = tid, q0 = (k + 3) & ~3;
+    float *g = Ab + (int64_t)k * lda;
+    const float *col = elem_ptr<NB>(const_cast<float *>(S), 0, k);
+    const uint32_t bytes = 4u * (uint32_t)(NP - q0);
+    if (bytes) {
+        tc::bulk_s2g(g + q0, col + q0, bytes);
+        tc::bulk_commit();
     }
+    const int m = q0 - k;
+    if (m > 0) g[k] = col[k];
+    if (m > 1) g[k + 1] = col[k + 1];
+    if (m > 2) g[k + 2] = col[k + 2];
+    if (bytes) tc::bulk_wait_read0();  // the block's shared memory outlives the reads
 }
 
-template <int NB, int NT>
-__global__ void __launch_bounds__(NT)
+// FULL: n == NP and 16-byte aligned columns (the launcher checks): bulk copies.
+// At n = 128 a thread gets 128 registers and four blocks share an SM: measured
+// on GB300 that beats five blocks at 96 registers (60 against 67 us for 1024
+// matrices).
+template <int NB, int NT, bool FULL>
+__global__ void __launch_bounds__(NT, NB >= 3 ? 4 : 8)
 potrf_cta_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int batch,
                  int *__restrict__ info, int info_off)
 {
@@ -258,7 +283,8 @@ potrf_cta_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int bat
     extern __shared__ __align__(16) float S[];
     __shared__ __align__(16) float colbuf[2][32];
     __shared__ __align__(16) float sinv[32];
-    __shared__ int sh_fail;
+    __shared__ __align__(8) uint64_t mbar[2];  // bulk loads: panel 0, the rest
+    __shared__ int sh_fail, sh_err;
 
     const int64_t mat = blockIdx.x;
     pdl_wait();
@@ -267,29 +293,35 @@ potrf_cta_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int bat
     float *__restrict__ Ab = A + mat * strideA;
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    if (tid == 0) sh_fail = 0;
 
-    // Load. Column k is copied by one warp straight into shared memory with
-    // asynchronous copies, 16 bytes at a time where both sides are aligned
-    // (A, lda and strideA multiples of 4 floats) and 4 bytes at the ragged
-    // ends, so every copy of the matrix is in flight at once. Panel 0 is the
-    // first copy group: it is factored while the rest is still arriving.
-    // Rows n .. NP-1 are an identity block written directly.
+    // Load. 16-byte aligned batches (A, lda and strideA multiples of 4 floats)
+    // of exact order n = NP take the bulk-copy path (one copy per column, all
+    // in flight at once); otherwise column k is copied by one warp with
+    // asynchronous 16-byte copies where both sides are aligned and 4-byte ones
+    // at the ragged ends, and rows n .. NP-1 get the identity block. Either
+    // way panel 0 is the first group: it is factored while the rest arrives.
     const bool vec = ((reinterpret_cast<uintptr_t>(A) & 15) == 0) && ((lda & 3) == 0) &&
                      ((strideA & 3) == 0);
-    const bool full = vec && n == NP;
-    if (full) {
-        load_columns_full<NB, NT>(S, Ab, lda, 0, 32, warp, lane);
-        cp_async_commit();
-        load_columns_full<NB, NT>(S, Ab, lda, 32, NP, warp, lane);
-        cp_async_commit();
+    if (tid == 0) {
+        sh_fail = 0;
+        sh_err = 0;
+        if constexpr (FULL) {
+            tc::mbar_init(&mbar[0], 32);
+            if (NB > 1) tc::mbar_init(&mbar[1], NP - 32);
+            tc::fence_mbar_init();
+        }
+    }
+    __syncthreads();
+    if constexpr (FULL) {
+        bulk_load_full<NB>(S, Ab, lda, tid, mbar);
+        if (tid == 0 && !tc::mbar_wait(&mbar[0], 0, kWaitCycles)) sh_err = 1;
     } else {
         load_columns<NB, NT>(S, Ab, n, lda, 0, 32, vec, warp, lane);
         cp_async_commit();
         load_columns<NB, NT>(S, Ab, n, lda, 32, NP, vec, warp, lane);
         cp_async_commit();
+        cp_async_wait<1>();
     }
-    cp_async_wait<1>();
     __syncthreads();
 
     // Panel 0's diagonal block, then per panel p (look-ahead): the panel solve
@@ -302,18 +334,22 @@ potrf_cta_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int bat
     // same sub-partition.
     constexpr int NW = NT / 32;
     const int rot = (int)(blockIdx.x % NW);
-    if (warp == rot) factor_diag_block(S, Gm::ld(0), lane, 0, n, colbuf, sinv, &sh_fail);
+    if (warp == rot && !sh_err) factor_diag_block(S, Gm::ld(0), lane, 0, n, colbuf, sinv, &sh_fail);
     __syncthreads();
 #pragma unroll 1
-    for (int p = 0; p < NB && !sh_fail; ++p) {
+    for (int p = 0; p < NB && !sh_fail && !sh_err; ++p) {
         const int c0 = 32 * p;
         const int c1 = c0 + 32;
         if (c1 >= n) break;
         float *P = S + Gm::off(p);
         const int ldp = Gm::ld(p);
         for (int a = 32 + tid; a < NP - c0; a += NT) trsm_row(P, ldp, a, sinv);
-        if (p == 0) cp_async_wait<0>();  // the trailing columns have arrived
+        if (p == 0) {  // the trailing columns have arrived
+            if constexpr (!FULL) cp_async_wait<0>();
+            else if (tid == 0 && !tc::mbar_wait(&mbar[1], 0, kWaitCycles)) sh_err = 1;
+        }
         __syncthreads();
+        if (sh_err) break;
         // 4 x 4 tiles of the trailing triangle (rows/cols from c1), T per side;
         // consecutive threads take consecutive tile rows of one tile column
         const int T = (NP - c1) / 4;
@@ -340,10 +376,31 @@ potrf_cta_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int bat
         __syncthreads();
     }
 
-    cp_async_wait<0>();  // a failed panel 0 leaves the loop before the first wait
-    __syncthreads();
-    if (full) store_columns_full<NB, NT>(S, Ab, lda, warp, lane);
-    else store_columns<NB, NT>(S, Ab, n, lda, vec, warp, lane);
+    if (sh_err) {
+        // a bulk load never completed: report it, and give the copies a last
+        // bounded chance to land before the shared memory is released
+        if (tid == 0) {
+            tc::mbar_wait(&mbar[0], 0, kWaitCycles);
+            if (NB > 1) tc::mbar_wait(&mbar[1], 0, kWaitCycles);
+            info[mat] = -1;
+        }
+        return;
+    }
+    if constexpr (FULL) {
+        // a failed panel 0 leaves the loop before the second wait
+        if (NB > 1 && tid == 0 && !tc::mbar_wait(&mbar[1], 0, kWaitCycles)) sh_err = 1;
+        tc::fence_async_smem();  // this thread's shared-memory writes -> bulk stores
+        __syncthreads();
+        if (sh_err) {
+            if (tid == 0) info[mat] = -1;
+            return;
+        }
+        bulk_store_full<NB>(S, Ab, lda, tid);
+    } else {
+        cp_async_wait<0>();  // a failed panel 0 leaves the loop before the first wait
+        __syncthreads();
+        store_columns<NB, NT>(S, Ab, n, lda, vec, warp, lane);
+    }
     if (tid == 0) {
         const int f = sh_fail;
         if (info_off < 0) info[mat] = f;
@@ -351,28 +408,40 @@ potrf_cta_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int bat
     }
 }
 
-template <int NB, int NT>
-int launch_nb(float *A, int n, int lda, int64_t strideA, int batch, int *info, cudaStream_t st,
-              int info_off)
+template <int NB, int NT, bool FULL>
+int launch_v(float *A, int n, int lda, int64_t strideA, int batch, int *info, cudaStream_t st,
+             int info_off)
 {
     constexpr int bytes = CtaGeom<NB>::bytes;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(potrf_cta_kernel<NB, NT>,
+        attr_err = cudaFuncSetAttribute(potrf_cta_kernel<NB, NT, FULL>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     });
     if (attr_err != cudaSuccess) return (int)attr_err;
-    return launch_pdl(potrf_cta_kernel<NB, NT>, dim3((unsigned)batch), dim3(NT), (size_t)bytes,
-                      st, A, n, lda, strideA, batch, info, info_off);
+    return launch_pdl(potrf_cta_kernel<NB, NT, FULL>, dim3((unsigned)batch), dim3(NT),
+                      (size_t)bytes, st, A, n, lda, strideA, batch, info, info_off);
 }
 
+template <int NB, int NT>
+int launch_nb(float *A, int n, int lda, int64_t strideA, int batch, int *info, cudaStream_t st,
+              int info_off)
+{
+    const bool vec = ((reinterpret_cast<uintptr_t>(A) & 15) == 0) && ((lda & 3) == 0) &&
+                     ((strideA & 3) == 0);
+    if (vec && n == CtaGeom<NB>::NP)
+        return launch_v<NB, NT, true>(A, n, lda, strideA, batch, info, st, info_off);
+    return launch_v<NB, NT, false>(A, n, lda, strideA, batch, info, st, info_off);
+}
+
+// the n = NP bulk-copy kernel (the one the n = 128 and blocked workloads run)
 template <int NB, int NT>
 int attrs_nb(cudaFuncAttributes *fa, int *threads, int *dyn)
 {
     *threads = NT;
     *dyn = CtaGeom<NB>::bytes;
-    return (int)cudaFuncGetAttributes(fa, potrf_cta_kernel<NB, NT>);
+    return (int)cudaFuncGetAttributes(fa, potrf_cta_kernel<NB, NT, true>);
 }
 
 }  // namespace

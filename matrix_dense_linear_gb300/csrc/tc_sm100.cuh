@@ -133,6 +133,40 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *mbar, uint32_t parity, long 
 // 32 lanes x 32 columns of 32-bit values from tensor memory: thread i of the
 // warp receives lane (lane_base + i), columns col .. col+31. The warp may only
 // address its own 32-lane quarter (lane_base = 32 * (warp % 4)).
+// Arrive on an mbarrier and add `bytes` to the transaction count of its
+// current phase (bytes may be 0: a plain arrive).
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *mbar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 ::"r"(smem_u32(mbar)), "r"(bytes) : "memory");
+}
+
+// Bulk (non-tensor) asynchronous copy global -> shared of `bytes` bytes
+// (both addresses 16-byte aligned, bytes a multiple of 16), completing on
+// the mbarrier as transaction bytes.
+__device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src, uint32_t bytes,
+                                         uint64_t *mbar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes"
+                 " [%0], [%1], %2, [%3];"
+                 ::"r"(smem_u32(dst_smem)), "l"(src), "r"(bytes), "r"(smem_u32(mbar))
+                 : "memory");
+}
+
+// Bulk asynchronous copy shared -> global (same alignment rules), tracked by
+// the issuing thread's bulk groups.
+__device__ __forceinline__ void bulk_s2g(void *dst, const void *src_smem, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 ::"l"(dst), "r"(smem_u32(src_smem)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// wait until the shared-memory sources of this thread's bulk stores have been read
+__device__ __forceinline__ void bulk_wait_read0()
+{
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
 {
     uint32_t r[32];
