@@ -80,7 +80,7 @@ def dominant_kernel(n: int) -> str:
         return "potrf_warp64_kernel"
     if n <= 128:
         return "potrf_cta_kernel"
-    return "syrk_tile_kernel"
+    return "syrk_tc_kernel"  # the trailing update of 16-byte aligned batches
 
 
 def kernel_source(n: int) -> str:
@@ -89,7 +89,7 @@ def kernel_source(n: int) -> str:
         return os.path.join(d, "potrf_warp.cu")
     if n <= 128:
         return os.path.join(d, "potrf_cta.cu")
-    return os.path.join(d, "potrf_blocked.cu")
+    return os.path.join(d, "syrk_tc.cu")
 
 
 def traffic_for(name: str, n: int):

@@ -64,9 +64,9 @@ __device__ __forceinline__ float *elem_ptr(float *S, int i, int k)
 // below it back as 16-byte broadcasts (from the quad holding d_j on); then
 // l = r[j] rsqrt(d_j) and r[k] -= (l rsqrt(d_j)) c_k for k > j. Lane j keeps
 // its pivot; at the end every lane writes s = rsqrt(d) of its column to sinv
-// and the first pivot with !(d > 0) is reported as c0 + j + 1 in *fail_out.
-// The diagonal entry l_jj = d_j rsqrt(d_j) is the square root of the pivot.
-// Columns from n on (the identity block) are left as they are.
+// and the first pivot with !(d > 0) is reported as c0 + j + 1 in *fail_out;
+// the diagonal entry is sqrt(d_j). Columns from n on (the identity block) are
+// left as they are.
 __device__ __forceinline__ void factor_diag_block(float *P, int ldp, int lane, int c0, int n,
                                                   float (*colbuf)[32], float *sinv,
                                                   int *fail_out)
@@ -102,7 +102,9 @@ __device__ __forceinline__ void factor_diag_block(float *P, int ldp, int lane, i
     }
 #pragma unroll
     for (int k = 0; k < 32; ++k)
-        if (k <= lane) P[lane + k * ldp] = r[k];
+        if (k < lane) P[lane + k * ldp] = r[k];
+    // the diagonal from the lane's own pivot (sqrt(+Inf) = +Inf, like the definition)
+    if (c0 + lane < n) P[lane + lane * ldp] = sqrt_approx(my_d);
     sinv[lane] = rsqrt_approx(my_d);
     const unsigned bad = __ballot_sync(0xffffffffu, !pivot_ok(my_d));
     if (lane == 0 && bad) *fail_out = c0 + __ffs(bad);

@@ -12,8 +12,11 @@
 // tensor memory. Three quarters of the flops run on the tensor cores; only the
 // 32-column triangular solves stay on the FP32 pipes.
 //
-// Needs 16-byte aligned panels (the caller falls back to the FP32 kernel
-// otherwise). Every wait is bounded; a block that gives up marks info = -1.
+// The off-diagonal rows of L11 are staged one column block at a time (fetched
+// into registers while the previous block is solved), which keeps the block's
+// shared memory at 75 KB: three blocks share an SM. Needs 16-byte aligned
+// panels (the caller falls back to the FP32 kernel otherwise). Every wait is
+// bounded; a block that gives up marks info = -1.
 #include <mutex>
 
 #include "bl_common.cuh"
@@ -25,26 +28,76 @@ namespace {
 constexpr uint32_t kLbo = 128;
 constexpr uint32_t kSbo = 8 * 128 + 16;          // K = 32 per row group, +16 B (banks)
 constexpr uint32_t kXTile = 16 * kSbo;           // 128 rows
-// rows of L_{k,j} (k > j) for block j, and the byte offset of its hi/lo pair
-__host__ __device__ constexpr uint32_t lt_rows(int j) { return 96u - 32u * (uint32_t)j; }
-__host__ __device__ constexpr uint32_t lt_off(int j)
-{
-    return j == 0 ? 0u : (j == 1 ? 12u * kSbo * 2u : 20u * kSbo * 2u);
-}
-constexpr uint32_t kLtBytes = (12 + 8 + 4) * kSbo * 2;
+constexpr long long kWaitCycles = 2000000000LL;
+
+// rows of L_{k,j}, k > j, for column block j
+__host__ __device__ constexpr uint32_t lt_rows(int j) { return (uint32_t)(96 - 32 * j); }
+
+// Shared memory: the X operand (hi, lo); the off-diagonal rows of one column
+// block of L11 at a time (hi, lo; sized for block 0); the four diagonal
+// blocks; the reciprocal diagonal. 75 KB: three blocks share an SM.
 constexpr uint32_t kOffX = 0;
 constexpr uint32_t kOffLt = 2 * kXTile;
-constexpr uint32_t kOffLd = kOffLt + kLtBytes;   // diagonal blocks, 4 x 32 x 32 floats
+constexpr uint32_t kLtBytes = 2 * (lt_rows(0) / 8) * kSbo;
+constexpr uint32_t kOffLd = kOffLt + kLtBytes;
 constexpr uint32_t kOffRinv = kOffLd + 4 * 32 * 32 * 4;
 constexpr int kSmemBytes = (int)(kOffRinv + 128 * 4);
-constexpr long long kWaitCycles = 2000000000LL;
 
 __device__ __forceinline__ uint32_t core_off(int r, int q)
 {
     return (uint32_t)(r >> 3) * kSbo + (uint32_t)q * kLbo + (uint32_t)(r & 7) * 16;
 }
 
-__global__ void __launch_bounds__(128, 2)
+// Column block j of L11 below its diagonal block, L_{k,j} for k > j, in 4 x 4
+// pieces (rows i..i+3 of columns 4q..4q+3 of the block), row quads fastest so
+// that a warp's 16-byte loads run down one column. A thread owns pieces tid
+// and tid + 128: load() fetches them into registers, stage() splits them into
+// the K-major hi/lo operand tiles.
+struct LtPieces {
+    float4 v[2][4];
+    __device__ __forceinline__ void load(const float *L11, int lda, int j, int tid)
+    {
+        const int nrq = (int)lt_rows(j) / 4;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int b = tid + 128 * u;
+            if (b < nrq * 8) {
+                const int rq = b % nrq, q = b / nrq;
+                const float *src = L11 + 32 * (j + 1) + 4 * rq + (int64_t)(32 * j + 4 * q) * lda;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    v[u][c] = *reinterpret_cast<const float4 *>(src + (int64_t)c * lda);
+            }
+        }
+    }
+    __device__ __forceinline__ void stage(uint8_t *hi, int j, int tid) const
+    {
+        const int nrq = (int)lt_rows(j) / 4;
+        uint8_t *lo = hi + lt_rows(j) / 8 * kSbo;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int b = tid + 128 * u;
+            if (b < nrq * 8) {
+                const int rq = b % nrq, q = b / nrq;
+                const float cv[4][4] = {{v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w},
+                                        {v[u][1].x, v[u][1].y, v[u][1].z, v[u][1].w},
+                                        {v[u][2].x, v[u][2].y, v[u][2].z, v[u][2].w},
+                                        {v[u][3].x, v[u][3].y, v[u][3].z, v[u][3].w}};  // [k][row]
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float h[4], l[4];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) tc::split_tf32(cv[c][i], h[c], l[c]);
+                    const uint32_t off = core_off(4 * rq + i, q);
+                    *reinterpret_cast<float4 *>(hi + off) = make_float4(h[0], h[1], h[2], h[3]);
+                    *reinterpret_cast<float4 *>(lo + off) = make_float4(l[0], l[1], l[2], l[3]);
+                }
+            }
+        }
+    }
+};
+
+__global__ void __launch_bounds__(128, 3)
 trsm_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
                int *__restrict__ info)
 {
@@ -62,6 +115,7 @@ trsm_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     const float *L11 = Ab + c0 + (int64_t)c0 * lda;         // L11(i, k) = L11[i + k*lda]
     float *Ld = reinterpret_cast<float *>(smem + kOffLd);    // Ld[j*1024 + t*32 + k] = L(32j+k, 32j+t)
     float *rinv = reinterpret_cast<float *>(smem + kOffRinv);
+    uint8_t *Lt = smem + kOffLt;
 
     if (tid == 0) {
         sh_err = 0;
@@ -81,37 +135,10 @@ trsm_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     }
     cp_async_commit();
 
-    // off-diagonal row blocks L_{k,j} (k > j) as K-major hi/lo tiles: 4 x 4
-    // blocks (rows i..i+3, columns 4q..4q+3 of block j), 16-byte loads
-#pragma unroll 1
-    for (int b = tid; b < (24 + 16 + 8) * 8; b += 128) {
-        const int j = b < 192 ? 0 : (b < 320 ? 1 : 2);
-        const int bb = b - (j == 0 ? 0 : (j == 1 ? 192 : 320));
-        // row quads fastest: a warp's loads are 16-byte runs of one column and
-        // its stores land in distinct banks
-        const int nrq = (int)lt_rows(j) / 4;
-        const int rq = bb % nrq, q = bb / nrq;  // row quad within L_{.,j}, k quad
-        const int i0 = 32 * (j + 1) + 4 * rq;  // L11 row
-        float4 v[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-            v[c] = *reinterpret_cast<const float4 *>(L11 + i0 + (int64_t)(32 * j + 4 * q + c) * lda);
-        const float cv[4][4] = {{v[0].x, v[0].y, v[0].z, v[0].w},
-                                {v[1].x, v[1].y, v[1].z, v[1].w},
-                                {v[2].x, v[2].y, v[2].z, v[2].w},
-                                {v[3].x, v[3].y, v[3].z, v[3].w}};  // [k][row]
-        uint8_t *hi = smem + kOffLt + lt_off(j);
-        uint8_t *lo = hi + lt_rows(j) / 8 * kSbo;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float h[4], l[4];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tc::split_tf32(cv[c][i], h[c], l[c]);
-            const uint32_t off = core_off(4 * rq + i, q);
-            *reinterpret_cast<float4 *>(hi + off) = make_float4(h[0], h[1], h[2], h[3]);
-            *reinterpret_cast<float4 *>(lo + off) = make_float4(l[0], l[1], l[2], l[3]);
-        }
-    }
+    // the off-diagonal rows of column block 0
+    LtPieces pc;
+    pc.load(L11, lda, 0, tid);
+    pc.stage(Lt, 0, tid);
 
     tc::fence_before_sync();
     __syncthreads();
@@ -151,17 +178,21 @@ trsm_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
             __syncthreads();
             if (sh_err) break;
             tc::fence_after_sync();
+            // the operand tiles are free again: the off-diagonal rows of block j
+            if (j < 3) pc.stage(Lt, j, tid);
         }
+        // block j+1's off-diagonal rows travel while block j is solved
+        if (j + 1 < 3) pc.load(L11, lda, j + 1, tid);
         float x[32];
         tc::tmem_ld32(tlane + 32 * j, x);
         const float *Lj = Ld + j * 1024;
 #pragma unroll
         for (int t = 0; t < 32; ++t) {
             x[t] = -x[t] * rinv[32 * j + t];
-            const float *Lt = Lj + t * 32;
+            const float *Lt_ = Lj + t * 32;
 #pragma unroll
             for (int q = (t + 1) / 4; q < 8; ++q) {
-                const float4 l4 = reinterpret_cast<const float4 *>(Lt)[q];
+                const float4 l4 = reinterpret_cast<const float4 *>(Lt_)[q];
                 const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
@@ -196,7 +227,7 @@ trsm_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
             const uint32_t N = lt_rows(j);
             const uint32_t idesc = tc::idesc_tf32(128, N);
             const uint32_t xh = sbase + kOffX, xl = xh + kXTile;
-            const uint32_t bh = sbase + kOffLt + lt_off(j), bl = bh + N / 8 * kSbo;
+            const uint32_t bh = sbase + kOffLt, bl = bh + N / 8 * kSbo;
             const uint32_t d = tmem + 32 * (j + 1);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
@@ -218,8 +249,21 @@ trsm_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     if (tid == 0 && sh_err) info[mat] = -1;
 }
 
-std::once_flag g_once;
-cudaError_t g_attr = cudaSuccess;
+int launch_k(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
+             cudaStream_t stream)
+{
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(trsm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kSmemBytes);
+    });
+    if (attr != cudaSuccess) return (int)attr;
+    const int m = n - c0 - 128;
+    dim3 grid((unsigned)batch, (unsigned)((m + 127) / 128));
+    trsm_tc_kernel<<<grid, 128, kSmemBytes, stream>>>(A, n, lda, strideA, c0, info);
+    return (int)cudaGetLastError();
+}
 
 }  // namespace
 
@@ -229,15 +273,7 @@ int launch_trsm_tc(float *A, int n, int lda, int64_t strideA, int batch, int *in
                    cudaStream_t stream)
 {
     if (((reinterpret_cast<uintptr_t>(A) & 15) != 0) || (lda & 3) || (strideA & 3)) return 1;
-    std::call_once(g_once, [] {
-        g_attr = cudaFuncSetAttribute(trsm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      kSmemBytes);
-    });
-    if (g_attr != cudaSuccess) return (int)g_attr;
-    const int m = n - c0 - 128;
-    dim3 grid((unsigned)batch, (unsigned)((m + 127) / 128));
-    trsm_tc_kernel<<<grid, 128, kSmemBytes, stream>>>(A, n, lda, strideA, c0, info);
-    return (int)cudaGetLastError();
+    return launch_k(A, n, lda, strideA, batch, info, c0, stream);
 }
 
 }  // namespace bl
