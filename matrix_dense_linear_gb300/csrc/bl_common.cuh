@@ -102,6 +102,9 @@ int launch_tmem(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                 cudaStream_t stream, InfoMode mode);
 int launch_blocked(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                    cudaStream_t stream);
+// K2c: n = 128, A, lda and strideA 16-byte aligned (the caller checks)
+int launch_cta_tc(float *A, int lda, int64_t strideA, int batch, int *info, cudaStream_t stream,
+                  InfoMode mode);
 
 int launch_syrk_tc(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
                    cudaStream_t stream);
@@ -109,6 +112,7 @@ int attrs_syrk_tc(cudaFuncAttributes *fa);
 int launch_trsm_tc(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
                    cudaStream_t stream);
 
+int attrs_cta_tc(cudaFuncAttributes *fa, int *threads, int *dyn_smem);
 int attrs_warp(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem);
 int attrs_cta(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem);
 int attrs_tmem(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem);
