@@ -33,7 +33,6 @@ namespace {
 constexpr uint32_t kLbo = 128;               // K-adjacent core matrices
 constexpr uint32_t kSbo = 8 * 128 + 16;      // K = 32 per row group, +16 B (banks)
 constexpr uint32_t kTileBytes = 16 * kSbo;   // 128 rows
-constexpr int kOperandBytes = 2 * kTileBytes;  // hi, lo
 // requested dynamic shared memory: the operand tiles, padded so that at most
 // four blocks (4 x 128 TMEM columns = all 512) share an SM
 constexpr int kSmemBytes = 48 * 1024;
