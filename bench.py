@@ -7,6 +7,7 @@ the L2 was flushed. Prints ONE JSON line on rank 0.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload n64] [--no-per-n] [--no-cpu-baseline]
+  python bench.py --sweep     # batch sweep of the small orders, one JSON line per point
 
 The headline workload is n=64, batch=1024 (A = G G^T/64 + 0.1 I); `per_n`
 adds the same measurement for every workload (n = 32, 64, 128, 256, 1024).
@@ -294,13 +295,17 @@ def e2e_steps(w: DeviceWorkload, steps: int, warmup: int, barrier) -> dict:
     return {"ms": total, "h2d": bt.buf.nbytes, "d2h": bt.buf.nbytes + 4 * bt.batch}
 
 
-def oracle_rate(bt, seconds: float = 3.0, max_matrices: int | None = None) -> dict:
-    """The CPU oracle, as it stands, on the host cores: matrices/s on a bounded
-    sample (whole batch, or its first max_matrices), repeated >= `seconds`."""
+def oracle_rate(bt, seconds: float = 3.0, max_matrices: int | None = None,
+                nthreads: int | None = None) -> dict:
+    """The CPU oracle, as it stands, on the host cores (all, or nthreads):
+    matrices/s on a bounded sample (whole batch, or its first max_matrices),
+    repeated >= `seconds`."""
     import oracle
     m = bt.batch if max_matrices is None else min(bt.batch, max_matrices)
+    if nthreads == 1 and max_matrices is None:
+        m = min(m, 256)  # a bounded single-core sample
     idx = None if m == bt.batch else list(range(m))
-    th = oracle.default_threads()
+    th = oracle.default_threads() if nthreads is None else nthreads
     t0 = time.perf_counter()
     passes = 0
     while True:
@@ -376,6 +381,7 @@ def run_ours(args, rank: int, world: int, barrier) -> dict | None:
     info = w.info.cpu().numpy()
     assert not info.any(), "benchmark factorization reported failures"
 
+    lat_us = single_call_us(w) if rank == 0 else None
     e2e = e2e_steps(w, args.steps, min(args.warmup, 3), barrier)
     if world > 1:
         import torch.distributed as dist
@@ -417,10 +423,13 @@ def run_ours(args, rank: int, world: int, barrier) -> dict | None:
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "ms_per_step": e2e["ms"] / args.steps},
         "gpu_launches": nl * args.steps,
+        "single_call_us": lat_us,
         "clocks": sampler.summary(t_s0, t_s1) if sampler else None,
     }
     if args.cpu_baseline and world == 1:
         out["cpu_baseline"] = oracle_rate(bt, 3.0, oracle_sample_size(n))
+        one = oracle_rate(bt, 2.0, oracle_sample_size(n), nthreads=1)
+        out["cpu_baseline"]["one_core"] = {"value": one["value"], "sample": one["sample"]}
     del w
     torch.cuda.empty_cache()
 
@@ -459,6 +468,69 @@ def run_ours(args, rank: int, world: int, barrier) -> dict | None:
             torch.cuda.empty_cache()
         out["per_n"] = rows
     return out
+
+
+def single_call_us(w: DeviceWorkload, reps: int = 5) -> float:
+    """Latency of one call launched from the host (median over reps): events
+    around one launch on an idle stream, cold L2, replica untouched."""
+    import torch
+    st = torch.cuda.current_stream()
+    ts = []
+    for r in range(reps):
+        k = r % w.nrep
+        w.refresh(k)
+        w.flush_l2()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        w.call(k, st.cuda_stream)
+        e1.record(st)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3)
+    return statistics.median(ts)
+
+
+def run_sweep(args) -> list:
+    """Batch sweep of the latency-scale orders (n = 32, 64, 128) up to 65536
+    matrices: per point the median over 5 timed replays of K calls (graph,
+    cold replicas), the single-call latency and the roofline fraction. Batches
+    beyond a workload's own are the workload's matrices repeated."""
+    import torch
+
+    import matrix_dense_linear_gb300 as bl
+    bl.library()
+    dev = torch.device("cuda", 0)
+    pk = peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    rows = []
+    for name in ("n32", "n64", "n128"):
+        base = make_host_batch(name)
+        for batch in (1, 16, 152, 1024, 4096, 16384, 65536):
+            if name == "n128" and batch > 16384:
+                continue
+            reps = -(-batch // base.batch)
+            buf = np.tile(base.buf[: base.batch * base.strideA], reps)[: batch * base.strideA]
+            bt = type(base)(buf=np.ascontiguousarray(buf), n=base.n, lda=base.lda,
+                            strideA=base.strideA, batch=batch, fill=base.fill)
+            w = DeviceWorkload(bt, args.steps, dev)
+            for i in range(min(args.warmup, w.nrep)):
+                w.call(i, torch.cuda.current_stream().cuda_stream)
+            torch.cuda.synchronize()
+            k = min(args.steps, w.nrep)
+            ms = statistics.median(time_steps(w, k, lambda: None) / k for _ in range(5))
+            lat = single_call_us(w)
+            assert not w.info.cpu().numpy().any()
+            rf = roofline_entry(name, bt.n, batch, ms, pk, sms)
+            row = {"sweep": name, "n": bt.n, "batch": batch, "ms_per_call": ms,
+                   "single_call_us": lat, "matrices_per_s": batch / (ms / 1e3),
+                   "roofline": {k2: rf[k2] for k2 in ("bound", "frac", "roof_ms")},
+                   "calls_timed": k}
+            print(json.dumps(row), flush=True)
+            rows.append(row)
+            del w
+            torch.cuda.empty_cache()
+    return rows
 
 
 def run_reference(args) -> dict:
@@ -507,12 +579,18 @@ def main():
                     help="factor only the first B matrices of the workload (profiling)")
     ap.add_argument("--no-per-n", dest="per_n", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--sweep", action="store_true",
+                    help="batch sweep of n = 32, 64, 128 (one JSON line per point)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+
+    if args.sweep:
+        run_sweep(args)
+        return
 
     if args.impl == "reference":
         if rank == 0:
