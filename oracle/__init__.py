@@ -1,11 +1,12 @@
-"""CPU oracle for batched SPOTRF (lower, column-major, strided batch).
+"""CPU oracle for batched SPOTRF and SPOTRS (lower, column-major, strided batch).
 
 TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
 baseline leg of ``bench.py`` may import this package. The CUDA library never
 links, loads or calls it, and it never calls the CUDA library.
 
 The arithmetic lives in ``chol_ref.c`` (plain C, IEEE double, unblocked
-Cholesky-Crout); this module only compiles it with gcc into
+Cholesky-Crout) and ``potrs_ref.c`` (forward and backward substitution with the
+factor); this module only compiles them with gcc into
 ``oracle/_build/liboracle.so`` and marshals numpy arrays through ctypes.
 """
 from __future__ import annotations
@@ -19,7 +20,7 @@ from typing import Optional, Sequence
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "chol_ref.c")
+_SRCS = [os.path.join(_HERE, "chol_ref.c"), os.path.join(_HERE, "potrs_ref.c")]
 _BUILD = os.path.join(_HERE, "_build")
 _SO = os.path.join(_BUILD, "liboracle.so")
 _lock = threading.Lock()
@@ -30,12 +31,12 @@ def build(force: bool = False) -> str:
     """Compile the oracle (gcc, -O2, no FMA contraction). Returns the .so path."""
     with _lock:
         if (not force and os.path.exists(_SO)
-                and os.path.getmtime(_SO) >= os.path.getmtime(_SRC)):
+                and all(os.path.getmtime(_SO) >= os.path.getmtime(f) for f in _SRCS)):
             return _SO
         os.makedirs(_BUILD, exist_ok=True)
         tmp = _SO + f".tmp{os.getpid()}"
         cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
-               "-pthread", _SRC, "-o", tmp, "-lm"]
+               "-pthread", *_SRCS, "-o", tmp, "-lm"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _SO)
         return _SO
@@ -52,6 +53,15 @@ def _load():
         lib.oracle_potrf_batched.argtypes = [
             ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
             ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int]
+        lib.oracle_potrs_one.restype = None
+        lib.oracle_potrs_one.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_void_p, ctypes.c_int]
+        lib.oracle_potrs_batched.restype = ctypes.c_int
+        lib.oracle_potrs_batched.argtypes = [
+            ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_void_p,
+            ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
+            ctypes.c_int64, ctypes.c_int]
         _lib = lib
     return _lib
 
@@ -100,3 +110,51 @@ def potrf_batched(buf: np.ndarray, n: int, lda: int, strideA: int, batch: int,
     used = lib.oracle_potrf_batched(src.ctypes.data, n, lda, sA, m, L.ctypes.data,
                                     n * n, info.ctypes.data, th)
     return L.transpose(0, 2, 1), info, int(used)
+
+
+def potrs_one(L: np.ndarray, B: np.ndarray) -> np.ndarray:
+    """Solve (L L^T) X = B for one factor (only its lower triangle is used).
+
+    ``L`` (n x n) and ``B`` (n x nrhs, or a vector) are rounded to float32
+    first (the oracle's input type). Returns X as float64 of B's shape."""
+    l32 = np.asfortranarray(np.asarray(L, dtype=np.float32))
+    b = np.asarray(B, dtype=np.float32)
+    vec = b.ndim == 1
+    b32 = np.asfortranarray(b.reshape(b.shape[0], -1))
+    n, nrhs = b32.shape
+    X = np.zeros((n, nrhs), dtype=np.float64, order="F")
+    _load().oracle_potrs_one(l32.ctypes.data, n, max(1, n), b32.ctypes.data, nrhs, max(1, n),
+                             X.ctypes.data, max(1, n))
+    X = np.ascontiguousarray(X)
+    return X[:, 0] if vec else X
+
+
+def potrs_batched(lbuf: np.ndarray, n: int, lda: int, strideA: int, bbuf: np.ndarray,
+                  nrhs: int, ldb: int, strideB: int, batch: int,
+                  indices: Optional[Sequence[int]] = None,
+                  nthreads: Optional[int] = None) -> tuple[np.ndarray, int]:
+    """Solve A_b X_b = B_b with the factors of a strided float32 batch.
+
+    ``lbuf`` holds L_b(i, j) at ``lbuf[b*strideA + i + j*lda]`` (lower triangle
+    read), ``bbuf`` B_b(i, c) at ``bbuf[b*strideB + i + c*ldb]``. ``indices``
+    picks a subset of b. Returns (X, threads) with X[t, i, c] (float64)."""
+    lib = _load()
+    lbuf = np.ascontiguousarray(lbuf, dtype=np.float32)
+    bbuf = np.ascontiguousarray(bbuf, dtype=np.float32)
+    if indices is None:
+        ls, sA, bs, sB, m = lbuf, strideA, bbuf, strideB, batch
+    else:
+        idx = list(indices)
+        m = len(idx)
+        spanL, spanB = lda * n, ldb * nrhs
+        ls = np.empty(max(1, m * spanL), dtype=np.float32)
+        bs = np.empty(max(1, m * spanB), dtype=np.float32)
+        for t, b in enumerate(idx):
+            ls[t * spanL:(t + 1) * spanL] = lbuf[b * strideA: b * strideA + spanL]
+            bs[t * spanB:(t + 1) * spanB] = bbuf[b * strideB: b * strideB + spanB]
+        sA, sB = spanL, spanB
+    X = np.zeros((m, nrhs, n), dtype=np.float64)  # [t, c, i]: column-major per matrix
+    th = default_threads() if nthreads is None else nthreads
+    used = lib.oracle_potrs_batched(ls.ctypes.data, n, lda, sA, bs.ctypes.data, nrhs, ldb, sB,
+                                    m, X.ctypes.data, n * nrhs, th)
+    return X.transpose(0, 2, 1), int(used)

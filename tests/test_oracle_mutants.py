@@ -116,3 +116,82 @@ def test_mutant_is_caught(name, tmp_path):
         assert failed == [], failed
     else:
         assert failed, f"planted mistake {name!r} passed every pin"
+
+
+# --------------------------------------------------------------------------
+# The SPOTRS oracle (forward and backward substitution with the factor)
+# --------------------------------------------------------------------------
+
+SRC_TRS = os.path.join(os.path.dirname(SRC), "potrs_ref.c")
+
+TRS_MUTANTS = {
+    "identity": ("", ""),
+    "forward reads the upper triangle": ("s -= (double)L[i + (int64_t)k * lda] * x[k];",
+                                         "s -= (double)L[k + (int64_t)i * lda] * x[k];"),
+    "backward not transposed": ("s -= (double)L[k + (int64_t)i * lda] * x[k];",
+                                "s -= (double)L[i + (int64_t)k * lda] * x[k];"),
+    "backward skipped": ("for (int i = n - 1; i >= 0; --i) {", "for (int i = n - 1; i >= n; --i) {"),
+    "dropped forward term": ("for (int k = 0; k < i; ++k)", "for (int k = 1; k < i; ++k)"),
+    "dropped backward term": ("for (int k = i + 1; k < n; ++k)", "for (int k = i + 2; k < n; ++k)"),
+    "multiply instead of divide": ("x[i] = s / (double)L[i + (int64_t)i * lda];",
+                                   "x[i] = s * (double)L[i + (int64_t)i * lda];"),
+}
+
+
+def _compile_trs(name: str, tmp_path) -> ctypes.CDLL:
+    old, new = TRS_MUTANTS[name]
+    src = open(SRC_TRS).read()
+    if old:
+        assert old in src, f"mutation site for {name!r} not found"
+        src = src.replace(old, new, 1)
+    c = tmp_path / "t.c"
+    so = tmp_path / "t.so"
+    c.write_text(src)
+    subprocess.run(["gcc", "-O1", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
+                    str(c), "-o", str(so), "-lm"], check=True)
+    lib = ctypes.CDLL(str(so))
+    lib.oracle_potrs_one.restype = None
+    lib.oracle_potrs_one.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                     ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int]
+    return lib
+
+
+def _potrs(lib, L, B):
+    l32 = np.asfortranarray(np.asarray(L, dtype=np.float32))
+    b32 = np.asfortranarray(np.asarray(B, dtype=np.float32))
+    n, nrhs = b32.shape
+    X = np.zeros((n, nrhs), order="F")
+    lib.oracle_potrs_one(l32.ctypes.data, n, n, b32.ctypes.data, nrhs, n, X.ctypes.data, n)
+    return np.ascontiguousarray(X)
+
+
+def _trs_battery(lib) -> list[str]:
+    from tests.test_oracle_potrs import _int_factor
+    failed = []
+    # exact integer solution with a poisoned upper triangle
+    n = 9
+    L = _int_factor(n, 3)
+    X = np.random.default_rng(4).integers(-5, 6, (n, 3)).astype(np.float64)
+    B = L @ (L.T @ X)
+    Lp = L + np.triu(np.full((n, n), 1e30), 1)
+    if not np.array_equal(_potrs(lib, Lp, B), X):
+        failed.append("integer solution")
+    # backward error on a well-conditioned factor
+    g = np.random.default_rng(6)
+    G = g.standard_normal((40, 40))
+    Lw = np.linalg.cholesky(G @ G.T / 40 + np.eye(40)).astype(np.float32).astype(np.float64)
+    Bw = g.standard_normal((40, 2)).astype(np.float32).astype(np.float64)
+    Xw = _potrs(lib, Lw, Bw)
+    r = np.linalg.norm(Lw @ (Lw.T @ Xw) - Bw)
+    if not (r <= 10 * 40 * 2.0 ** -53 * np.linalg.norm(Lw) ** 2 * np.linalg.norm(Xw)):
+        failed.append("backward error")
+    return failed
+
+
+@pytest.mark.parametrize("name", list(TRS_MUTANTS))
+def test_trs_mutant_is_caught(name, tmp_path):
+    failed = _trs_battery(_compile_trs(name, tmp_path))
+    if name == "identity":
+        assert failed == [], failed
+    else:
+        assert failed, f"planted mistake {name!r} passed every pin"
