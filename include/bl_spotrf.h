@@ -119,6 +119,52 @@ int bl_spotrf_route(int n, int batch);
 int bl_spotrf_kernel_info(int route, int n, int *regs, int *local_bytes, int *static_smem,
                           int *dynamic_smem, int *threads);
 
+/*
+ * bl_spotrs_batched - solve A_b X_b = B_b for a strided batch, given the
+ * Cholesky factors L_b (A_b = L_b L_b^T, as bl_spotrf_batched leaves them):
+ * the forward solve L Y = B, then the backward solve L^T X = Y, each
+ * right-hand side column independently (the potrf-then-two-triangular-solves
+ * composition of posv on the "BatchLAS perf_blackwell" page; LAPACK SPOTRS
+ * with uplo = 'L'). X overwrites B.
+ *
+ *   L        device pointer to factor 0 (float, column-major); only its lower
+ *            triangle (i >= j, i < n) is read; nothing of it is written.
+ *   n        order (0 <= n <= BL_SPOTRF_MAX_N).
+ *   lda      leading dimension of L, lda >= max(1, n).
+ *   strideA  distance in floats between L_b and L_{b+1}; >= lda*n when batch > 1.
+ *   B        device pointer to right-hand sides 0 (float, column-major, n x nrhs).
+ *            Rows n..ldb-1 of every column and the memory between batches
+ *            are never read or written.
+ *   nrhs     number of right-hand sides (>= 0).
+ *   ldb      leading dimension of B, ldb >= max(1, n).
+ *   strideB  distance in floats between B_b and B_{b+1}; >= ldb*nrhs when batch > 1.
+ *   batch    number of systems (>= 0).
+ *   stream   CUDA stream the work is enqueued on.
+ *
+ * Ownership and threading as bl_spotrf_batched: no allocation, no sync,
+ * stream-ordered, reentrant. Every L_b must be a valid factor (nonzero
+ * diagonal); a zero or NaN diagonal gives Inf/NaN solutions, not an error.
+ * Returns 0 when enqueued, a negative -i when argument i is invalid (nothing
+ * is enqueued; checked in the order -2, -6, -9, -3, -7, -4, -8, -1, -5; -2
+ * also when n > BL_SPOTRF_MAX_N), or the cudaError_t of a failed launch.
+ * Quick return: nothing is enqueued when batch, n or nrhs is 0.
+ */
+int bl_spotrs_batched(const float *L, int n, int lda, int64_t strideA, float *B, int nrhs,
+                      int ldb, int64_t strideB, int batch, cudaStream_t stream);
+
+/*
+ * bl_sposv_batched - factor and solve: A_b = L_b L_b^T in place of A_b (as
+ * bl_spotrf_batched, info[b] as there), then for every b with info[b] == 0
+ * solve A_b X_b = B_b in place of B_b (as bl_spotrs_batched). Systems whose
+ * factorization failed keep B_b unchanged (LAPACK SPOSV returns no solution
+ * there). Arguments as the two calls above, info a device pointer to batch
+ * ints. Returns 0, a negative argument index (checked in the order -2, -6,
+ * -9, -3, -7, -4, -8, -1, -5, -10; -2 also when n > BL_SPOTRF_MAX_N) or a
+ * cudaError_t. n == 0 sets info[b] = 0; nrhs == 0 only factors.
+ */
+int bl_sposv_batched(float *A, int n, int lda, int64_t strideA, float *B, int nrhs, int ldb,
+                     int64_t strideB, int batch, int *info, cudaStream_t stream);
+
 /* Version string of the library ("bl_spotrf <major>.<minor> sm_103a"). */
 const char *bl_spotrf_version(void);
 

@@ -16,7 +16,8 @@ __all__ = ["ROUTE_AUTO", "ROUTE_WARP", "ROUTE_CTA", "ROUTE_BLOCKED", "ROUTE_TMEM
            "ROUTE_CTA_TC", "MAX_N",
            "BLError",
            "library", "library_path", "spotrf_batched", "spotrf_batched_ex", "route",
-           "kernel_info", "version", "factor", "factor_host"]
+           "kernel_info", "version", "factor", "factor_host", "spotrs_batched",
+           "sposv_batched", "solve", "factor_solve"]
 
 ROUTE_AUTO, ROUTE_WARP, ROUTE_CTA, ROUTE_BLOCKED, ROUTE_TMEM, ROUTE_CTA_TC = 0, 1, 2, 3, 4, 5
 MAX_N = 4096
@@ -32,6 +33,8 @@ SYMBOLS = {
     "bl_spotrf_route": (_I, [_I, _I]),
     "bl_spotrf_kernel_info": (_I, [_I, _I, _VP, _VP, _VP, _VP, _VP]),
     "bl_spotrf_version": (ctypes.c_char_p, []),
+    "bl_spotrs_batched": (_I, [_VP, _I, _I, _I64, _VP, _I, _I, _I64, _I, _VP]),
+    "bl_sposv_batched": (_I, [_VP, _I, _I, _I64, _VP, _I, _I, _I64, _I, _VP, _VP]),
 }
 
 
@@ -105,6 +108,35 @@ def kernel_info(route_: int, n: int) -> dict:
         raise BLError(code, "kernel_info")
     keys = ["regs", "local_bytes", "static_smem", "dynamic_smem", "threads"]
     return {k: v.value for k, v in zip(keys, vals)}
+
+
+def spotrs_batched(L, n: int, lda: int, strideA: int, B, nrhs: int, ldb: int, strideB: int,
+                   batch: int, stream=None) -> int:
+    """bl_spotrs_batched: L and B are device tensors (or raw device pointers);
+    X overwrites B. Returns the library status (0 = enqueued)."""
+    return library().bl_spotrs_batched(_ptr(L), n, lda, strideA, _ptr(B), nrhs, ldb, strideB,
+                                       batch, _stream(stream))
+
+
+def sposv_batched(A, n: int, lda: int, strideA: int, B, nrhs: int, ldb: int, strideB: int,
+                  batch: int, info, stream=None) -> int:
+    """bl_sposv_batched: factor A in place, then solve into B where info == 0."""
+    return library().bl_sposv_batched(_ptr(A), n, lda, strideA, _ptr(B), nrhs, ldb, strideB,
+                                      batch, _ptr(info), _stream(stream))
+
+
+def solve(L, n, lda, strideA, B, nrhs, ldb, strideB, batch, stream=None) -> None:
+    """spotrs_batched, raising BLError on a nonzero status."""
+    code = spotrs_batched(L, n, lda, strideA, B, nrhs, ldb, strideB, batch, stream)
+    if code:
+        raise BLError(code, "spotrs")
+
+
+def factor_solve(A, n, lda, strideA, B, nrhs, ldb, strideB, batch, info, stream=None) -> None:
+    """sposv_batched, raising BLError on a nonzero status."""
+    code = sposv_batched(A, n, lda, strideA, B, nrhs, ldb, strideB, batch, info, stream)
+    if code:
+        raise BLError(code, "sposv")
 
 
 def version() -> str:

@@ -93,9 +93,48 @@ int run(float *A, int n, int lda, int64_t strideA, int batch, int *info, cudaStr
     }
 }
 
+int check_trs_args(const float *L, int n, int lda, int64_t strideA, const float *B, int nrhs,
+                   int ldb, int64_t strideB, int batch)
+{
+    if (n < 0 || n > BL_SPOTRF_MAX_N) return -2;
+    if (nrhs < 0) return -6;
+    if (batch < 0) return -9;
+    if (lda < (n > 1 ? n : 1)) return -3;
+    if (ldb < (n > 1 ? n : 1)) return -7;
+    if (batch > 1 && strideA < (int64_t)lda * n) return -4;
+    if (batch > 1 && strideB < (int64_t)ldb * nrhs) return -8;
+    const bool work = n > 0 && nrhs > 0 && batch > 0;
+    if (work && L == nullptr) return -1;
+    if (work && B == nullptr) return -5;
+    return 0;
+}
+
 }  // namespace
 
 extern "C" {
+
+int bl_spotrs_batched(const float *L, int n, int lda, int64_t strideA, float *B, int nrhs,
+                      int ldb, int64_t strideB, int batch, cudaStream_t stream)
+{
+    const int e = check_trs_args(L, n, lda, strideA, B, nrhs, ldb, strideB, batch);
+    if (e) return e;
+    if (batch == 0 || n == 0 || nrhs == 0) return 0;
+    if (trace_enabled())
+        std::fprintf(stderr, "bl_spotrs: n=%d nrhs=%d batch=%d\n", n, nrhs, batch);
+    return bl::launch_potrs(L, n, lda, strideA, B, nrhs, ldb, strideB, batch, nullptr, stream);
+}
+
+int bl_sposv_batched(float *A, int n, int lda, int64_t strideA, float *B, int nrhs, int ldb,
+                     int64_t strideB, int batch, int *info, cudaStream_t stream)
+{
+    int e = check_trs_args(A, n, lda, strideA, B, nrhs, ldb, strideB, batch);
+    if (e) return e;
+    if (info == nullptr && batch > 0) return -10;
+    e = run(A, n, lda, strideA, batch, info, stream, BL_ROUTE_AUTO);
+    if (e || batch == 0 || n == 0 || nrhs == 0) return e;
+    return bl::launch_potrs(A, n, lda, strideA, B, nrhs, ldb, strideB, batch, info, stream);
+}
+
 
 int bl_spotrf_batched(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                       cudaStream_t stream)

@@ -113,6 +113,9 @@ int launch_trsm_tc(float *A, int n, int lda, int64_t strideA, int batch, int *in
                    cudaStream_t stream);
 
 int attrs_cta_tc(cudaFuncAttributes *fa, int *threads, int *dyn_smem);
+int launch_potrs(const float *L, int n, int lda, int64_t strideA, float *B, int nrhs, int ldb,
+                 int64_t strideB, int batch, const int *info, cudaStream_t stream);
+int attrs_potrs(cudaFuncAttributes *fa, int *threads, int *dyn_smem);
 int attrs_warp(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem);
 int attrs_cta(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem);
 int attrs_tmem(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem);

@@ -79,6 +79,46 @@ def test_check_order(bl):
     assert lib.bl_spotrf_batched(None, 4, 4, 1, 2, None, None) == -4
 
 
+@pytest.mark.parametrize("args,code", [
+    # (L, n, lda, strideA, B, nrhs, ldb, strideB, batch) -> status; nothing reaches the GPU
+    ((8, -1, 1, 1, 8, 1, 1, 1, 1), -2),
+    ((8, 4097, 4097, 4097 * 4097, 8, 1, 4097, 4097, 1), -2),
+    ((8, 4, 4, 16, 8, -1, 4, 4, 1), -6),
+    ((8, 4, 4, 16, 8, 2, 4, 8, -1), -9),
+    ((8, 4, 3, 16, 8, 2, 4, 8, 2), -3),
+    ((8, 4, 4, 16, 8, 2, 3, 8, 2), -7),
+    ((8, 4, 4, 15, 8, 2, 4, 8, 2), -4),
+    ((8, 4, 4, 16, 8, 2, 4, 7, 2), -8),
+    ((None, 4, 4, 16, 8, 2, 4, 8, 2), -1),
+    ((8, 4, 4, 16, None, 2, 4, 8, 2), -5),
+    ((None, 4, 4, 16, None, 2, 4, 8, 0), 0),   # batch == 0: nothing to do
+    ((None, 0, 1, 0, None, 2, 1, 2, 3), 0),    # n == 0
+    ((None, 4, 4, 16, None, 0, 4, 0, 3), 0),   # nrhs == 0
+])
+def test_trs_argument_checks(bl, args, code):
+    lib = bl.library()
+    assert lib.bl_spotrs_batched(*args, None) == code
+    L, n, lda, sA, B, nrhs, ldb, sB, batch = args
+    if code != 0:
+        assert lib.bl_sposv_batched(*args, 8, None) == code
+
+
+def test_trs_check_order(bl):
+    lib = bl.library()
+    assert lib.bl_spotrs_batched(None, -1, 0, 0, None, -1, 0, 0, -1, None) == -2
+    assert lib.bl_spotrs_batched(None, 4, 0, 0, None, -1, 0, 0, -1, None) == -6
+    assert lib.bl_spotrs_batched(None, 4, 0, 0, None, 1, 0, 0, -1, None) == -9
+    assert lib.bl_spotrs_batched(None, 4, 0, 0, None, 1, 0, 0, 2, None) == -3
+    assert lib.bl_spotrs_batched(None, 4, 4, 0, None, 1, 0, 0, 2, None) == -7
+    assert lib.bl_spotrs_batched(None, 4, 4, 0, None, 1, 4, 0, 2, None) == -4
+    assert lib.bl_spotrs_batched(None, 4, 4, 16, None, 1, 4, 0, 2, None) == -8
+    assert lib.bl_spotrs_batched(None, 4, 4, 16, None, 1, 4, 4, 2, None) == -1
+    assert lib.bl_spotrs_batched(8, 4, 4, 16, None, 1, 4, 4, 2, None) == -5
+    # sposv: info last
+    assert lib.bl_sposv_batched(8, 4, 4, 16, 8, 1, 4, 4, 2, None, None) == -10
+    assert lib.bl_sposv_batched(8, 4, 4, 16, None, 1, 4, 4, 2, None, None) == -5
+
+
 def test_forced_route_that_cannot_run(bl):
     lib = bl.library()
     assert lib.bl_spotrf_batched_ex(8, 65, 65, 65 * 65, 1, 8, None, bl.ROUTE_WARP) == -8
