@@ -8,6 +8,7 @@ the L2 was flushed. Prints ONE JSON line on rank 0.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload n64] [--no-per-n] [--no-cpu-baseline]
   python bench.py --sweep     # batch sweep of the small orders, one JSON line per point
+  python bench.py --op potrs --workload n256 --nrhs 16   # the solve with the factor
 
 The headline workload is n=64, batch=1024 (A = G G^T/64 + 0.1 I); `per_n`
 adds the same measurement for every workload (n = 32, 64, 128, 256, 1024).
@@ -533,6 +534,91 @@ def run_sweep(args) -> list:
     return rows
 
 
+def run_potrs(args) -> dict:
+    """Batched SPOTRS (solve with the factor) on a workload's factors: the
+    batch is factored once on the device, then each timed step solves nrhs
+    right-hand sides per system on its own cold replica of B (L2 flushed
+    outside the timed region). Work per system: 2 n^2 nrhs flops; bytes: the
+    factor's lower triangle read, B read and X written."""
+    import torch
+
+    import matrix_dense_linear_gb300 as bl
+    bl.library()
+    dev = torch.device("cuda", 0)
+    pk = peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    bt = make_host_batch(args.workload, args.batch)
+    n, batch, nrhs = bt.n, bt.batch, args.nrhs
+    dA = torch.from_numpy(bt.buf).to(dev)
+    info = torch.zeros(batch, dtype=torch.int32, device=dev)
+    bl.factor(dA, n, bt.lda, bt.strideA, batch, info)
+    torch.cuda.synchronize()
+    assert not info.cpu().numpy().any()
+    g = np.random.default_rng(7)
+    span = batch * n * nrhs
+    Bh = torch.from_numpy(g.standard_normal(span).astype(np.float32))
+    pristine = Bh.to(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    nrep = int(max(1, min(max(args.steps, -(-2 * l2 // (4 * span))),
+                          REPLICA_CAP_BYTES // (4 * span))))
+    reps = torch.empty((nrep, span), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def call(i, st):
+        code = bl.spotrs_batched(dA, n, bt.lda, bt.strideA, reps[i], nrhs, n, n * nrhs, batch,
+                                 st)
+        if code:
+            raise bl.BLError(code, "spotrs")
+
+    st = torch.cuda.current_stream()
+    for i in range(min(args.warmup, nrep)):
+        reps[i].copy_(pristine)
+        call(i, st.cuda_stream)
+    torch.cuda.synchronize()
+    total, done = 0.0, 0
+    while done < args.steps:
+        chunk = min(nrep, args.steps - done)
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            cs = torch.cuda.current_stream().cuda_stream
+            for i in range(chunk):
+                call(i, cs)
+        for i in range(chunk):
+            reps[i].copy_(pristine)
+        flush.fill_(1.0)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        gr.replay()
+        e1.record(st)
+        torch.cuda.synchronize()
+        total += e0.elapsed_time(e1)
+        done += chunk
+        del gr
+    ms = total / args.steps
+    t = ms / 1e3
+    flops = 2.0 * n * n * nrhs * batch
+    bytes_ = (2.0 * n * (n + 1) + 8.0 * n * nrhs) * batch
+    fp32 = sms * 128 * 2 * pk["sm_max_mhz"] * 1e6
+    t_hbm, t_alu = bytes_ / (pk["hbm_gbs"] * 1e9), flops / fp32
+    if t_hbm >= t_alu:
+        roof = {"bound": "hbm", "achieved": bytes_ / t / 1e9, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": bytes_ / t / 1e9 / pk["hbm_gbs"]}
+    else:
+        roof = {"bound": "alu", "achieved": flops / t / 1e12, "peak": fp32 / 1e12,
+                "unit": "TFLOP/s", "frac": flops / t / fp32}
+    return {"op": "potrs", "metric": "batched SPOTRS systems/s", "value": batch / t,
+            "unit": "systems/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "dtype": "f32", "data": "synthetic",
+            "gflops": flops / t / 1e9, "roofline": roof,
+            "config": {"workload": f"{args.workload} factors, {nrhs} right-hand sides each",
+                       "n": n, "batch": batch, "nrhs": nrhs,
+                       "l2": "flushed before each timed chunk; every step solves into its own "
+                             "replica of B",
+                       "timing": "CUDA events around the replay of a CUDA graph of the K calls"},
+            "gpu_launches": args.steps}
+
+
 def run_reference(args) -> dict:
     """The oracle as it stands, timed on the host cores, on the same workload:
     each step is one pass over a bounded sample of the batch."""
@@ -579,6 +665,9 @@ def main():
                     help="factor only the first B matrices of the workload (profiling)")
     ap.add_argument("--no-per-n", dest="per_n", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--op", choices=["potrf", "potrs"], default="potrf",
+                    help="potrs: time the solve with the factor instead (one JSON line)")
+    ap.add_argument("--nrhs", type=int, default=16, help="right-hand sides per system (potrs)")
     ap.add_argument("--sweep", action="store_true",
                     help="batch sweep of n = 32, 64, 128 (one JSON line per point)")
     args = ap.parse_args()
@@ -590,6 +679,9 @@ def main():
 
     if args.sweep:
         run_sweep(args)
+        return
+    if args.op == "potrs":
+        print(json.dumps(run_potrs(args)), flush=True)
         return
 
     if args.impl == "reference":

@@ -102,7 +102,7 @@ def _check_solution(L32, B, X, X_ref, what):
     assert err <= 4 * n * U * kappa, f"{what}: forward error {err:.3e}, kappa {kappa:.1f}"
 
 
-CASES = [(1, 1), (5, 3), (31, 8), (32, 32), (33, 33), (64, 1), (64, 70), (100, 17),
+CASES = [(1, 1), (5, 3), (31, 8), (32, 32), (33, 33), (64, 1), (64, 2), (64, 70), (100, 17),
          (128, 32), (129, 40), (256, 16), (300, 5)]
 
 
