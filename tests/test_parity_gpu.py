@@ -10,7 +10,9 @@ from __future__ import annotations
 import numpy as np
 import pytest
 
+import oracle
 import synth
+from tests import checks
 from tests.gpu_helpers import assert_untouched, compare, run_gpu
 
 pytestmark = pytest.mark.gpu
@@ -55,6 +57,27 @@ def test_large_orders(n):
     out, info = run_gpu(bt)
     compare(bt, out, info, what=f"n={n}")
     assert_untouched(out, bt.buf, bt, what=f"n={n}")
+
+
+@pytest.mark.parametrize("n", [2048, 3000, 4096])
+def test_larger_orders(n):
+    """Orders above the workloads' (the blocked route's 1025 .. 4096 range, one
+    matrix): the leading 1024 x 1024 block of L against the oracle (the factor
+    of a leading principal block is that block of the factor), info bit-exact,
+    and the reconstruction of the whole matrix within the budget."""
+    bt = _gram_batch(n, 1, 350 + n, fill="nan")
+    out, info = run_gpu(bt)
+    assert info[0] == 0
+    assert_untouched(out, bt.buf, bt, what=f"n={n}")
+    A_low = np.tril(np.array(bt.view()[0]))
+    L = np.tril(np.array(synth.strided_view(out, n, n, n * n, 1)[0], dtype=np.float64))
+    m = 1024
+    L_ref, info_ref = oracle.potrf_one(checks.sym_from_lower(A_low[:m, :m]))
+    assert info_ref == 0
+    err = np.abs(L[:m, :m] - L_ref).max() / np.abs(L_ref).max()
+    assert err <= checks.MAXREL_PER_N * m, f"n={n}: leading block max rel {err:.3e}"
+    rec = checks.recon_error(L, A_low)
+    assert rec <= checks.RECON_PER_N * n, f"n={n}: reconstruction {rec:.3e}"
 
 
 @pytest.mark.parametrize("n", [5, 32, 48, 64, 128, 200])
