@@ -60,6 +60,12 @@ __device__ __forceinline__ void cp_async_wait() {
 // pdl_wait() before their first access to global memory (it returns once the
 // previous grid has completed and its writes are visible) and pdl_trigger()
 // to let the next kernel start launching early.
+// Named barrier 1..15 over nthreads threads (a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger()
 {

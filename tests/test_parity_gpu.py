@@ -157,6 +157,25 @@ def test_routes_agree(n):
             assert np.abs(got - ref).max() <= 2e-5 * n * np.abs(ref).max()
 
 
+def test_n64_small_and_large_batch_kernels_agree():
+    """n = 33 .. 64 runs two warps per matrix in small batches and one warp in
+    large ones; the same matrices factored both ways agree with each other and
+    with the oracle."""
+    n, big = 48, 2000
+    bt = _gram_batch(n, big, 760, fill="nan")
+    out_big, info_big = run_gpu(bt)
+    small = synth.pack(lambda b: np.array(bt.view()[b], dtype=np.float64), n, 8, fill="nan")
+    out_small, info_small = run_gpu(small)
+    assert not info_big[:8].any() and not info_small.any()
+    gv = synth.strided_view(out_big, n, n, n * n, big)
+    sv = synth.strided_view(out_small, n, n, n * n, 8)
+    for b in range(8):
+        a, c = np.tril(np.array(gv[b], dtype=np.float64)), np.tril(np.array(sv[b], dtype=np.float64))
+        assert np.abs(a - c).max() <= 2e-5 * n * np.abs(a).max()
+    compare(small, out_small, info_small, what="n=48 small batch")
+    compare(bt, out_big, info_big, indices=[0, 999, 1999], what="n=48 large batch")
+
+
 def test_n_zero_and_batch_zero():
     import torch
 
