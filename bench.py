@@ -266,8 +266,10 @@ def soak(w: DeviceWorkload, seconds: float) -> None:
 
 
 def e2e_steps(w: DeviceWorkload, steps: int, warmup: int, barrier) -> dict:
-    """Same metric through the public host-buffer call: every step copies the
-    batch from pinned host memory, factors it, and copies matrices + info back."""
+    """Same metric through the public host-buffer call (bl_spotrf_batched_host):
+    every step copies the batch from pinned host memory, factors it, and copies
+    matrices + info back, in two slices on two streams so the copies of one
+    overlap the factorization and copies of the other."""
     import torch
 
     import matrix_dense_linear_gb300 as bl
@@ -276,11 +278,12 @@ def e2e_steps(w: DeviceWorkload, steps: int, warmup: int, barrier) -> dict:
     host = torch.empty_like(host_in).pin_memory()
     info_h = torch.zeros(bt.batch, dtype=torch.int32).pin_memory()
     A_dev = w.rep[0]
+    st = torch.cuda.current_stream()
+    streams = [st, torch.cuda.Stream()]
     for _ in range(warmup):
         host.copy_(host_in)
-        bl.factor_host(host, bt.n, bt.lda, bt.strideA, bt.batch, info_h, A_dev, w.info)
+        bl.factor_host(host, bt.n, bt.lda, bt.strideA, bt.batch, info_h, A_dev, w.info, streams)
     torch.cuda.synchronize()
-    st = torch.cuda.current_stream()
     total = 0.0
     for _ in range(steps):
         host.copy_(host_in)  # a fresh input each step, outside the timed interval
@@ -288,7 +291,7 @@ def e2e_steps(w: DeviceWorkload, steps: int, warmup: int, barrier) -> dict:
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(st)
-        bl.factor_host(host, bt.n, bt.lda, bt.strideA, bt.batch, info_h, A_dev, w.info)
+        bl.factor_host(host, bt.n, bt.lda, bt.strideA, bt.batch, info_h, A_dev, w.info, streams)
         e1.record(st)
         torch.cuda.synchronize()
         total += e0.elapsed_time(e1)

@@ -120,6 +120,35 @@ int bl_spotrf_kernel_info(int route, int n, int *regs, int *local_bytes, int *st
                           int *dynamic_smem, int *threads);
 
 /*
+ * bl_spotrf_batched_host - bl_spotrf_batched for a batch held in host memory:
+ * copy it to the device, factor it there, copy the matrices and info back.
+ * The batch is cut into `chunks` slices of whole matrices (chunks <= 0: one
+ * per stream); slice c runs on streams[c % nstreams] (its host-to-device
+ * copy, its factorization, its device-to-host copies), so with a stream per
+ * slice the host-to-device copies run back to back on one copy engine while
+ * earlier slices are factored and copied back on the other. Only the batch's
+ * own span (matrix b at b*strideA, lda*n floats each, with any gaps between
+ * them) is copied; the kernels touch the lower triangles only, so everything
+ * else returns unchanged.
+ *
+ *   A_host, info_host  host memory (page-locked for the copies to overlap),
+ *                      same layout as the device call's A and info.
+ *   A_dev, info_dev    device work buffers of the same sizes, owned by the
+ *                      caller (the library still allocates nothing).
+ *   streams, nstreams  the caller's CUDA streams (nstreams >= 1; entries may
+ *                      repeat, then their slices serialize). The call does not
+ *                      synchronize: the results are on the host once every
+ *                      stream is done.
+ *
+ * Returns what bl_spotrf_batched returns (argument indices as there, with the
+ * device buffers checked as A and info; -11 when streams is NULL or nstreams
+ * < 1), or the cudaError_t of a failed copy.
+ */
+int bl_spotrf_batched_host(float *A_host, int n, int lda, int64_t strideA, int batch,
+                           int *info_host, float *A_dev, int *info_dev, int chunks,
+                           const cudaStream_t *streams, int nstreams);
+
+/*
  * bl_spotrs_batched - solve A_b X_b = B_b for a strided batch, given the
  * Cholesky factors L_b (A_b = L_b L_b^T, as bl_spotrf_batched leaves them):
  * the forward solve L Y = B, then the backward solve L^T X = Y, each

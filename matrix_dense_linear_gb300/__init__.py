@@ -33,6 +33,7 @@ SYMBOLS = {
     "bl_spotrf_route": (_I, [_I, _I]),
     "bl_spotrf_kernel_info": (_I, [_I, _I, _VP, _VP, _VP, _VP, _VP]),
     "bl_spotrf_version": (ctypes.c_char_p, []),
+    "bl_spotrf_batched_host": (_I, [_VP, _I, _I, _I64, _I, _VP, _VP, _VP, _I, _VP, _I]),
     "bl_spotrs_batched": (_I, [_VP, _I, _I, _I64, _VP, _I, _I, _I64, _I, _VP]),
     "bl_sposv_batched": (_I, [_VP, _I, _I, _I64, _VP, _I, _I, _I64, _I, _VP, _VP]),
 }
@@ -152,18 +153,30 @@ def factor(A, n: int, lda: int, strideA: int, batch: int, info, stream=None,
 
 
 def factor_host(A_host, n: int, lda: int, strideA: int, batch: int, info_host,
-                A_dev=None, info_dev=None, stream=None) -> None:
-    """Factor a batch that lives in (pinned) host memory: copy it to the device,
-    factor it there, copy the matrices and info back, all on one stream. The
-    device buffers are the caller's if given, else allocated by torch."""
+                A_dev=None, info_dev=None, streams=None, chunks: int = 0) -> None:
+    """Factor a batch that lives in (pinned) host memory through
+    bl_spotrf_batched_host: slices of the batch go host -> device, are factored
+    and come back, one stream per slice, so copies and factorization overlap.
+    The device buffers are the caller's if given, else allocated by torch; the
+    streams are the caller's (torch streams) or two made here (two slices
+    measured best for the 16.8 MB n = 64 batch on GB300). Waits for all
+    streams before returning."""
     import torch
-    st = torch.cuda.current_stream() if stream is None else stream
-    with torch.cuda.stream(st):
-        if A_dev is None:
-            A_dev = torch.empty_like(A_host, device="cuda")
-        if info_dev is None:
-            info_dev = torch.empty_like(info_host, device="cuda")
-        A_dev.copy_(A_host, non_blocking=True)
-        factor(A_dev, n, lda, strideA, batch, info_dev, st)
-        A_host.copy_(A_dev, non_blocking=True)
-        info_host.copy_(info_dev, non_blocking=True)
+    if A_dev is None:
+        A_dev = torch.empty_like(A_host, device="cuda")
+    if info_dev is None:
+        info_dev = torch.empty_like(info_host, device="cuda")
+    cur = torch.cuda.current_stream()
+    if streams is None:
+        streams = [cur, torch.cuda.Stream()]
+    for s in streams:
+        s.wait_stream(cur)  # the device buffers are free once earlier work is done
+    arr = (ctypes.c_void_p * len(streams))(*[_stream(s) for s in streams])
+    code = library().bl_spotrf_batched_host(_ptr(A_host), n, lda, strideA, batch,
+                                            _ptr(info_host), _ptr(A_dev), _ptr(info_dev),
+                                            chunks, arr, len(streams))
+    if code:
+        raise BLError(code, "host")
+    for s in streams:
+        cur.wait_stream(s)
+    cur.synchronize()

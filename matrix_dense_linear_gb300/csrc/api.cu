@@ -113,6 +113,50 @@ int check_trs_args(const float *L, int n, int lda, int64_t strideA, const float 
 
 extern "C" {
 
+int bl_spotrf_batched_host(float *A_host, int n, int lda, int64_t strideA, int batch,
+                           int *info_host, float *A_dev, int *info_dev, int chunks,
+                           const cudaStream_t *streams, int nstreams)
+{
+    int e = check_args(A_dev, n, lda, strideA, batch, info_dev);
+    if (e) return e;
+    if (batch > 0 && n > 0 && A_host == nullptr) return -1;
+    if (batch > 0 && info_host == nullptr) return -6;
+    if (streams == nullptr || nstreams < 1) return -11;
+    if (batch == 0) return 0;
+    const int64_t span = (int64_t)lda * n;  // floats of one matrix
+    if (chunks <= 0) chunks = nstreams;
+    if (chunks > batch) chunks = batch;
+    // Issued phase by phase (every slice's copy in, then every factorization,
+    // then every copy out): a copy out waits for its factorization, and copies
+    // queued behind it would wait too, so the copies in go first.
+    for (int phase = 0; phase < 3; ++phase) {
+        for (int c = 0; c < chunks; ++c) {
+            const int b0 = (int)((int64_t)batch * c / chunks);
+            const int b1 = (int)((int64_t)batch * (c + 1) / chunks);
+            if (b1 <= b0) continue;
+            cudaStream_t s = streams[c % nstreams];
+            const int64_t off = (int64_t)b0 * strideA;
+            const size_t bytes = (size_t)(((int64_t)(b1 - 1 - b0) * strideA + span) * 4);
+            if (phase == 0 && n > 0)
+                e = (int)cudaMemcpyAsync(A_dev + off, A_host + off, bytes, cudaMemcpyHostToDevice,
+                                         s);
+            else if (phase == 1)
+                e = run(A_dev + off, n, lda, strideA, b1 - b0, info_dev + b0, s, BL_ROUTE_AUTO);
+            else if (phase == 2) {
+                if (n > 0)
+                    e = (int)cudaMemcpyAsync(A_host + off, A_dev + off, bytes,
+                                             cudaMemcpyDeviceToHost, s);
+                if (!e)
+                    e = (int)cudaMemcpyAsync(info_host + b0, info_dev + b0,
+                                             sizeof(int) * (size_t)(b1 - b0),
+                                             cudaMemcpyDeviceToHost, s);
+            }
+            if (e) return e;
+        }
+    }
+    return 0;
+}
+
 int bl_spotrs_batched(const float *L, int n, int lda, int64_t strideA, float *B, int nrhs,
                       int ldb, int64_t strideB, int batch, cudaStream_t stream)
 {

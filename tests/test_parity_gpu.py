@@ -176,6 +176,22 @@ def test_n64_small_and_large_batch_kernels_agree():
     compare(bt, out_big, info_big, indices=[0, 999, 1999], what="n=48 large batch")
 
 
+@pytest.mark.parametrize("n,batch,chunks", [(48, 10, 3), (128, 7, 0), (200, 5, 2), (32, 40, 1)])
+def test_host_buffer_call(n, batch, chunks):
+    """bl_spotrf_batched_host: slices over two streams, host buffers in and out,
+    gaps between matrices and the upper triangles come back unchanged."""
+    import torch
+
+    import matrix_dense_linear_gb300 as bl
+    bt = _gram_batch(n, batch, 780 + n, fill="nan", strideA=n * n + 5)
+    host = torch.from_numpy(bt.buf.copy()).pin_memory()
+    info_h = torch.full((batch,), -7, dtype=torch.int32).pin_memory()
+    bl.factor_host(host, n, bt.lda, bt.strideA, batch, info_h, chunks=chunks)
+    out, info = host.numpy(), info_h.numpy()
+    compare(bt, out, info, what=f"host n={n} chunks={chunks}")
+    assert_untouched(out, bt.buf, bt, what=f"host n={n}")
+
+
 def test_n_zero_and_batch_zero():
     import torch
 
