@@ -50,9 +50,6 @@ extern "C" {
                                panel triangular solve, lower-only trailing update, any n */
 #define BL_ROUTE_TMEM 4     /* K2t: one thread block per matrix, the matrix resident in tensor
                                memory, trailing updates on the tensor cores, n <= 128 */
-#define BL_ROUTE_CTA_TC 5   /* K2c: K2 with each panel's trailing update on the tensor cores
-                               (3xTF32), for n == 128 with A, lda and strideA 16-byte
-                               aligned; any other n <= 128 runs K2 */
 
 /*
  * bl_spotrf_batched - factor a strided batch in place.
@@ -95,8 +92,7 @@ int bl_spotrf_batched(float *A, int n, int lda, int64_t strideA, int batch, int 
  * bl_spotrf_batched_ex - as bl_spotrf_batched, with the kernel class forced
  * (route = BL_ROUTE_*; BL_ROUTE_AUTO selects by n like bl_spotrf_batched).
  * Returns -8 when the forced route cannot factor this n (WARP: n > 64;
- * CTA, TMEM or CTA_TC: n > 128), after the checks above. For tests and
- * measurement.
+ * CTA or TMEM: n > 128), after the checks above. For tests and measurement.
  */
 int bl_spotrf_batched_ex(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                          cudaStream_t stream, int route);

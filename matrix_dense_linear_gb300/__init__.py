@@ -12,14 +12,13 @@ import ctypes
 import os
 from typing import Optional
 
-__all__ = ["ROUTE_AUTO", "ROUTE_WARP", "ROUTE_CTA", "ROUTE_BLOCKED", "ROUTE_TMEM",
-           "ROUTE_CTA_TC", "MAX_N",
+__all__ = ["ROUTE_AUTO", "ROUTE_WARP", "ROUTE_CTA", "ROUTE_BLOCKED", "ROUTE_TMEM", "MAX_N",
            "BLError",
            "library", "library_path", "spotrf_batched", "spotrf_batched_ex", "route",
            "kernel_info", "version", "factor", "factor_host", "spotrs_batched",
            "sposv_batched", "solve", "factor_solve"]
 
-ROUTE_AUTO, ROUTE_WARP, ROUTE_CTA, ROUTE_BLOCKED, ROUTE_TMEM, ROUTE_CTA_TC = 0, 1, 2, 3, 4, 5
+ROUTE_AUTO, ROUTE_WARP, ROUTE_CTA, ROUTE_BLOCKED, ROUTE_TMEM = 0, 1, 2, 3, 4
 MAX_N = 4096
 _PKG = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_PKG, "libbl_spotrf.so")

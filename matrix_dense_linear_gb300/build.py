@@ -82,11 +82,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
 
 def ptxas_report() -> str:
-    """Concatenated ptxas resource reports of the last build."""
+    """Concatenated ptxas resource reports of the last build (current sources
+    only: reports left by a deleted source are ignored)."""
     out = []
-    for f in sorted(glob.glob(os.path.join(BUILD, "*.ptxas.txt"))):
-        with open(f) as fh:
-            out.append(fh.read())
+    for src in sources():
+        f = os.path.join(BUILD, os.path.splitext(os.path.basename(src))[0] + ".ptxas.txt")
+        if os.path.exists(f):
+            with open(f) as fh:
+                out.append(fh.read())
     return "\n".join(out)
 
 

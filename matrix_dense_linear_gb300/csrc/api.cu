@@ -43,11 +43,6 @@ int check_args(const float *A, int n, int lda, int64_t strideA, int batch, const
     return 0;
 }
 
-bool aligned16(const float *A, int lda, int64_t strideA)
-{
-    return (reinterpret_cast<uintptr_t>(A) & 15) == 0 && (lda & 3) == 0 && (strideA & 3) == 0;
-}
-
 int route_for(int n)
 {
     if (n <= kWarpMaxN) return BL_ROUTE_WARP;
@@ -61,7 +56,6 @@ bool route_can_run(int route, int n)
     case BL_ROUTE_WARP: return n <= kWarpMaxN;
     case BL_ROUTE_CTA: return n <= kCtaMaxN;
     case BL_ROUTE_TMEM: return n <= kCtaMaxN;
-    case BL_ROUTE_CTA_TC: return n <= kCtaMaxN;
     case BL_ROUTE_BLOCKED: return true;
     default: return false;
     }
@@ -85,10 +79,6 @@ int run(float *A, int n, int lda, int64_t strideA, int batch, int *info, cudaStr
         return bl::launch_cta(A, n, lda, strideA, batch, info, stream, bl::InfoMode{-1});
     case BL_ROUTE_TMEM:
         return bl::launch_tmem(A, n, lda, strideA, batch, info, stream, bl::InfoMode{-1});
-    case BL_ROUTE_CTA_TC:
-        if (n == 128 && aligned16(A, lda, strideA))
-            return bl::launch_cta_tc(A, lda, strideA, batch, info, stream, bl::InfoMode{-1});
-        return bl::launch_cta(A, n, lda, strideA, batch, info, stream, bl::InfoMode{-1});
     default: return bl::launch_blocked(A, n, lda, strideA, batch, info, stream);
     }
 }
@@ -189,7 +179,7 @@ int bl_spotrf_batched(float *A, int n, int lda, int64_t strideA, int batch, int 
 int bl_spotrf_batched_ex(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                          cudaStream_t stream, int route)
 {
-    if (route < BL_ROUTE_AUTO || route > BL_ROUTE_CTA_TC) return -8;
+    if (route < BL_ROUTE_AUTO || route > BL_ROUTE_TMEM) return -8;
     return run(A, n, lda, strideA, batch, info, stream, route);
 }
 
@@ -210,9 +200,6 @@ int bl_spotrf_kernel_info(int route, int n, int *regs, int *local_bytes, int *st
     case BL_ROUTE_WARP: e = bl::attrs_warp(n, &fa, &th, &dyn); break;
     case BL_ROUTE_CTA: e = bl::attrs_cta(n, &fa, &th, &dyn); break;
     case BL_ROUTE_TMEM: e = bl::attrs_tmem(n, &fa, &th, &dyn); break;
-    case BL_ROUTE_CTA_TC:
-        e = n == 128 ? bl::attrs_cta_tc(&fa, &th, &dyn) : bl::attrs_cta(n, &fa, &th, &dyn);
-        break;
     default: e = bl::attrs_blocked(n, &fa, &th, &dyn); break;
     }
     if (e) return e;

@@ -1,6 +1,6 @@
-// Pieces shared by the shared-memory kernels for n <= 128 (K2 and its
-// tensor-core variant K2c): the packed panel storage of the lower triangle,
-// its bulk copies, the warp-level diagonal factor and the one-row panel solve.
+// Pieces of the shared-memory kernel for n <= 128 (K2): the packed panel
+// storage of the lower triangle, its bulk copies, the warp-level diagonal
+// factor and the one-row panel solve.
 #pragma once
 
 #include "bl_common.cuh"

@@ -17,7 +17,7 @@ from tests.gpu_helpers import assert_untouched, compare, run_gpu
 
 pytestmark = pytest.mark.gpu
 
-WARP, CTA, BLOCKED, TMEM, CTA_TC = 1, 2, 3, 4, 5
+WARP, CTA, BLOCKED, TMEM = 1, 2, 3, 4
 
 
 def _routes(n):
@@ -25,7 +25,7 @@ def _routes(n):
     if n <= 64:
         r.append(WARP)
     if n <= 128:
-        r += [CTA, TMEM, CTA_TC]
+        r += [CTA, TMEM]
     return sorted(set(r))
 
 
@@ -213,8 +213,7 @@ def test_nondefault_stream():
 
 
 @pytest.mark.parametrize("route,n", [(1, 8), (1, 16), (1, 32), (1, 64), (2, 32), (2, 64),
-                                     (2, 96), (2, 128), (3, 256), (4, 100), (4, 128),
-                                     (5, 100), (5, 128)])
+                                     (2, 96), (2, 128), (3, 256), (4, 100), (4, 128)])
 def test_kernels_use_no_local_memory(route, n):
     import matrix_dense_linear_gb300 as bl
     ki = bl.kernel_info(route, n)
