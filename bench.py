@@ -41,8 +41,9 @@ REPLICA_CAP_BYTES = 96 << 30
 # capture, with the sha256 of the kernel's source file at capture time; a
 # changed source reports null. Filled from the summaries under profiles/.
 TRAFFIC = {
-    # workload: (source file, sha256 prefix, bytes per launch, summary file)
-    "n64": ("matrix_dense_linear_gb300/csrc/potrf_warp.cu", "5e9bb36d30360aee", 12665088,
+    # workload: (source files, sha256 prefix over them, bytes per launch, summary file)
+    "n64": (("matrix_dense_linear_gb300/csrc/potrf_warp.cu",
+             "matrix_dense_linear_gb300/csrc/bl_common.cuh"), "ac9c7df2e63d7be8", 12661248,
             "profiles/potrf_warp64_n64_b1024.md"),
 }
 
@@ -98,9 +99,12 @@ def traffic_for(name: str, n: int):
     ent = TRAFFIC.get(name)
     if not ent:
         return None
-    src, sha, nbytes, _ = ent
-    with open(os.path.join(ROOT, src), "rb") as f:
-        cur = hashlib.sha256(f.read()).hexdigest()
+    srcs, sha, nbytes, _ = ent
+    h = hashlib.sha256()
+    for src in srcs:
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    cur = h.hexdigest()
     return nbytes if cur.startswith(sha) else None
 
 
