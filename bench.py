@@ -541,6 +541,52 @@ def run_sweep(args) -> list:
     return rows
 
 
+# (n, batch) pairs at which the pages quote their own timings (other hardware)
+PAGES_SHAPES = "32x4096,64x1024,128x256,128x8192,256x64,512x16,512x640,1024x4,1024x60,17x16384"
+
+
+def run_shapes(args) -> list:
+    """Time arbitrary (n, batch) shapes, one JSON line each: A = G G^T / n + I
+    (G iid normal, 64 distinct matrices repeated to fill the batch), packed
+    lda = n, strideA = n^2; K calls per point on cold replicas (graph replay,
+    L2 flushed before each replay), median over 3 replays."""
+    import torch
+
+    import matrix_dense_linear_gb300 as bl
+    import synth
+    bl.library()
+    dev = torch.device("cuda", 0)
+    pk = peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    rows = []
+    for spec in args.shapes.split(","):
+        n, batch = (int(x) for x in spec.lower().split("x"))
+        distinct = min(batch, 64)
+        base = synth.pack(lambda b: synth.gram(n, synth.rng(6, b), "normal", float(n), 1.0),
+                          n, distinct)
+        reps = -(-batch // distinct)
+        buf = np.ascontiguousarray(np.tile(base.buf, reps)[: batch * n * n])
+        bt = type(base)(buf=buf, n=n, lda=n, strideA=n * n, batch=batch, fill=base.fill)
+        w = DeviceWorkload(bt, args.steps, dev)
+        for i in range(min(args.warmup, w.nrep)):
+            w.call(i, torch.cuda.current_stream().cuda_stream)
+        torch.cuda.synchronize()
+        k = min(args.steps, w.nrep)
+        ms = statistics.median(time_steps(w, k, lambda: None) / k for _ in range(3))
+        assert not w.info.cpu().numpy().any()
+        rf = roofline_entry("shape", n, batch, ms, pk, sms)
+        row = {"shape": spec, "n": n, "batch": batch, "ms_per_call": ms,
+               "us_per_call": ms * 1e3, "matrices_per_s": batch / (ms / 1e3),
+               "tflops": flops_per_matrix(n) * batch / (ms / 1e3) / 1e12,
+               "roofline": {k2: rf[k2] for k2 in ("bound", "frac", "roof_ms")},
+               "calls_timed": k}
+        print(json.dumps(row), flush=True)
+        rows.append(row)
+        del w
+        torch.cuda.empty_cache()
+    return rows
+
+
 def run_potrs(args) -> dict:
     """Batched SPOTRS (solve with the factor) on a workload's factors: the
     batch is factored once on the device, then each timed step solves nrhs
@@ -677,6 +723,9 @@ def main():
     ap.add_argument("--nrhs", type=int, default=16, help="right-hand sides per system (potrs)")
     ap.add_argument("--sweep", action="store_true",
                     help="batch sweep of n = 32, 64, 128 (one JSON line per point)")
+    ap.add_argument("--shapes", default=None, metavar="NxB,...",
+                    help="time these (n, batch) shapes (one JSON line each); 'pages' = "
+                         "the shapes the pages quote timings for")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -686,6 +735,11 @@ def main():
 
     if args.sweep:
         run_sweep(args)
+        return
+    if args.shapes:
+        if args.shapes == "pages":
+            args.shapes = PAGES_SHAPES
+        run_shapes(args)
         return
     if args.op == "potrs":
         print(json.dumps(run_potrs(args)), flush=True)
