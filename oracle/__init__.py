@@ -1,4 +1,5 @@
-"""CPU oracle for batched SPOTRF and SPOTRS (lower, column-major, strided batch).
+"""CPU oracle for batched SPOTRF and SPOTRS (column-major, strided batch, uplo
+'L' or 'U').
 
 TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
 baseline leg of ``bench.py`` may import this package. The CUDA library never
@@ -49,19 +50,23 @@ def _load():
         lib.oracle_potrf_one.restype = ctypes.c_int
         lib.oracle_potrf_one.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_void_p, ctypes.c_int]
-        lib.oracle_potrf_batched.restype = ctypes.c_int
-        lib.oracle_potrf_batched.argtypes = [
-            ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
-            ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int]
+        lib.oracle_potrf_upper_one.restype = ctypes.c_int
+        lib.oracle_potrf_upper_one.argtypes = lib.oracle_potrf_one.argtypes
+        lib.oracle_potrf_batched_uplo.restype = ctypes.c_int
+        lib.oracle_potrf_batched_uplo.argtypes = [
+            ctypes.c_char, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
+            ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int]
         lib.oracle_potrs_one.restype = None
         lib.oracle_potrs_one.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_void_p, ctypes.c_int]
-        lib.oracle_potrs_batched.restype = ctypes.c_int
-        lib.oracle_potrs_batched.argtypes = [
-            ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_void_p,
-            ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
-            ctypes.c_int64, ctypes.c_int]
+        lib.oracle_potrs_upper_one.restype = None
+        lib.oracle_potrs_upper_one.argtypes = lib.oracle_potrs_one.argtypes
+        lib.oracle_potrs_batched_uplo.restype = ctypes.c_int
+        lib.oracle_potrs_batched_uplo.argtypes = [
+            ctypes.c_char, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
+            ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
+            ctypes.c_void_p, ctypes.c_int64, ctypes.c_int]
         _lib = lib
     return _lib
 
@@ -71,26 +76,38 @@ def default_threads() -> int:
                else (os.cpu_count() or 1))
 
 
-def potrf_one(A: np.ndarray) -> tuple[np.ndarray, int]:
-    """Factor one dense matrix (only its lower triangle is used).
+def _upper(uplo: str) -> bool:
+    if uplo not in ("L", "U", "l", "u"):
+        raise ValueError(f"uplo must be 'L' or 'U', not {uplo!r}")
+    return uplo in ("U", "u")
+
+
+def potrf_one(A: np.ndarray, uplo: str = "L") -> tuple[np.ndarray, int]:
+    """Factor one dense matrix (only its lower triangle is used; with
+    ``uplo="U"`` only its upper triangle).
 
     ``A`` is any n x n array; it is rounded to float32 first (the oracle's
-    input type). Returns (L as float64 n x n with L[i, j] = l_ij, info)."""
+    input type). Returns (the factor as float64 n x n, info): L[i, j] = l_ij
+    (A = L L^T), or with "U" U[i, j] = u_ij (A = U^T U)."""
     a32 = np.asfortranarray(np.asarray(A, dtype=np.float32))
     n = a32.shape[0]
     L = np.zeros((n, n), dtype=np.float64, order="F")
-    info = _load().oracle_potrf_one(a32.ctypes.data, n, max(1, n), L.ctypes.data, max(1, n))
+    lib = _load()
+    fn = lib.oracle_potrf_upper_one if _upper(uplo) else lib.oracle_potrf_one
+    info = fn(a32.ctypes.data, n, max(1, n), L.ctypes.data, max(1, n))
     return np.ascontiguousarray(L), int(info)
 
 
 def potrf_batched(buf: np.ndarray, n: int, lda: int, strideA: int, batch: int,
                   indices: Optional[Sequence[int]] = None,
-                  nthreads: Optional[int] = None) -> tuple[np.ndarray, np.ndarray, int]:
+                  nthreads: Optional[int] = None,
+                  uplo: str = "L") -> tuple[np.ndarray, np.ndarray, int]:
     """Factor matrices of a strided float32 batch.
 
     ``buf`` is flat float32 with A_b(i, j) at ``buf[b*strideA + i + j*lda]``.
     ``indices`` picks a subset of b (default: all). Returns (L, info, threads)
-    with L[t, i, j] = l_ij of the t-th picked matrix (float64) and info[t].
+    with L[t, i, j] = l_ij of the t-th picked matrix (float64) and info[t];
+    with ``uplo="U"`` the upper triangles are read and L[t, i, j] = u_ij.
     """
     lib = _load()
     buf = np.ascontiguousarray(buf, dtype=np.float32)
@@ -107,13 +124,15 @@ def potrf_batched(buf: np.ndarray, n: int, lda: int, strideA: int, batch: int,
     L = np.zeros((m, n, n), dtype=np.float64)  # [t, j, i]: column-major per matrix
     info = np.zeros(m, dtype=np.int32)
     th = default_threads() if nthreads is None else nthreads
-    used = lib.oracle_potrf_batched(src.ctypes.data, n, lda, sA, m, L.ctypes.data,
-                                    n * n, info.ctypes.data, th)
+    used = lib.oracle_potrf_batched_uplo(b"U" if _upper(uplo) else b"L", src.ctypes.data, n,
+                                         lda, sA, m, L.ctypes.data, n * n, info.ctypes.data,
+                                         th)
     return L.transpose(0, 2, 1), info, int(used)
 
 
-def potrs_one(L: np.ndarray, B: np.ndarray) -> np.ndarray:
-    """Solve (L L^T) X = B for one factor (only its lower triangle is used).
+def potrs_one(L: np.ndarray, B: np.ndarray, uplo: str = "L") -> np.ndarray:
+    """Solve (L L^T) X = B for one factor (only its lower triangle is used);
+    with ``uplo="U"`` solve (U^T U) X = B, U = ``L``'s upper triangle.
 
     ``L`` (n x n) and ``B`` (n x nrhs, or a vector) are rounded to float32
     first (the oracle's input type). Returns X as float64 of B's shape."""
@@ -123,8 +142,10 @@ def potrs_one(L: np.ndarray, B: np.ndarray) -> np.ndarray:
     b32 = np.asfortranarray(b.reshape(b.shape[0], -1))
     n, nrhs = b32.shape
     X = np.zeros((n, nrhs), dtype=np.float64, order="F")
-    _load().oracle_potrs_one(l32.ctypes.data, n, max(1, n), b32.ctypes.data, nrhs, max(1, n),
-                             X.ctypes.data, max(1, n))
+    lib = _load()
+    fn = lib.oracle_potrs_upper_one if _upper(uplo) else lib.oracle_potrs_one
+    fn(l32.ctypes.data, n, max(1, n), b32.ctypes.data, nrhs, max(1, n), X.ctypes.data,
+       max(1, n))
     X = np.ascontiguousarray(X)
     return X[:, 0] if vec else X
 
@@ -132,12 +153,13 @@ def potrs_one(L: np.ndarray, B: np.ndarray) -> np.ndarray:
 def potrs_batched(lbuf: np.ndarray, n: int, lda: int, strideA: int, bbuf: np.ndarray,
                   nrhs: int, ldb: int, strideB: int, batch: int,
                   indices: Optional[Sequence[int]] = None,
-                  nthreads: Optional[int] = None) -> tuple[np.ndarray, int]:
+                  nthreads: Optional[int] = None, uplo: str = "L") -> tuple[np.ndarray, int]:
     """Solve A_b X_b = B_b with the factors of a strided float32 batch.
 
     ``lbuf`` holds L_b(i, j) at ``lbuf[b*strideA + i + j*lda]`` (lower triangle
-    read), ``bbuf`` B_b(i, c) at ``bbuf[b*strideB + i + c*ldb]``. ``indices``
-    picks a subset of b. Returns (X, threads) with X[t, i, c] (float64)."""
+    read; with ``uplo="U"`` the upper factor U_b, upper triangle read),
+    ``bbuf`` B_b(i, c) at ``bbuf[b*strideB + i + c*ldb]``. ``indices`` picks a
+    subset of b. Returns (X, threads) with X[t, i, c] (float64)."""
     lib = _load()
     lbuf = np.ascontiguousarray(lbuf, dtype=np.float32)
     bbuf = np.ascontiguousarray(bbuf, dtype=np.float32)
@@ -155,6 +177,7 @@ def potrs_batched(lbuf: np.ndarray, n: int, lda: int, strideA: int, bbuf: np.nda
         sA, sB = spanL, spanB
     X = np.zeros((m, nrhs, n), dtype=np.float64)  # [t, c, i]: column-major per matrix
     th = default_threads() if nthreads is None else nthreads
-    used = lib.oracle_potrs_batched(ls.ctypes.data, n, lda, sA, bs.ctypes.data, nrhs, ldb, sB,
-                                    m, X.ctypes.data, n * nrhs, th)
+    used = lib.oracle_potrs_batched_uplo(b"U" if _upper(uplo) else b"L", ls.ctypes.data, n,
+                                         lda, sA, bs.ctypes.data, nrhs, ldb, sB, m,
+                                         X.ctypes.data, n * nrhs, th)
     return X.transpose(0, 2, 1), int(used)

@@ -195,3 +195,126 @@ def test_trs_mutant_is_caught(name, tmp_path):
         assert failed == [], failed
     else:
         assert failed, f"planted mistake {name!r} passed every pin"
+
+
+# --------------------------------------------------------------------------
+# uplo = 'U': mistakes planted in the upper-triangle functions only
+# --------------------------------------------------------------------------
+
+UPPER_MUTANTS = {
+    "identity": ("", ""),
+    "pivot sign": ("d -= ukj * ukj;", "d += ukj * ukj;"),
+    "lower triangle read": ("double s = (double)A[j + (int64_t)i * lda];",
+                            "double s = (double)A[i + (int64_t)j * lda];"),
+    "transposed operand": ("s -= U[k + (int64_t)j * ldu] * U[k + (int64_t)i * ldu];",
+                           "s -= U[k + (int64_t)j * ldu] * U[i + (int64_t)k * ldu];"),
+    "dropped update term": ("for (int k = 0; k < j; ++k)\n                s -=",
+                            "for (int k = 0; k + 1 < j; ++k)\n                s -="),
+    "info zero-based": ("return j + 1;", "return j;"),
+    "zero pivot passes": ("if (!(d > 0.0))", "if (d < 0.0)"),
+}
+
+UPPER_TRS_MUTANTS = {
+    "identity": ("", ""),
+    "forward reads the lower triangle": ("s -= (double)U[k + (int64_t)i * lda] * x[k];",
+                                         "s -= (double)U[i + (int64_t)k * lda] * x[k];"),
+    "backward transposed": ("s -= (double)U[i + (int64_t)k * lda] * x[k];",
+                            "s -= (double)U[k + (int64_t)i * lda] * x[k];"),
+    "backward skipped": ("for (int i = n - 1; i >= 0; --i) {", "for (int i = n - 1; i >= n; --i) {"),
+    "dropped forward term": ("for (int k = 0; k < i; ++k)", "for (int k = 1; k < i; ++k)"),
+}
+
+
+def _compile_after(src_path: str, marker: str, old: str, new: str, tmp_path, tag: str):
+    """Compile ``src_path`` with the first ``old`` after ``marker`` replaced."""
+    src = open(src_path).read()
+    if old:
+        at = src.index(marker)
+        pos = src.index(old, at)
+        src = src[:pos] + new + src[pos + len(old):]
+    c = tmp_path / f"{tag}.c"
+    so = tmp_path / f"{tag}.so"
+    c.write_text(src)
+    subprocess.run(["gcc", "-O1", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
+                    str(c), "-o", str(so), "-lm"], check=True)
+    return ctypes.CDLL(str(so))
+
+
+def _potrf_upper(lib, A):
+    a32 = np.asfortranarray(np.asarray(A, dtype=np.float32))
+    n = a32.shape[0]
+    U = np.zeros((n, n), order="F")
+    info = lib.oracle_potrf_upper_one(a32.ctypes.data, n, n, U.ctypes.data, n)
+    return np.ascontiguousarray(U), info
+
+
+def _upper_battery(lib) -> list[str]:
+    from tests.test_oracle_upper import _int_upper
+    lib.oracle_potrf_upper_one.restype = ctypes.c_int
+    lib.oracle_potrf_upper_one.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_void_p, ctypes.c_int]
+    failed = []
+    U = _int_upper(16, 17)
+    A = (U.T @ U).astype(np.float32)
+    Ap = np.triu(A) + np.tril(np.full_like(A, 1e30), -1)
+    Uo, info = _potrf_upper(lib, Ap)
+    if info != 0 or not np.array_equal(Uo, U):
+        failed.append("integer factor")
+    g = np.random.default_rng(12)
+    for n in (3, 4):
+        for t in range(20):
+            G = g.standard_normal((n, n))
+            A32 = ((G @ G.T + 0.1 * np.eye(n)) if t % 2 else (G + G.T)).astype(np.float32)
+            Lb, ib = _brute(np.ascontiguousarray(A32.T))
+            Uo, io = _potrf_upper(lib, A32)
+            m = n if ib == 0 else ib - 1
+            if io != ib or (m and not np.allclose(Uo[:m, :], Lb[:, :m].T, rtol=1e-9,
+                                                  atol=1e-12)):
+                failed.append(f"brute n={n}")
+                break
+    d = np.array([1.0, 4.0, 0.0, 9.0], dtype=np.float32)
+    if _potrf_upper(lib, np.diag(d))[1] != 3:
+        failed.append("diagonal zero")
+    return failed
+
+
+@pytest.mark.parametrize("name", list(UPPER_MUTANTS))
+def test_upper_mutant_is_caught(name, tmp_path):
+    old, new = UPPER_MUTANTS[name]
+    lib = _compile_after(SRC, "int oracle_potrf_upper_one(", old, new, tmp_path, "u")
+    failed = _upper_battery(lib)
+    if name == "identity":
+        assert failed == [], failed
+    else:
+        assert failed, f"planted mistake {name!r} passed every pin"
+
+
+def _upper_trs_battery(lib) -> list[str]:
+    from tests.test_oracle_upper import _int_upper
+    lib.oracle_potrs_upper_one.restype = None
+    lib.oracle_potrs_upper_one.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_void_p, ctypes.c_int]
+    failed = []
+    n = 9
+    U = _int_upper(n, 5)
+    X = np.random.default_rng(6).integers(-5, 6, (n, 3)).astype(np.float64)
+    B = U.T @ (U @ X)
+    Up = np.asfortranarray((U + np.tril(np.full((n, n), 1e30), -1)).astype(np.float32))
+    b32 = np.asfortranarray(B.astype(np.float32))
+    Xo = np.zeros((n, 3), order="F")
+    lib.oracle_potrs_upper_one(Up.ctypes.data, n, n, b32.ctypes.data, 3, n, Xo.ctypes.data, n)
+    if not np.array_equal(Xo, X):
+        failed.append("integer solution")
+    return failed
+
+
+@pytest.mark.parametrize("name", list(UPPER_TRS_MUTANTS))
+def test_upper_trs_mutant_is_caught(name, tmp_path):
+    old, new = UPPER_TRS_MUTANTS[name]
+    lib = _compile_after(SRC_TRS, "void oracle_potrs_upper_one(", old, new, tmp_path, "ut")
+    failed = _upper_trs_battery(lib)
+    if name == "identity":
+        assert failed == [], failed
+    else:
+        assert failed, f"planted mistake {name!r} passed every pin"
