@@ -204,11 +204,17 @@ class DeviceWorkload:
     def flush_l2(self):
         self.flush.fill_(1.0)
 
+    uplo = "L"
+
     def call(self, i: int, stream) -> None:
         import matrix_dense_linear_gb300 as bl
         bt = self.bt
-        code = bl.spotrf_batched(self.rep[i].data_ptr(), bt.n, bt.lda, bt.strideA, bt.batch,
-                                 self.info, stream)
+        if self.uplo == "L":
+            code = bl.spotrf_batched(self.rep[i].data_ptr(), bt.n, bt.lda, bt.strideA, bt.batch,
+                                     self.info, stream)
+        else:
+            code = bl.spotrf_batched_uplo(self.uplo, self.rep[i].data_ptr(), bt.n, bt.lda,
+                                          bt.strideA, bt.batch, self.info, stream)
         if code:
             raise bl.BLError(code)
 
@@ -568,6 +574,7 @@ def run_shapes(args) -> list:
         buf = np.ascontiguousarray(np.tile(base.buf, reps)[: batch * n * n])
         bt = type(base)(buf=buf, n=n, lda=n, strideA=n * n, batch=batch, fill=base.fill)
         w = DeviceWorkload(bt, args.steps, dev)
+        w.uplo = args.uplo
         for i in range(min(args.warmup, w.nrep)):
             w.call(i, torch.cuda.current_stream().cuda_stream)
         torch.cuda.synchronize()
@@ -575,7 +582,7 @@ def run_shapes(args) -> list:
         ms = statistics.median(time_steps(w, k, lambda: None) / k for _ in range(3))
         assert not w.info.cpu().numpy().any()
         rf = roofline_entry("shape", n, batch, ms, pk, sms)
-        row = {"shape": spec, "n": n, "batch": batch, "ms_per_call": ms,
+        row = {"shape": spec, "uplo": args.uplo, "n": n, "batch": batch, "ms_per_call": ms,
                "us_per_call": ms * 1e3, "matrices_per_s": batch / (ms / 1e3),
                "tflops": flops_per_matrix(n) * batch / (ms / 1e3) / 1e12,
                "roofline": {k2: rf[k2] for k2 in ("bound", "frac", "roof_ms")},
@@ -726,6 +733,8 @@ def main():
     ap.add_argument("--shapes", default=None, metavar="NxB,...",
                     help="time these (n, batch) shapes (one JSON line each); 'pages' = "
                          "the shapes the pages quote timings for")
+    ap.add_argument("--uplo", choices=["L", "U"], default="L",
+                    help="storage of the factor for --shapes (U: upper triangle)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

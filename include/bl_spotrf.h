@@ -1,6 +1,7 @@
 /*
  * bl_spotrf.h - batched single-precision Cholesky factorization (SPOTRF,
- * uplo = 'L') for many small independent matrices on one NVIDIA GB300 (sm_103a).
+ * uplo = 'L' or 'U') and the solves with the factor (SPOTRS, SPOSV) for many
+ * small independent matrices on one NVIDIA GB300 (sm_103a).
  *
  * The operation. For each b < batch, the symmetric positive definite matrix
  * A_b = A + b*strideA (column-major, element (i, j) at A_b[i + j*lda]) is
@@ -189,6 +190,36 @@ int bl_spotrs_batched(const float *L, int n, int lda, int64_t strideA, float *B,
  */
 int bl_sposv_batched(float *A, int n, int lda, int64_t strideA, float *B, int nrhs, int ldb,
                      int64_t strideB, int batch, int *info, cudaStream_t stream);
+
+/*
+ * The uplo = 'U' forms (LAPACK's other storage; also the lower triangle of a
+ * row-major matrix, such as a (batch, n, n) row-major tensor). With uplo 'U'
+ * or 'u' the factor is A_b = U_b^T U_b, U_b upper triangular with a positive
+ * diagonal (U_b = L_b^T of the same symmetric matrix: the same pivots, the
+ * same info), and only the upper triangle (i <= j, j < n) of each A_b is read
+ * and written; the strict lower triangle, rows n..lda-1 and the gaps stay
+ * untouched. The solve reads U_b's upper triangle: U^T Y = B, then U X = Y.
+ * uplo 'L' or 'l' is exactly the call without uplo.
+ *
+ * uplo is argument 1, so every other argument's index is one higher than in
+ * the call without it: -1 for an invalid uplo, then the codes of that call
+ * minus one, in the same order (bl_spotrf_batched_uplo: -2 A, -3 n, -4 lda,
+ * -5 strideA, -6 batch, -7 info, -8 n > BL_SPOTRF_MAX_N; _ex: -9 route or a
+ * route that cannot run n, which includes BL_ROUTE_TMEM for 'U';
+ * bl_spotrs_batched_uplo: -2 .. -10; bl_sposv_batched_uplo: -2 .. -11).
+ * Positive values are cudaError_t codes, as above. Kernels: the same routes;
+ * for n > 128 with 'U' the panel solve and the trailing update run on the
+ * FP32 kernels, not the tensor cores.
+ */
+int bl_spotrf_batched_uplo(char uplo, float *A, int n, int lda, int64_t strideA, int batch,
+                           int *info, cudaStream_t stream);
+int bl_spotrf_batched_uplo_ex(char uplo, float *A, int n, int lda, int64_t strideA, int batch,
+                              int *info, cudaStream_t stream, int route);
+int bl_spotrs_batched_uplo(char uplo, const float *A, int n, int lda, int64_t strideA, float *B,
+                           int nrhs, int ldb, int64_t strideB, int batch, cudaStream_t stream);
+int bl_sposv_batched_uplo(char uplo, float *A, int n, int lda, int64_t strideA, float *B,
+                          int nrhs, int ldb, int64_t strideB, int batch, int *info,
+                          cudaStream_t stream);
 
 /* Version string of the library ("bl_spotrf <major>.<minor> sm_103a"). */
 const char *bl_spotrf_version(void);

@@ -25,7 +25,7 @@ library_path = os.path.join(_PKG, "libbl_spotrf.so")
 _lib = None
 
 # (name, restype, argtypes) of every symbol include/bl_spotrf.h declares
-_VP, _I, _I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+_VP, _I, _I64, _C = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_char
 SYMBOLS = {
     "bl_spotrf_batched": (_I, [_VP, _I, _I, _I64, _I, _VP, _VP]),
     "bl_spotrf_batched_ex": (_I, [_VP, _I, _I, _I64, _I, _VP, _VP, _I]),
@@ -35,6 +35,10 @@ SYMBOLS = {
     "bl_spotrf_batched_host": (_I, [_VP, _I, _I, _I64, _I, _VP, _VP, _VP, _I, _VP, _I]),
     "bl_spotrs_batched": (_I, [_VP, _I, _I, _I64, _VP, _I, _I, _I64, _I, _VP]),
     "bl_sposv_batched": (_I, [_VP, _I, _I, _I64, _VP, _I, _I, _I64, _I, _VP, _VP]),
+    "bl_spotrf_batched_uplo": (_I, [_C, _VP, _I, _I, _I64, _I, _VP, _VP]),
+    "bl_spotrf_batched_uplo_ex": (_I, [_C, _VP, _I, _I, _I64, _I, _VP, _VP, _I]),
+    "bl_spotrs_batched_uplo": (_I, [_C, _VP, _I, _I, _I64, _VP, _I, _I, _I64, _I, _VP]),
+    "bl_sposv_batched_uplo": (_I, [_C, _VP, _I, _I, _I64, _VP, _I, _I, _I64, _I, _VP, _VP]),
 }
 
 
@@ -95,6 +99,36 @@ def spotrf_batched_ex(A, n: int, lda: int, strideA: int, batch: int, info, strea
                                           _stream(stream), route)
 
 
+def _uplo(uplo) -> bytes:
+    return uplo.encode() if isinstance(uplo, str) else bytes(uplo)
+
+
+def spotrf_batched_uplo(uplo, A, n: int, lda: int, strideA: int, batch: int, info, stream=None,
+                        route: int = ROUTE_AUTO) -> int:
+    """bl_spotrf_batched_uplo(_ex): uplo "L" or "U" ("U": A = U^T U in the upper
+    triangles; the lower triangle of a row-major matrix). Returns the status;
+    argument indices count uplo as argument 1."""
+    if route == ROUTE_AUTO:
+        return library().bl_spotrf_batched_uplo(_uplo(uplo), _ptr(A), n, lda, strideA, batch,
+                                                _ptr(info), _stream(stream))
+    return library().bl_spotrf_batched_uplo_ex(_uplo(uplo), _ptr(A), n, lda, strideA, batch,
+                                               _ptr(info), _stream(stream), route)
+
+
+def spotrs_batched_uplo(uplo, L, n: int, lda: int, strideA: int, B, nrhs: int, ldb: int,
+                        strideB: int, batch: int, stream=None) -> int:
+    """bl_spotrs_batched_uplo: the solve with an upper ("U") or lower factor."""
+    return library().bl_spotrs_batched_uplo(_uplo(uplo), _ptr(L), n, lda, strideA, _ptr(B),
+                                            nrhs, ldb, strideB, batch, _stream(stream))
+
+
+def sposv_batched_uplo(uplo, A, n: int, lda: int, strideA: int, B, nrhs: int, ldb: int,
+                       strideB: int, batch: int, info, stream=None) -> int:
+    """bl_sposv_batched_uplo: factor (upper or lower storage) and solve."""
+    return library().bl_sposv_batched_uplo(_uplo(uplo), _ptr(A), n, lda, strideA, _ptr(B), nrhs,
+                                           ldb, strideB, batch, _ptr(info), _stream(stream))
+
+
 def route(n: int, batch: int) -> int:
     """bl_spotrf_route: the kernel class chosen for (n, batch); needs no GPU."""
     return library().bl_spotrf_route(n, batch)
@@ -125,16 +159,25 @@ def sposv_batched(A, n: int, lda: int, strideA: int, B, nrhs: int, ldb: int, str
                                       batch, _ptr(info), _stream(stream))
 
 
-def solve(L, n, lda, strideA, B, nrhs, ldb, strideB, batch, stream=None) -> None:
-    """spotrs_batched, raising BLError on a nonzero status."""
-    code = spotrs_batched(L, n, lda, strideA, B, nrhs, ldb, strideB, batch, stream)
+def solve(L, n, lda, strideA, B, nrhs, ldb, strideB, batch, stream=None, uplo="L") -> None:
+    """spotrs_batched(_uplo), raising BLError on a nonzero status."""
+    if uplo in ("L", b"L"):
+        code = spotrs_batched(L, n, lda, strideA, B, nrhs, ldb, strideB, batch, stream)
+    else:
+        code = spotrs_batched_uplo(uplo, L, n, lda, strideA, B, nrhs, ldb, strideB, batch,
+                                   stream)
     if code:
         raise BLError(code, "spotrs")
 
 
-def factor_solve(A, n, lda, strideA, B, nrhs, ldb, strideB, batch, info, stream=None) -> None:
-    """sposv_batched, raising BLError on a nonzero status."""
-    code = sposv_batched(A, n, lda, strideA, B, nrhs, ldb, strideB, batch, info, stream)
+def factor_solve(A, n, lda, strideA, B, nrhs, ldb, strideB, batch, info, stream=None,
+                 uplo="L") -> None:
+    """sposv_batched(_uplo), raising BLError on a nonzero status."""
+    if uplo in ("L", b"L"):
+        code = sposv_batched(A, n, lda, strideA, B, nrhs, ldb, strideB, batch, info, stream)
+    else:
+        code = sposv_batched_uplo(uplo, A, n, lda, strideA, B, nrhs, ldb, strideB, batch, info,
+                                  stream)
     if code:
         raise BLError(code, "sposv")
 
@@ -144,9 +187,12 @@ def version() -> str:
 
 
 def factor(A, n: int, lda: int, strideA: int, batch: int, info, stream=None,
-           route_: int = ROUTE_AUTO) -> None:
+           route_: int = ROUTE_AUTO, uplo="L") -> None:
     """Factor in place on the device; raises BLError on a nonzero status."""
-    code = spotrf_batched_ex(A, n, lda, strideA, batch, info, stream, route_)
+    if uplo in ("L", b"L"):
+        code = spotrf_batched_ex(A, n, lda, strideA, batch, info, stream, route_)
+    else:
+        code = spotrf_batched_uplo(uplo, A, n, lda, strideA, batch, info, stream, route_)
     if code:
         raise BLError(code)
 

@@ -50,38 +50,50 @@ int route_for(int n)
     return BL_ROUTE_BLOCKED;
 }
 
-bool route_can_run(int route, int n)
+bool route_can_run(int route, int n, bool upper)
 {
     switch (route) {
     case BL_ROUTE_WARP: return n <= kWarpMaxN;
     case BL_ROUTE_CTA: return n <= kCtaMaxN;
-    case BL_ROUTE_TMEM: return n <= kCtaMaxN;
+    case BL_ROUTE_TMEM: return n <= kCtaMaxN && !upper;
     case BL_ROUTE_BLOCKED: return true;
     default: return false;
     }
 }
 
 int run(float *A, int n, int lda, int64_t strideA, int batch, int *info, cudaStream_t stream,
-        int route)
+        int route, bool upper = false)
 {
     int e = check_args(A, n, lda, strideA, batch, info);
     if (e) return e;
     if (route == BL_ROUTE_AUTO) route = route_for(n);
-    if (!route_can_run(route, n)) return -8;
+    if (!route_can_run(route, n, upper)) return -8;
     if (batch == 0) return 0;
     if (n == 0) return (int)cudaMemsetAsync(info, 0, sizeof(int) * (size_t)batch, stream);
     if (trace_enabled())
-        std::fprintf(stderr, "bl_spotrf: n=%d lda=%d strideA=%lld batch=%d route=%d\n", n, lda,
-                     (long long)strideA, batch, route);
+        std::fprintf(stderr, "bl_spotrf: uplo=%c n=%d lda=%d strideA=%lld batch=%d route=%d\n",
+                     upper ? 'U' : 'L', n, lda, (long long)strideA, batch, route);
     switch (route) {
-    case BL_ROUTE_WARP: return bl::launch_warp(A, n, lda, strideA, batch, info, stream);
+    case BL_ROUTE_WARP: return bl::launch_warp(A, n, lda, strideA, batch, info, stream, upper);
     case BL_ROUTE_CTA:
-        return bl::launch_cta(A, n, lda, strideA, batch, info, stream, bl::InfoMode{-1});
+        return bl::launch_cta(A, n, lda, strideA, batch, info, stream, bl::InfoMode{-1}, upper);
     case BL_ROUTE_TMEM:
         return bl::launch_tmem(A, n, lda, strideA, batch, info, stream, bl::InfoMode{-1});
-    default: return bl::launch_blocked(A, n, lda, strideA, batch, info, stream);
+    default: return bl::launch_blocked(A, n, lda, strideA, batch, info, stream, upper);
     }
 }
+
+// uplo argument: 0 lower, 1 upper, -1 invalid
+int parse_uplo(char uplo)
+{
+    if (uplo == 'L' || uplo == 'l') return 0;
+    if (uplo == 'U' || uplo == 'u') return 1;
+    return -1;
+}
+
+// the uplo entry points take uplo as argument 1: every other argument index
+// moves up by one
+int shift_arg(int e) { return e < 0 ? e - 1 : e; }
 
 int check_trs_args(const float *L, int n, int lda, int64_t strideA, const float *B, int nrhs,
                    int ldb, int64_t strideB, int batch)
@@ -147,26 +159,84 @@ int bl_spotrf_batched_host(float *A_host, int n, int lda, int64_t strideA, int b
     return 0;
 }
 
-int bl_spotrs_batched(const float *L, int n, int lda, int64_t strideA, float *B, int nrhs,
-                      int ldb, int64_t strideB, int batch, cudaStream_t stream)
+}  // extern "C"
+
+namespace {
+
+int spotrs(bool upper, const float *L, int n, int lda, int64_t strideA, float *B, int nrhs,
+           int ldb, int64_t strideB, int batch, cudaStream_t stream)
 {
     const int e = check_trs_args(L, n, lda, strideA, B, nrhs, ldb, strideB, batch);
     if (e) return e;
     if (batch == 0 || n == 0 || nrhs == 0) return 0;
     if (trace_enabled())
-        std::fprintf(stderr, "bl_spotrs: n=%d nrhs=%d batch=%d\n", n, nrhs, batch);
-    return bl::launch_potrs(L, n, lda, strideA, B, nrhs, ldb, strideB, batch, nullptr, stream);
+        std::fprintf(stderr, "bl_spotrs: uplo=%c n=%d nrhs=%d batch=%d\n", upper ? 'U' : 'L', n,
+                     nrhs, batch);
+    return bl::launch_potrs(L, n, lda, strideA, B, nrhs, ldb, strideB, batch, nullptr, stream,
+                            upper);
+}
+
+int sposv(bool upper, float *A, int n, int lda, int64_t strideA, float *B, int nrhs, int ldb,
+          int64_t strideB, int batch, int *info, cudaStream_t stream)
+{
+    int e = check_trs_args(A, n, lda, strideA, B, nrhs, ldb, strideB, batch);
+    if (e) return e;
+    if (info == nullptr && batch > 0) return -10;
+    e = run(A, n, lda, strideA, batch, info, stream, BL_ROUTE_AUTO, upper);
+    if (e || batch == 0 || n == 0 || nrhs == 0) return e;
+    return bl::launch_potrs(A, n, lda, strideA, B, nrhs, ldb, strideB, batch, info, stream,
+                            upper);
+}
+
+}  // namespace
+
+extern "C" {
+
+int bl_spotrs_batched(const float *L, int n, int lda, int64_t strideA, float *B, int nrhs,
+                      int ldb, int64_t strideB, int batch, cudaStream_t stream)
+{
+    return spotrs(false, L, n, lda, strideA, B, nrhs, ldb, strideB, batch, stream);
 }
 
 int bl_sposv_batched(float *A, int n, int lda, int64_t strideA, float *B, int nrhs, int ldb,
                      int64_t strideB, int batch, int *info, cudaStream_t stream)
 {
-    int e = check_trs_args(A, n, lda, strideA, B, nrhs, ldb, strideB, batch);
-    if (e) return e;
-    if (info == nullptr && batch > 0) return -10;
-    e = run(A, n, lda, strideA, batch, info, stream, BL_ROUTE_AUTO);
-    if (e || batch == 0 || n == 0 || nrhs == 0) return e;
-    return bl::launch_potrs(A, n, lda, strideA, B, nrhs, ldb, strideB, batch, info, stream);
+    return sposv(false, A, n, lda, strideA, B, nrhs, ldb, strideB, batch, info, stream);
+}
+
+int bl_spotrs_batched_uplo(char uplo, const float *A, int n, int lda, int64_t strideA, float *B,
+                           int nrhs, int ldb, int64_t strideB, int batch, cudaStream_t stream)
+{
+    const int u = parse_uplo(uplo);
+    if (u < 0) return -1;
+    return shift_arg(spotrs(u == 1, A, n, lda, strideA, B, nrhs, ldb, strideB, batch, stream));
+}
+
+int bl_sposv_batched_uplo(char uplo, float *A, int n, int lda, int64_t strideA, float *B,
+                          int nrhs, int ldb, int64_t strideB, int batch, int *info,
+                          cudaStream_t stream)
+{
+    const int u = parse_uplo(uplo);
+    if (u < 0) return -1;
+    return shift_arg(sposv(u == 1, A, n, lda, strideA, B, nrhs, ldb, strideB, batch, info,
+                           stream));
+}
+
+int bl_spotrf_batched_uplo(char uplo, float *A, int n, int lda, int64_t strideA, int batch,
+                           int *info, cudaStream_t stream)
+{
+    const int u = parse_uplo(uplo);
+    if (u < 0) return -1;
+    return shift_arg(run(A, n, lda, strideA, batch, info, stream, BL_ROUTE_AUTO, u == 1));
+}
+
+int bl_spotrf_batched_uplo_ex(char uplo, float *A, int n, int lda, int64_t strideA, int batch,
+                              int *info, cudaStream_t stream, int route)
+{
+    const int u = parse_uplo(uplo);
+    if (u < 0) return -1;
+    if (route < BL_ROUTE_AUTO || route > BL_ROUTE_TMEM) return -9;
+    return shift_arg(run(A, n, lda, strideA, batch, info, stream, route, u == 1));
 }
 
 
@@ -193,7 +263,7 @@ int bl_spotrf_kernel_info(int route, int n, int *regs, int *local_bytes, int *st
                           int *dynamic_smem, int *threads)
 {
     if (route == BL_ROUTE_AUTO) route = route_for(n);
-    if (n < 1 || !route_can_run(route, n)) return -8;
+    if (n < 1 || !route_can_run(route, n, false)) return -8;
     cudaFuncAttributes fa{};
     int th = 0, dyn = 0, e;
     switch (route) {

@@ -59,6 +59,17 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Where the factor lives. uplo = 'L': A = L L^T, l_ik (i >= k) at A[i + k lda],
+// the column-major lower triangle. uplo = 'U': A = U^T U with U = L^T, so the
+// same number l_ik = u_ki sits at A[k + i lda], the column-major upper
+// triangle (equivalently the lower triangle of the row-major matrix). Every
+// kernel computes L and only its addressing depends on the storage.
+template <bool UP>
+__device__ __forceinline__ int64_t lidx(int i, int k, int lda)
+{
+    return UP ? (int64_t)k + (int64_t)i * lda : (int64_t)i + (int64_t)k * lda;
+}
+
 // Programmatic dependent launch. Kernels launched with launch_pdl may start
 // while the previous kernel in the stream is still running; they call
 // pdl_wait() before their first access to global memory (it returns once the
@@ -104,14 +115,15 @@ struct InfoMode {
     int off;
 };
 
+// `upper`: the factor is stored in the upper triangle (uplo = 'U', see lidx).
 int launch_warp(float *A, int n, int lda, int64_t strideA, int batch, int *info,
-                cudaStream_t stream);
+                cudaStream_t stream, bool upper);
 int launch_cta(float *A, int n, int lda, int64_t strideA, int batch, int *info,
-               cudaStream_t stream, InfoMode mode);
+               cudaStream_t stream, InfoMode mode, bool upper);
 int launch_tmem(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                 cudaStream_t stream, InfoMode mode);
 int launch_blocked(float *A, int n, int lda, int64_t strideA, int batch, int *info,
-                   cudaStream_t stream);
+                   cudaStream_t stream, bool upper);
 
 int launch_syrk_tc(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
                    cudaStream_t stream);
@@ -120,7 +132,7 @@ int launch_trsm_tc(float *A, int n, int lda, int64_t strideA, int batch, int *in
                    cudaStream_t stream);
 
 int launch_potrs(const float *L, int n, int lda, int64_t strideA, float *B, int nrhs, int ldb,
-                 int64_t strideB, int batch, const int *info, cudaStream_t stream);
+                 int64_t strideB, int batch, const int *info, cudaStream_t stream, bool upper);
 int attrs_potrs(cudaFuncAttributes *fa, int *threads, int *dyn_smem);
 int attrs_warp(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem);
 int attrs_cta(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem);

@@ -44,6 +44,7 @@ __device__ __forceinline__ const float *l11_col(const float *Ls, int k)
 // block jb first subtracts the row's already solved blocks kb < jb (reloaded
 // from memory, the next one prefetched while the current one is applied),
 // then solves against L11's diagonal block jb.
+template <bool UP>
 __global__ void __launch_bounds__(kTrsmRows, 3)
 trsm_panel_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
                   const int *__restrict__ info)
@@ -53,13 +54,13 @@ trsm_panel_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0
     const int64_t mat = blockIdx.x;
     if (info[mat] != 0) return;
     float *__restrict__ Ab = A + mat * strideA;
-    const float *L11 = Ab + c0 + (int64_t)c0 * lda;
+    const float *L11 = Ab + c0 + (int64_t)c0 * lda;  // element (c0, c0), either storage
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
 
     for (int j = warp; j < kNb; j += kTrsmRows / 32) {
         float *dst = const_cast<float *>(l11_col(Ls, j));
-        for (int i = j + lane; i < kNb; i += 32) cp_async4(dst + i, L11 + i + (int64_t)j * lda);
+        for (int i = j + lane; i < kNb; i += 32) cp_async4(dst + i, L11 + lidx<UP>(i, j, lda));
     }
     cp_async_commit();
     cp_async_wait<0>();
@@ -70,23 +71,25 @@ trsm_panel_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0
     const int r0 = c0 + kNb;
     const int row = r0 + blockIdx.y * kTrsmRows + tid;
     if (row >= n) return;
-    float *X = Ab + row + (int64_t)c0 * lda;  // X[k*lda] = element (row, c0 + k)
+    // X[k * xs] = element (row, c0 + k) of L
+    float *X = Ab + lidx<UP>(row, c0, lda);
+    const int64_t xs = UP ? 1 : lda;
 
 #pragma unroll 1
     for (int jb = 0; jb < kNb / 32; ++jb) {
         float x[32], xp[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) x[c] = X[(int64_t)(32 * jb + c) * lda];
+        for (int c = 0; c < 32; ++c) x[c] = X[(int64_t)(32 * jb + c) * xs];
         if (jb > 0) {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) xp[c] = X[(int64_t)c * lda];
+            for (int c = 0; c < 32; ++c) xp[c] = X[(int64_t)c * xs];
         }
 #pragma unroll 1
         for (int kb = 0; kb < jb; ++kb) {
             float xn[32];
             if (kb + 1 < jb) {
 #pragma unroll
-                for (int c = 0; c < 32; ++c) xn[c] = X[(int64_t)(32 * (kb + 1) + c) * lda];
+                for (int c = 0; c < 32; ++c) xn[c] = X[(int64_t)(32 * (kb + 1) + c) * xs];
             }
 #pragma unroll
             for (int kk = 0; kk < 32; ++kk) {
@@ -125,7 +128,7 @@ trsm_panel_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0
             }
         }
 #pragma unroll
-        for (int c = 0; c < 32; ++c) X[(int64_t)(32 * jb + c) * lda] = x[c];
+        for (int c = 0; c < 32; ++c) X[(int64_t)(32 * jb + c) * xs] = x[c];
     }
 }
 
@@ -166,6 +169,23 @@ __device__ __forceinline__ void syrk_stage(float (*As)[kTile + 4], float (*Bs)[k
     }
 }
 
+// Upper storage: element (r, k) of an operand is at L[k + r lda]; sixteen
+// consecutive threads read one row's 16 k-values (coalesced 4-byte copies).
+__device__ __forceinline__ void syrk_stage_upper(float (*As)[kTile + 4], float (*Bs)[kTile + 4],
+                                                 const float *Li, const float *Lk, int lda,
+                                                 int kc, int mi, int mk, int tid)
+{
+#pragma unroll 4
+    for (int e = 0; e < (kKc * kTile) / 256; ++e) {
+        const int idx = tid + 256 * e;
+        const int k = idx & (kKc - 1), r = idx / kKc;
+        const int64_t o = (int64_t)r * lda + kc + k;
+        cp_async4_zfill(&As[k][r], Li + (r < mi ? o : 0), r < mi ? 4 : 0);
+        cp_async4_zfill(&Bs[k][r], Lk + (r < mk ? o : 0), r < mk ? 4 : 0);
+    }
+}
+
+template <bool UP>
 __global__ void __launch_bounds__(256)
 syrk_tile_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
                  const int *__restrict__ info)
@@ -187,14 +207,18 @@ syrk_tile_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     const int c1 = c0 + kNb;
     const int m = n - c1;
     const int ri = I * kTile, rk = K * kTile;  // tile origin, trailing coordinates
-    const float *Li = Ab + c1 + ri + (int64_t)c0 * lda;  // L21 rows ri.., column c0
-    const float *Lk = Ab + c1 + rk + (int64_t)c0 * lda;
+    const float *Li = Ab + lidx<UP>(c1 + ri, c0, lda);  // L21 rows ri.., column c0
+    const float *Lk = Ab + lidx<UP>(c1 + rk, c0, lda);
     const int mi = m - ri, mk = m - rk;
     const bool vec = ((reinterpret_cast<uintptr_t>(Li) & 15) == 0) &&
                      ((reinterpret_cast<uintptr_t>(Lk) & 15) == 0) && ((lda & 3) == 0);
     const int tid = threadIdx.x;
     // ty (rows) fastest: a warp's 16 row groups of one column are contiguous
     const int ty = tid & 15, tx = tid >> 4;
+    auto stage = [&](int buf, int kc) {
+        if constexpr (UP) syrk_stage_upper(As[buf], Bs[buf], Li, Lk, lda, kc, mi, mk, tid);
+        else syrk_stage(As[buf], Bs[buf], Li, Lk, lda, kc, mi, mk, vec, tid);
+    };
 
     float acc[8][8];
 #pragma unroll
@@ -202,13 +226,11 @@ syrk_tile_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
 #pragma unroll
         for (int b = 0; b < 8; ++b) acc[a][b] = 0.0f;
 
-    syrk_stage(As[0], Bs[0], Li, Lk, lda, 0, mi, mk, vec, tid);
+    stage(0, 0);
     cp_async_commit();
 #pragma unroll 1
     for (int c = 0; c < kNb / kKc; ++c) {
-        if (c + 1 < kNb / kKc)
-            syrk_stage(As[(c + 1) & 1], Bs[(c + 1) & 1], Li, Lk, lda, (c + 1) * kKc, mi, mk,
-                       vec, tid);
+        if (c + 1 < kNb / kKc) stage((c + 1) & 1, (c + 1) * kKc);
         cp_async_commit();
         cp_async_wait<1>();
         __syncthreads();
@@ -230,7 +252,37 @@ syrk_tile_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
         __syncthreads();
     }
 
-    float *C = Ab + c1 + (int64_t)c1 * lda;
+    float *C = Ab + c1 + (int64_t)c1 * lda;  // element (c1, c1), either storage
+    if constexpr (UP) {
+        // element (gr, gc) of the trailing lower triangle at C[gc + gr lda]:
+        // the four columns 4tx + b of one row are contiguous
+        const bool full = ((reinterpret_cast<uintptr_t>(C) & 15) == 0) && ((lda & 3) == 0) &&
+                          I != K && ri + kTile <= m && rk + kTile <= m;
+#pragma unroll
+        for (int ah = 0; ah < 2; ++ah)
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                const int gr = ri + 64 * ah + 4 * ty + a;
+#pragma unroll
+                for (int bh = 0; bh < 2; ++bh) {
+                    const int gc0 = rk + 64 * bh + 4 * tx;
+                    float *p = C + gc0 + (int64_t)gr * lda;
+                    if (full) {
+                        float4 v = *reinterpret_cast<float4 *>(p);
+                        v.x -= acc[4 * ah + a][4 * bh + 0];
+                        v.y -= acc[4 * ah + a][4 * bh + 1];
+                        v.z -= acc[4 * ah + a][4 * bh + 2];
+                        v.w -= acc[4 * ah + a][4 * bh + 3];
+                        *reinterpret_cast<float4 *>(p) = v;
+                    } else if (gr < m) {
+#pragma unroll
+                        for (int b = 0; b < 4; ++b)
+                            if (gc0 + b < m && gr >= gc0 + b) p[b] -= acc[4 * ah + a][4 * bh + b];
+                    }
+                }
+            }
+        return;
+    }
     const bool full = vec && ((reinterpret_cast<uintptr_t>(C) & 15) == 0) && I != K &&
                       ri + kTile <= m && rk + kTile <= m;
 #pragma unroll
@@ -264,29 +316,39 @@ syrk_tile_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
 }  // namespace
 
 int launch_blocked(float *A, int n, int lda, int64_t strideA, int batch, int *info,
-                   cudaStream_t stream)
+                   cudaStream_t stream, bool upper)
 {
     for (int c0 = 0; c0 < n; c0 += kNb) {
         const int nb = n - c0 < kNb ? n - c0 : kNb;
         int e = launch_cta(A + c0 + (int64_t)c0 * lda, nb, lda, strideA, batch, info, stream,
-                           InfoMode{c0 == 0 ? -1 : c0});
+                           InfoMode{c0 == 0 ? -1 : c0}, upper);
         if (e) return e;
         const int m = n - c0 - nb;
         if (m <= 0) break;
         // block updates of the panel solve on the tensor cores when aligned
-        e = launch_trsm_tc(A, n, lda, strideA, batch, info, c0, stream);
+        // (lower storage), else FP32
+        e = upper ? 1 : launch_trsm_tc(A, n, lda, strideA, batch, info, c0, stream);
         if (e == 1) {
             dim3 gt((unsigned)batch, (unsigned)((m + kTrsmRows - 1) / kTrsmRows));
-            trsm_panel_kernel<<<gt, kTrsmRows, 0, stream>>>(A, n, lda, strideA, c0, info);
+            if (upper)
+                trsm_panel_kernel<true><<<gt, kTrsmRows, 0, stream>>>(A, n, lda, strideA, c0,
+                                                                      info);
+            else
+                trsm_panel_kernel<false><<<gt, kTrsmRows, 0, stream>>>(A, n, lda, strideA, c0,
+                                                                       info);
             e = (int)cudaGetLastError();
         }
         if (e) return e;
-        // tensor cores (3xTF32) when the panels are 16-byte aligned, else FP32
-        e = launch_syrk_tc(A, n, lda, strideA, batch, info, c0, stream);
+        // tensor cores (3xTF32) when the panels are 16-byte aligned (lower
+        // storage), else FP32
+        e = upper ? 1 : launch_syrk_tc(A, n, lda, strideA, batch, info, c0, stream);
         if (e == 1) {
             const int T = (m + kTile - 1) / kTile;
             dim3 gs((unsigned)batch, (unsigned)(T * (T + 1) / 2));
-            syrk_tile_kernel<<<gs, 256, 0, stream>>>(A, n, lda, strideA, c0, info);
+            if (upper)
+                syrk_tile_kernel<true><<<gs, 256, 0, stream>>>(A, n, lda, strideA, c0, info);
+            else
+                syrk_tile_kernel<false><<<gs, 256, 0, stream>>>(A, n, lda, strideA, c0, info);
             e = (int)cudaGetLastError();
         }
         if (e) return e;

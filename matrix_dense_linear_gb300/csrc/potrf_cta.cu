@@ -23,7 +23,8 @@
 //      panel's columns, then (look-ahead) one warp factors the next diagonal
 //      block while the other warps update the remaining columns;
 // with one __syncthreads after each phase. Rows and columns n .. NP-1 are an
-// identity block. Entries above the diagonal inside a diagonal block of the
+// identity block. The upper storage (uplo = 'U') only changes the load and
+// the store: row c of L is copied from / to column c of the upper triangle. Entries above the diagonal inside a diagonal block of the
 // storage are scratch: they are never read into a lower result or stored.
 #include <mutex>
 
@@ -124,11 +125,44 @@ __device__ __forceinline__ void store_columns(const float *S, float *Ab, int n, 
     }
 }
 
+// Upper storage (uplo = 'U'): row c of L is the contiguous column c of the
+// upper triangle in memory (l_ck at Ab[k + c lda], k <= c). Rows c >= k0 of
+// columns [k0, k1) are copied by warp c mod NW, lanes over k (coalesced 4-byte
+// reads, each element to its place in the packed columns); then the identity
+// rows of those columns as in load_columns.
+template <int NB, int NT>
+__device__ __forceinline__ void load_upper(float *S, const float *Ab, int n, int lda, int k0,
+                                           int k1, int warp, int lane)
+{
+    constexpr int NP = CtaGeom<NB>::NP;
+    for (int c = k0 + warp; c < n; c += NT / 32) {
+        const float *g = Ab + (int64_t)c * lda;
+        const int kend = c + 1 < k1 ? c + 1 : k1;
+        for (int k = k0 + lane; k < kend; k += 32) cp_async4(elem_ptr<NB>(S, c, k), g + k);
+    }
+    for (int k = k0 + warp; k < k1; k += NT / 32) {
+        float *col = elem_ptr<NB>(S, 0, k);
+        const int hi = k < n ? n : k;
+        for (int i = hi + lane; i < NP; i += 32) col[i] = (i == k) ? 1.0f : 0.0f;
+    }
+}
+
+template <int NB, int NT>
+__device__ __forceinline__ void store_upper(const float *S, float *Ab, int n, int lda, int warp,
+                                            int lane)
+{
+    for (int c = warp; c < n; c += NT / 32) {
+        float *g = Ab + (int64_t)c * lda;
+        for (int k = lane; k <= c; k += 32) g[k] = *elem_ptr<NB>(const_cast<float *>(S), c, k);
+    }
+}
+
 // FULL: n == NP and 16-byte aligned columns (the launcher checks): bulk copies.
 // At n = 128 a thread gets 128 registers and four blocks share an SM: measured
 // on GB300 that beats five blocks at 96 registers (60 against 67 us for 1024
 // matrices).
-template <int NB, int NT, bool FULL>
+// UP: the factor lives in the upper triangle (never with FULL).
+template <int NB, int NT, bool FULL, bool UP>
 __global__ void __launch_bounds__(NT, NB >= 3 ? 4 : 8)
 potrf_cta_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int batch,
                  int *__restrict__ info, int info_off)
@@ -170,6 +204,12 @@ potrf_cta_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int bat
     if constexpr (FULL) {
         bulk_load_full<NB>(S, Ab, lda, tid, mbar);
         if (tid == 0 && !tc::mbar_wait(&mbar[0], 0, kWaitCycles)) sh_err = 1;
+    } else if constexpr (UP) {
+        load_upper<NB, NT>(S, Ab, n, lda, 0, 32, warp, lane);
+        cp_async_commit();
+        load_upper<NB, NT>(S, Ab, n, lda, 32, NP, warp, lane);
+        cp_async_commit();
+        cp_async_wait<1>();
     } else {
         load_columns<NB, NT>(S, Ab, n, lda, 0, 32, vec, warp, lane);
         cp_async_commit();
@@ -254,7 +294,8 @@ potrf_cta_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int bat
     } else {
         cp_async_wait<0>();  // a failed panel 0 leaves the loop before the first wait
         __syncthreads();
-        store_columns<NB, NT>(S, Ab, n, lda, vec, warp, lane);
+        if constexpr (UP) store_upper<NB, NT>(S, Ab, n, lda, warp, lane);
+        else store_columns<NB, NT>(S, Ab, n, lda, vec, warp, lane);
     }
     if (tid == 0) {
         const int f = sh_fail;
@@ -263,7 +304,7 @@ potrf_cta_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int bat
     }
 }
 
-template <int NB, int NT, bool FULL>
+template <int NB, int NT, bool FULL, bool UP>
 int launch_v(float *A, int n, int lda, int64_t strideA, int batch, int *info, cudaStream_t st,
              int info_off)
 {
@@ -271,23 +312,24 @@ int launch_v(float *A, int n, int lda, int64_t strideA, int batch, int *info, cu
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(potrf_cta_kernel<NB, NT, FULL>,
+        attr_err = cudaFuncSetAttribute(potrf_cta_kernel<NB, NT, FULL, UP>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     });
     if (attr_err != cudaSuccess) return (int)attr_err;
-    return launch_pdl(potrf_cta_kernel<NB, NT, FULL>, dim3((unsigned)batch), dim3(NT),
+    return launch_pdl(potrf_cta_kernel<NB, NT, FULL, UP>, dim3((unsigned)batch), dim3(NT),
                       (size_t)bytes, st, A, n, lda, strideA, batch, info, info_off);
 }
 
 template <int NB, int NT>
 int launch_nb(float *A, int n, int lda, int64_t strideA, int batch, int *info, cudaStream_t st,
-              int info_off)
+              int info_off, bool upper)
 {
+    if (upper) return launch_v<NB, NT, false, true>(A, n, lda, strideA, batch, info, st, info_off);
     const bool vec = ((reinterpret_cast<uintptr_t>(A) & 15) == 0) && ((lda & 3) == 0) &&
                      ((strideA & 3) == 0);
     if (vec && n == CtaGeom<NB>::NP)
-        return launch_v<NB, NT, true>(A, n, lda, strideA, batch, info, st, info_off);
-    return launch_v<NB, NT, false>(A, n, lda, strideA, batch, info, st, info_off);
+        return launch_v<NB, NT, true, false>(A, n, lda, strideA, batch, info, st, info_off);
+    return launch_v<NB, NT, false, false>(A, n, lda, strideA, batch, info, st, info_off);
 }
 
 // the n = NP bulk-copy kernel (the one the n = 128 and blocked workloads run)
@@ -296,18 +338,19 @@ int attrs_nb(cudaFuncAttributes *fa, int *threads, int *dyn)
 {
     *threads = NT;
     *dyn = CtaGeom<NB>::bytes;
-    return (int)cudaFuncGetAttributes(fa, potrf_cta_kernel<NB, NT, true>);
+    return (int)cudaFuncGetAttributes(fa, potrf_cta_kernel<NB, NT, true, false>);
 }
 
 }  // namespace
 
 int launch_cta(float *A, int n, int lda, int64_t strideA, int batch, int *info,
-               cudaStream_t stream, InfoMode mode)
+               cudaStream_t stream, InfoMode mode, bool upper)
 {
-    if (n <= 32) return launch_nb<1, 32>(A, n, lda, strideA, batch, info, stream, mode.off);
-    if (n <= 64) return launch_nb<2, 64>(A, n, lda, strideA, batch, info, stream, mode.off);
-    if (n <= 96) return launch_nb<3, 128>(A, n, lda, strideA, batch, info, stream, mode.off);
-    return launch_nb<4, 128>(A, n, lda, strideA, batch, info, stream, mode.off);
+    const int o = mode.off;
+    if (n <= 32) return launch_nb<1, 32>(A, n, lda, strideA, batch, info, stream, o, upper);
+    if (n <= 64) return launch_nb<2, 64>(A, n, lda, strideA, batch, info, stream, o, upper);
+    if (n <= 96) return launch_nb<3, 128>(A, n, lda, strideA, batch, info, stream, o, upper);
+    return launch_nb<4, 128>(A, n, lda, strideA, batch, info, stream, o, upper);
 }
 
 int attrs_cta(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem)

@@ -29,7 +29,7 @@ namespace {
 
 constexpr int kWarpsPerBlock = 1;  // one warp per block: blocks spread evenly over the SMs
 
-template <int N>
+template <int N, bool UP>
 __global__ void __launch_bounds__(32 * kWarpsPerBlock)
 potrf_warp_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int batch,
                   int *__restrict__ info)
@@ -52,7 +52,7 @@ potrf_warp_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int ba
 #pragma unroll
     for (int k = 0; k < N; ++k) {
         float v = (row == k) ? 1.0f : 0.0f;
-        if (live && k <= row) v = Ab[row + (int64_t)k * lda];
+        if (live && k <= row) v = Ab[lidx<UP>(row, k, lda)];
         r[k] = v;
     }
 
@@ -85,10 +85,10 @@ potrf_warp_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int ba
 
 #pragma unroll
     for (int k = 0; k < N; ++k)
-        if (live && k <= row) Ab[row + (int64_t)k * lda] = r[k];
+        if (live && k <= row) Ab[lidx<UP>(row, k, lda)] = r[k];
     // the diagonal from the lane's own pivot (sqrt(+Inf) = +Inf, like the
     // definition); info = the group's lowest row whose pivot failed
-    if (live) Ab[row + (int64_t)row * lda] = sqrt_approx(dm);
+    if (live) Ab[lidx<UP>(row, row, lda)] = sqrt_approx(dm);
     const unsigned bad = __ballot_sync(0xffffffffu, live && !pivot_ok(dm));
     constexpr unsigned kGroupMask = (N == 32) ? 0xffffffffu : ((1u << (N & 31)) - 1u);
     const unsigned mine = (bad >> (grp * N)) & kGroupMask;
@@ -101,6 +101,7 @@ potrf_warp_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int ba
 // compile-time split, since the column loop is unrolled). The pivot test and
 // the diagonal's square root are taken once at the end from each lane's own
 // pivot (info by a warp ballot: the lowest failing row).
+template <bool UP>
 __global__ void __launch_bounds__(32 * kWarpsPerBlock)
 potrf_warp64_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int batch,
                     int *__restrict__ info)
@@ -121,13 +122,13 @@ potrf_warp64_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int 
 #pragma unroll
     for (int k = 0; k < 32; ++k) {
         float v = (rowa == k) ? 1.0f : 0.0f;
-        if (livea && k <= rowa) v = Ab[rowa + (int64_t)k * lda];
+        if (livea && k <= rowa) v = Ab[lidx<UP>(rowa, k, lda)];
         ra[k] = v;
     }
 #pragma unroll
     for (int k = 0; k < 64; ++k) {
         float v = (rowb == k) ? 1.0f : 0.0f;
-        if (liveb && k <= rowb) v = Ab[rowb + (int64_t)k * lda];
+        if (liveb && k <= rowb) v = Ab[lidx<UP>(rowb, k, lda)];
         rb[k] = v;
     }
 
@@ -169,13 +170,13 @@ potrf_warp64_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int 
 
 #pragma unroll
     for (int k = 0; k < 32; ++k)
-        if (livea && k <= rowa) Ab[rowa + (int64_t)k * lda] = ra[k];
+        if (livea && k <= rowa) Ab[lidx<UP>(rowa, k, lda)] = ra[k];
 #pragma unroll
     for (int k = 0; k < 64; ++k)
-        if (liveb && k <= rowb) Ab[rowb + (int64_t)k * lda] = rb[k];
+        if (liveb && k <= rowb) Ab[lidx<UP>(rowb, k, lda)] = rb[k];
     // diagonal entries from the pivots (sqrt(+Inf) = +Inf, like the definition)
-    if (livea) Ab[rowa + (int64_t)rowa * lda] = sqrt_approx(da);
-    if (liveb) Ab[rowb + (int64_t)rowb * lda] = sqrt_approx(db);
+    if (livea) Ab[lidx<UP>(rowa, rowa, lda)] = sqrt_approx(da);
+    if (liveb) Ab[lidx<UP>(rowb, rowb, lda)] = sqrt_approx(db);
     const unsigned fa = __ballot_sync(0xffffffffu, livea && !pivot_ok(da));
     const unsigned fb = __ballot_sync(0xffffffffu, liveb && !pivot_ok(db));
     if (valid && lane == 0) info[mat] = fa ? __ffs(fa) : (fb ? 32 + __ffs(fb) : 0);
@@ -189,6 +190,7 @@ potrf_warp64_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int 
 // w = (c rsqrt d) rsqrt d as warp 0 takes for that row), then factors the block
 // alone as the n <= 32 kernel does. One 64-thread barrier per column keeps the
 // two in step; the serial path per lane drops from 2.5k to 1.5k FMAs.
+template <bool UP>
 __global__ void __maxnreg__(136)
 potrf_warp64x2_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int batch,
                       int *__restrict__ info)
@@ -210,8 +212,8 @@ potrf_warp64x2_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, in
         float ra[32], rb[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-            ra[k] = (k <= rowa) ? Ab[rowa + (int64_t)k * lda] : 0.0f;
-            rb[k] = liveb ? Ab[rowb + (int64_t)k * lda] : 0.0f;
+            ra[k] = (k <= rowa) ? Ab[lidx<UP>(rowa, k, lda)] : 0.0f;
+            rb[k] = liveb ? Ab[lidx<UP>(rowb, k, lda)] : 0.0f;
         }
         float da = 1.0f;
 #pragma unroll
@@ -246,10 +248,10 @@ potrf_warp64x2_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, in
         }
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-            if (k < rowa) Ab[rowa + (int64_t)k * lda] = ra[k];
-            if (liveb) Ab[rowb + (int64_t)k * lda] = rb[k];
+            if (k < rowa) Ab[lidx<UP>(rowa, k, lda)] = ra[k];
+            if (liveb) Ab[lidx<UP>(rowb, k, lda)] = rb[k];
         }
-        Ab[rowa + (int64_t)rowa * lda] = sqrt_approx(da);
+        Ab[lidx<UP>(rowa, rowa, lda)] = sqrt_approx(da);
         const unsigned bad = __ballot_sync(0xffffffffu, !pivot_ok(da));
         if (lane == 0) fail_a = bad;
     } else {
@@ -258,7 +260,7 @@ potrf_warp64x2_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, in
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
             float v = (k == lane) ? 1.0f : 0.0f;
-            if (liveb && k <= lane) v = Ab[rowb + (int64_t)(32 + k) * lda];
+            if (liveb && k <= lane) v = Ab[lidx<UP>(rowb, (32 + k), lda)];
             rc[k] = v;
         }
 #pragma unroll 1
@@ -302,8 +304,8 @@ potrf_warp64x2_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, in
         if (liveb) {
 #pragma unroll
             for (int k = 0; k < 32; ++k)
-                if (k < lane) Ab[rowb + (int64_t)(32 + k) * lda] = rc[k];
-            Ab[rowb + (int64_t)rowb * lda] = sqrt_approx(db);
+                if (k < lane) Ab[lidx<UP>(rowb, (32 + k), lda)] = rc[k];
+            Ab[lidx<UP>(rowb, rowb, lda)] = sqrt_approx(db);
         }
         const unsigned bad = __ballot_sync(0xffffffffu, liveb && !pivot_ok(db));
         __syncwarp();
@@ -317,13 +319,13 @@ potrf_warp64x2_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, in
     named_bar_sync(2, 64);
 }
 
-template <int N>
+template <int N, bool UP>
 int launch_n(float *A, int n, int lda, int64_t strideA, int batch, int *info, cudaStream_t st)
 {
     constexpr int G = 32 / N;
     const int64_t per_block = (int64_t)kWarpsPerBlock * G;
     const int64_t blocks = (batch + per_block - 1) / per_block;
-    return launch_pdl(potrf_warp_kernel<N>, dim3((unsigned)blocks), dim3(32 * kWarpsPerBlock), 0,
+    return launch_pdl(potrf_warp_kernel<N, UP>, dim3((unsigned)blocks), dim3(32 * kWarpsPerBlock), 0,
                       st, A, n, lda, strideA, batch, info);
 }
 
@@ -348,34 +350,43 @@ int sm_count()
 // two-warp kernel (lower latency: 6.4 against 7.7 us for one matrix, 7.5
 // against 10.0 us for 152 on GB300); one warp per matrix above, where the
 // two-warp kernel would need a second wave (1024 matrices: 11.3 against 17.3 us).
+template <bool UP>
 int launch_64(float *A, int n, int lda, int64_t strideA, int batch, int *info, cudaStream_t st)
 {
     if ((int64_t)batch <= (int64_t)kX2BlocksPerSm * sm_count())
-        return launch_pdl(potrf_warp64x2_kernel, dim3((unsigned)batch), dim3(64), 0, st, A, n,
-                          lda, strideA, batch, info);
+        return launch_pdl(potrf_warp64x2_kernel<UP>, dim3((unsigned)batch), dim3(64), 0, st, A,
+                          n, lda, strideA, batch, info);
     const int64_t blocks = (batch + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    return launch_pdl(potrf_warp64_kernel, dim3((unsigned)blocks), dim3(32 * kWarpsPerBlock), 0,
+    return launch_pdl(potrf_warp64_kernel<UP>, dim3((unsigned)blocks), dim3(32 * kWarpsPerBlock), 0,
                       st, A, n, lda, strideA, batch, info);
+}
+
+template <bool UP>
+int launch_uplo(float *A, int n, int lda, int64_t strideA, int batch, int *info,
+                cudaStream_t stream)
+{
+    if (n <= 8) return launch_n<8, UP>(A, n, lda, strideA, batch, info, stream);
+    if (n <= 16) return launch_n<16, UP>(A, n, lda, strideA, batch, info, stream);
+    if (n <= 32) return launch_n<32, UP>(A, n, lda, strideA, batch, info, stream);
+    return launch_64<UP>(A, n, lda, strideA, batch, info, stream);
 }
 
 }  // namespace
 
 int launch_warp(float *A, int n, int lda, int64_t strideA, int batch, int *info,
-                cudaStream_t stream)
+                cudaStream_t stream, bool upper)
 {
-    if (n <= 8) return launch_n<8>(A, n, lda, strideA, batch, info, stream);
-    if (n <= 16) return launch_n<16>(A, n, lda, strideA, batch, info, stream);
-    if (n <= 32) return launch_n<32>(A, n, lda, strideA, batch, info, stream);
-    return launch_64(A, n, lda, strideA, batch, info, stream);
+    return upper ? launch_uplo<true>(A, n, lda, strideA, batch, info, stream)
+                 : launch_uplo<false>(A, n, lda, strideA, batch, info, stream);
 }
 
 int attrs_warp(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem)
 {
     cudaError_t e;
-    if (n <= 8) e = cudaFuncGetAttributes(fa, potrf_warp_kernel<8>);
-    else if (n <= 16) e = cudaFuncGetAttributes(fa, potrf_warp_kernel<16>);
-    else if (n <= 32) e = cudaFuncGetAttributes(fa, potrf_warp_kernel<32>);
-    else e = cudaFuncGetAttributes(fa, potrf_warp64_kernel);  // the large-batch kernel
+    if (n <= 8) e = cudaFuncGetAttributes(fa, potrf_warp_kernel<8, false>);
+    else if (n <= 16) e = cudaFuncGetAttributes(fa, potrf_warp_kernel<16, false>);
+    else if (n <= 32) e = cudaFuncGetAttributes(fa, potrf_warp_kernel<32, false>);
+    else e = cudaFuncGetAttributes(fa, potrf_warp64_kernel<false>);  // the large-batch kernel
     *threads = 32 * kWarpsPerBlock;
     *dyn_smem = 0;
     return (int)e;

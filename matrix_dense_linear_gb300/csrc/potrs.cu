@@ -1,5 +1,6 @@
-// KS: batched SPOTRS (uplo = 'L'): solve A_b X_b = B_b in place of B_b with
-// the Cholesky factor L_b of A_b, as the two triangular solves of the posv
+// KS: batched SPOTRS: solve A_b X_b = B_b in place of B_b with the Cholesky
+// factor L_b of A_b (uplo = 'L'; with uplo = 'U' the factor U_b = L_b^T is
+// read from the upper triangle, the same solves), as the two triangular solves of the posv
 // composition of "BatchLAS perf_blackwell" (potrf, then L Y = B, then
 // L^T X = Y; "BatchLAS perf_trsm" fuses the solves for the tiny sizes).
 //
@@ -65,17 +66,19 @@ __device__ __forceinline__ void stage_solved(float *S, const float *Bb, int ldb,
 // Block (rb, cb) of L (rows 32rb.., columns 32cb..) into Ls.
 //   COLMAJOR: Ls[col * kLd + row] (element (row, col) of the block)
 //   else:     Ls[row * kLd + col]
-template <int NT, bool COLMAJOR>
+// A warp reads one column of the block from the lower storage and one row
+// from the upper (UP), both contiguous in memory.
+template <int NT, bool COLMAJOR, bool UP>
 __device__ __forceinline__ void stage_L(float *Ls, const float *Lb, int lda, int n, int rb, int cb,
                                         int tid)
 {
 #pragma unroll 4
     for (int e = 0; e < 1024 / NT; ++e) {
         const int idx = tid + NT * e;
-        const int row = idx & 31, col = idx >> 5;  // row fastest: a warp reads one column
+        const int row = UP ? idx >> 5 : idx & 31, col = UP ? idx & 31 : idx >> 5;
         const int gr = 32 * rb + row, gc = 32 * cb + col;
         float *dst = COLMAJOR ? Ls + col * kLd + row : Ls + row * kLd + col;
-        cp4(dst, Lb + gr + (int64_t)gc * lda, gr < n && gc < n && gr >= gc);
+        cp4(dst, Lb + lidx<UP>(gr, gc, lda), gr < n && gc < n && gr >= gc);
     }
 }
 
@@ -129,7 +132,7 @@ __device__ __forceinline__ void block_product(float (&acc)[C], const float *Ls, 
     }
 }
 
-template <int W, int C>
+template <int W, int C, bool UP>
 __global__ void __launch_bounds__(32 * W, W == 4 ? 8 : 9)
 potrs_kernel(const float *__restrict__ L, int n, int lda, int64_t strideA, float *__restrict__ B,
              int nrhs, int ldb, int64_t strideB, const int *__restrict__ info)
@@ -159,7 +162,7 @@ potrs_kernel(const float *__restrict__ L, int n, int lda, int64_t strideA, float
             acc[u] = (row < n && cw + u < nrhs) ? Bb[row + (int64_t)(cw + u) * ldb] : 0.0f;
         // block products with the solved blocks i < j (double-buffered)
         if (j > 0) {
-            stage_L<NT, true>(sm.L[0], Lb, lda, n, j, 0, tid);
+            stage_L<NT, true, UP>(sm.L[0], Lb, lda, n, j, 0, tid);
             stage_solved<NT, NC>(sm.S[0], Bb, ldb, n, nrhs, 0, c0, tid);
             cp_async_commit();
         }
@@ -167,7 +170,7 @@ potrs_kernel(const float *__restrict__ L, int n, int lda, int64_t strideA, float
         for (int i = 0; i < j; ++i) {
             const int buf = i & 1;
             if (i + 1 < j) {
-                stage_L<NT, true>(sm.L[buf ^ 1], Lb, lda, n, j, i + 1, tid);
+                stage_L<NT, true, UP>(sm.L[buf ^ 1], Lb, lda, n, j, i + 1, tid);
                 stage_solved<NT, NC>(sm.S[buf ^ 1], Bb, ldb, n, nrhs, i + 1, c0, tid);
                 cp_async_commit();
                 cp_async_wait<1>();
@@ -179,7 +182,7 @@ potrs_kernel(const float *__restrict__ L, int n, int lda, int64_t strideA, float
             __syncthreads();  // the buffer is restaged two products later
         }
         // the diagonal block, column-major: lane k reads l_(k,i) at D[i*kLd + k]
-        stage_L<NT, true>(sm.D, Lb, lda, n, j, j, tid);
+        stage_L<NT, true, UP>(sm.D, Lb, lda, n, j, j, tid);
         cp_async_commit();
         cp_async_wait<0>();
         __syncthreads();
@@ -225,7 +228,7 @@ potrs_kernel(const float *__restrict__ L, int n, int lda, int64_t strideA, float
         // block products with the solved blocks i > j: (L_ij)^T X_i, where lane
         // r needs l_(32i+k, 32j+r): L_ij staged row-major (Ls[k*kLd + r])
         if (j + 1 < NB) {
-            stage_L<NT, false>(sm.L[0], Lb, lda, n, j + 1, j, tid);
+            stage_L<NT, false, UP>(sm.L[0], Lb, lda, n, j + 1, j, tid);
             stage_solved<NT, NC>(sm.S[0], Bb, ldb, n, nrhs, j + 1, c0, tid);
             cp_async_commit();
         }
@@ -233,7 +236,7 @@ potrs_kernel(const float *__restrict__ L, int n, int lda, int64_t strideA, float
         for (int i = j + 1; i < NB; ++i) {
             const int buf = (i - j - 1) & 1;
             if (i + 1 < NB) {
-                stage_L<NT, false>(sm.L[buf ^ 1], Lb, lda, n, i + 1, j, tid);
+                stage_L<NT, false, UP>(sm.L[buf ^ 1], Lb, lda, n, i + 1, j, tid);
                 stage_solved<NT, NC>(sm.S[buf ^ 1], Bb, ldb, n, nrhs, i + 1, c0, tid);
                 cp_async_commit();
                 cp_async_wait<1>();
@@ -245,7 +248,7 @@ potrs_kernel(const float *__restrict__ L, int n, int lda, int64_t strideA, float
             __syncthreads();
         }
         // the diagonal block, row-major: lane k reads l_(i,k) at D[i*kLd + k]
-        stage_L<NT, false>(sm.D, Lb, lda, n, j, j, tid);
+        stage_L<NT, false, UP>(sm.D, Lb, lda, n, j, j, tid);
         cp_async_commit();
         cp_async_wait<0>();
         __syncthreads();
@@ -284,11 +287,14 @@ potrs_kernel(const float *__restrict__ L, int n, int lda, int64_t strideA, float
 
 template <int W, int C>
 int launch_wc(const float *L, int n, int lda, int64_t strideA, float *B, int nrhs, int ldb,
-              int64_t strideB, int batch, const int *info, cudaStream_t stream)
+              int64_t strideB, int batch, const int *info, cudaStream_t stream, bool upper)
 {
     const dim3 grid((unsigned)batch, (unsigned)((nrhs + W * C - 1) / (W * C)));
-    return launch_pdl(potrs_kernel<W, C>, grid, dim3(32 * W), 0, stream, L, n, lda, strideA, B,
-                      nrhs, ldb, strideB, info);
+    if (upper)
+        return launch_pdl(potrs_kernel<W, C, true>, grid, dim3(32 * W), 0, stream, L, n, lda,
+                          strideA, B, nrhs, ldb, strideB, info);
+    return launch_pdl(potrs_kernel<W, C, false>, grid, dim3(32 * W), 0, stream, L, n, lda,
+                      strideA, B, nrhs, ldb, strideB, info);
 }
 
 }  // namespace
@@ -296,9 +302,9 @@ int launch_wc(const float *L, int n, int lda, int64_t strideA, float *B, int nrh
 // Right-hand sides per block from nrhs: the narrowest shape that holds them,
 // up to 32 (4 warps x 8) per block.
 int launch_potrs(const float *L, int n, int lda, int64_t strideA, float *B, int nrhs, int ldb,
-                 int64_t strideB, int batch, const int *info, cudaStream_t stream)
+                 int64_t strideB, int batch, const int *info, cudaStream_t stream, bool upper)
 {
-#define BL_POTRS_ARGS L, n, lda, strideA, B, nrhs, ldb, strideB, batch, info, stream
+#define BL_POTRS_ARGS L, n, lda, strideA, B, nrhs, ldb, strideB, batch, info, stream, upper
     if (nrhs <= 1) return launch_wc<1, 1>(BL_POTRS_ARGS);
     if (nrhs <= 2) return launch_wc<1, 2>(BL_POTRS_ARGS);
     if (nrhs <= 4) return launch_wc<1, 4>(BL_POTRS_ARGS);
@@ -312,7 +318,7 @@ int attrs_potrs(cudaFuncAttributes *fa, int *threads, int *dyn_smem)
 {
     *threads = 128;
     *dyn_smem = 0;
-    return (int)cudaFuncGetAttributes(fa, potrs_kernel<4, 8>);
+    return (int)cudaFuncGetAttributes(fa, potrs_kernel<4, 8, false>);
 }
 
 }  // namespace bl

@@ -119,6 +119,38 @@ def test_trs_check_order(bl):
     assert lib.bl_sposv_batched(8, 4, 4, 16, None, 1, 4, 4, 2, None, None) == -5
 
 
+@pytest.mark.parametrize("uplo", [b"U", b"u", b"L", b"l"])
+def test_uplo_argument_codes_are_shifted(bl, uplo):
+    """The uplo entry points take uplo as argument 1: every code of the call
+    without it moves down by one (nothing below reaches the GPU)."""
+    lib = bl.library()
+    cases = [((8, -1, 1, 1, 1, 8), -2), ((8, 4, 4, 16, -1, 8), -5), ((8, 4, 3, 16, 2, 8), -3),
+             ((8, 4, 4, 15, 2, 8), -4), ((None, 4, 4, 16, 2, 8), -1),
+             ((8, 4, 4, 16, 2, None), -6), ((8, 4097, 4097, 4097 * 4097, 2, 8), -7)]
+    for args, code in cases:
+        assert lib.bl_spotrf_batched_uplo(uplo, *args, None) == code - 1
+        assert lib.bl_spotrf_batched_uplo_ex(uplo, *args, None, 0) == code - 1
+    assert lib.bl_spotrf_batched_uplo(uplo, None, 4, 4, 16, 0, None, None) == 0
+    assert lib.bl_spotrf_batched_uplo_ex(uplo, 8, 65, 65, 65 * 65, 1, 8, None,
+                                         bl.ROUTE_WARP) == -9
+    assert lib.bl_spotrf_batched_uplo_ex(uplo, 8, 4, 4, 16, 1, 8, None, 9) == -9
+    # solves: L/A -2, n -3, lda -4, strideA -5, B -6, nrhs -7, ldb -8, strideB -9, batch -10
+    assert lib.bl_spotrs_batched_uplo(uplo, 8, -1, 1, 1, 8, 1, 1, 1, 1, None) == -3
+    assert lib.bl_spotrs_batched_uplo(uplo, 8, 4, 4, 16, 8, 2, 4, 8, -1, None) == -10
+    assert lib.bl_spotrs_batched_uplo(uplo, 8, 4, 4, 16, None, 2, 4, 8, 2, None) == -6
+    assert lib.bl_sposv_batched_uplo(uplo, 8, 4, 4, 16, 8, 1, 4, 4, 2, None, None) == -11
+    assert lib.bl_sposv_batched_uplo(uplo, None, 4, 4, 16, 8, 1, 4, 4, 2, 8, None) == -2
+
+
+def test_bad_uplo(bl):
+    lib = bl.library()
+    for bad in (b"X", b"\x00", b"N"):
+        assert lib.bl_spotrf_batched_uplo(bad, 8, 4, 4, 16, 1, 8, None) == -1
+        assert lib.bl_spotrf_batched_uplo_ex(bad, 8, 4, 4, 16, 1, 8, None, 0) == -1
+        assert lib.bl_spotrs_batched_uplo(bad, 8, 4, 4, 16, 8, 1, 4, 4, 1, None) == -1
+        assert lib.bl_sposv_batched_uplo(bad, 8, 4, 4, 16, 8, 1, 4, 4, 1, 8, None) == -1
+
+
 def test_forced_route_that_cannot_run(bl):
     lib = bl.library()
     assert lib.bl_spotrf_batched_ex(8, 65, 65, 65 * 65, 1, 8, None, bl.ROUTE_WARP) == -8
