@@ -207,9 +207,8 @@ int bl_sposv_batched(float *A, int n, int lda, int64_t strideA, float *B, int nr
  * -5 strideA, -6 batch, -7 info, -8 n > BL_SPOTRF_MAX_N; _ex: -9 route or a
  * route that cannot run n, which includes BL_ROUTE_TMEM for 'U';
  * bl_spotrs_batched_uplo: -2 .. -10; bl_sposv_batched_uplo: -2 .. -11).
- * Positive values are cudaError_t codes, as above. Kernels: the same routes;
- * for n > 128 with 'U' the panel solve and the trailing update run on the
- * FP32 kernels, not the tensor cores.
+ * Positive values are cudaError_t codes, as above. Kernels: the same routes
+ * and the same arithmetic with transposed addresses (BL_ROUTE_TMEM excepted).
  */
 int bl_spotrf_batched_uplo(char uplo, float *A, int n, int lda, int64_t strideA, int batch,
                            int *info, cudaStream_t stream);

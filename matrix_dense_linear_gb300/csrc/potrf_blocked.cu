@@ -326,8 +326,7 @@ int launch_blocked(float *A, int n, int lda, int64_t strideA, int batch, int *in
         const int m = n - c0 - nb;
         if (m <= 0) break;
         // block updates of the panel solve on the tensor cores when aligned
-        // (lower storage), else FP32
-        e = upper ? 1 : launch_trsm_tc(A, n, lda, strideA, batch, info, c0, stream);
+        e = launch_trsm_tc(A, n, lda, strideA, batch, info, c0, stream, upper);
         if (e == 1) {
             dim3 gt((unsigned)batch, (unsigned)((m + kTrsmRows - 1) / kTrsmRows));
             if (upper)
@@ -339,9 +338,8 @@ int launch_blocked(float *A, int n, int lda, int64_t strideA, int batch, int *in
             e = (int)cudaGetLastError();
         }
         if (e) return e;
-        // tensor cores (3xTF32) when the panels are 16-byte aligned (lower
-        // storage), else FP32
-        e = upper ? 1 : launch_syrk_tc(A, n, lda, strideA, batch, info, c0, stream);
+        // tensor cores (3xTF32) when the panels are 16-byte aligned, else FP32
+        e = launch_syrk_tc(A, n, lda, strideA, batch, info, c0, stream, upper);
         if (e == 1) {
             const int T = (m + kTile - 1) / kTile;
             dim3 gs((unsigned)batch, (unsigned)(T * (T + 1) / 2));

@@ -27,34 +27,96 @@
 namespace bl {
 namespace {
 
-constexpr int kWarpsPerBlock = 1;  // one warp per block: blocks spread evenly over the SMs
+// Up to four warps (four matrices, or four groups of them) per block; the
+// launcher picks 1 or 4 (warps_per_block).
+constexpr int kMaxWarpsPerBlock = 4;
+
+// Row `row` of L, entries k0 .. k0+K-1: r[k] = l(row, k0 + k) where
+// k0 + k <= row and `live`; other entries keep their values. Lower storage:
+// 4-byte loads (the lanes of a warp read consecutive rows of one column).
+// Upper storage: the row is contiguous in memory; 16-byte loads where `vec`
+// and the whole quad lies on or left of the diagonal, 4-byte loads for the
+// partial quad, so nothing right of the diagonal is read.
+template <bool UP, int K>
+__device__ __forceinline__ void load_row(float (&r)[K], const float *Ab, int row, int k0,
+                                         int lda, bool live, bool vec)
+{
+    if constexpr (UP) {
+        const float *p = Ab + (int64_t)row * lda + k0;
+#pragma unroll
+        for (int q = 0; q < K / 4; ++q) {
+            if (live && vec && k0 + 4 * q + 3 <= row) {
+                const float4 v = *reinterpret_cast<const float4 *>(p + 4 * q);
+                r[4 * q] = v.x; r[4 * q + 1] = v.y; r[4 * q + 2] = v.z; r[4 * q + 3] = v.w;
+            } else {
+#pragma unroll
+                for (int t = 0; t < 4; ++t)
+                    if (live && k0 + 4 * q + t <= row) r[4 * q + t] = p[4 * q + t];
+            }
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < K; ++k)
+            if (live && k0 + k <= row) r[k] = Ab[lidx<false>(row, k0 + k, lda)];
+    }
+}
+
+// The inverse of load_row: entries k0 + k <= row of the row go back to memory.
+template <bool UP, int K>
+__device__ __forceinline__ void store_row(const float (&r)[K], float *Ab, int row, int k0,
+                                          int lda, bool live, bool vec)
+{
+    if constexpr (UP) {
+        float *p = Ab + (int64_t)row * lda + k0;
+#pragma unroll
+        for (int q = 0; q < K / 4; ++q) {
+            if (live && vec && k0 + 4 * q + 3 <= row) {
+                *reinterpret_cast<float4 *>(p + 4 * q) =
+                    make_float4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+            } else {
+#pragma unroll
+                for (int t = 0; t < 4; ++t)
+                    if (live && k0 + 4 * q + t <= row) p[4 * q + t] = r[4 * q + t];
+            }
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < K; ++k)
+            if (live && k0 + k <= row) Ab[lidx<false>(row, k0 + k, lda)] = r[k];
+    }
+}
+
+// 16-byte loads of the upper storage need A, lda and strideA in multiples of 4 floats
+__device__ __forceinline__ bool vec_ok(const float *A, int lda, int64_t strideA)
+{
+    return ((reinterpret_cast<uintptr_t>(A) & 15) == 0) && ((lda & 3) == 0) &&
+           ((strideA & 3) == 0);
+}
 
 template <int N, bool UP>
-__global__ void __launch_bounds__(32 * kWarpsPerBlock)
+__global__ void __launch_bounds__(32 * kMaxWarpsPerBlock)
 potrf_warp_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int batch,
                   int *__restrict__ info)
 {
     constexpr int G = 32 / N;  // matrices per warp
-    __shared__ __align__(16) float colbuf[kWarpsPerBlock][2][32];
+    __shared__ __align__(16) float colbuf[kMaxWarpsPerBlock][2][32];
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int grp = lane / N;
     const int row = lane - grp * N;
-    const int64_t mat = ((int64_t)blockIdx.x * kWarpsPerBlock + warp) * G + grp;
+    const int64_t mat = ((int64_t)blockIdx.x * (blockDim.x >> 5) + warp) * G + grp;
     const bool valid = mat < batch;
     const bool live = valid && row < n;
     float *__restrict__ Ab = A + (valid ? mat * strideA : 0);
     pdl_wait();
     pdl_trigger();
 
+    const bool vec = UP && vec_ok(A, lda, strideA);
     float r[N];
 #pragma unroll
-    for (int k = 0; k < N; ++k) {
-        float v = (row == k) ? 1.0f : 0.0f;
-        if (live && k <= row) v = Ab[lidx<UP>(row, k, lda)];
-        r[k] = v;
-    }
+    for (int k = 0; k < N; ++k) r[k] = (row == k) ? 1.0f : 0.0f;
+    load_row<UP>(r, Ab, row, 0, lda, live, vec);
 
     float dm = 1.0f;  // this lane's pivot
 #pragma unroll
@@ -83,9 +145,8 @@ potrf_warp_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int ba
         }
     }
 
-#pragma unroll
-    for (int k = 0; k < N; ++k)
-        if (live && k <= row) Ab[lidx<UP>(row, k, lda)] = r[k];
+    asm volatile("" : "+r"(lda));  // no load address lives to the stores
+    store_row<UP>(r, Ab, row, 0, lda, live, vec);
     // the diagonal from the lane's own pivot (sqrt(+Inf) = +Inf, like the
     // definition); info = the group's lowest row whose pivot failed
     if (live) Ab[lidx<UP>(row, row, lda)] = sqrt_approx(dm);
@@ -102,35 +163,33 @@ potrf_warp_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int ba
 // the diagonal's square root are taken once at the end from each lane's own
 // pivot (info by a warp ballot: the lowest failing row).
 template <bool UP>
-__global__ void __launch_bounds__(32 * kWarpsPerBlock)
+__global__ void __launch_bounds__(32 * kMaxWarpsPerBlock)
 potrf_warp64_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int batch,
                     int *__restrict__ info)
 {
-    __shared__ __align__(16) float colbuf[kWarpsPerBlock][2][64];
+    __shared__ __align__(16) float colbuf[kMaxWarpsPerBlock][2][64];
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int64_t mat = (int64_t)blockIdx.x * kWarpsPerBlock + warp;
+    const int64_t mat = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp;
     const bool valid = mat < batch;
     const int rowa = lane, rowb = lane + 32;
     const bool livea = valid && rowa < n, liveb = valid && rowb < n;
     float *__restrict__ Ab = A + (valid ? mat * strideA : 0);
+    // No early trigger here: the next launch's warps would take the free slots
+    // of this one's SMs (up to three warps per sub-partition at 153 registers)
+    // and then start unevenly (1024 matrices: 14.4 against 12.2 us in a chain
+    // of launches); the implicit trigger at exit keeps them out.
     pdl_wait();
-    pdl_trigger();
 
+    const bool vec = UP && vec_ok(A, lda, strideA);
     float ra[32], rb[64];
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
-        float v = (rowa == k) ? 1.0f : 0.0f;
-        if (livea && k <= rowa) v = Ab[lidx<UP>(rowa, k, lda)];
-        ra[k] = v;
-    }
+    for (int k = 0; k < 32; ++k) ra[k] = (rowa == k) ? 1.0f : 0.0f;
 #pragma unroll
-    for (int k = 0; k < 64; ++k) {
-        float v = (rowb == k) ? 1.0f : 0.0f;
-        if (liveb && k <= rowb) v = Ab[lidx<UP>(rowb, k, lda)];
-        rb[k] = v;
-    }
+    for (int k = 0; k < 64; ++k) rb[k] = (rowb == k) ? 1.0f : 0.0f;
+    load_row<UP>(ra, Ab, rowa, 0, lda, livea, vec);
+    load_row<UP>(rb, Ab, rowb, 0, lda, liveb, vec);
 
     float da = 1.0f, db = 1.0f;  // this lane's two pivots
 #pragma unroll
@@ -168,12 +227,12 @@ potrf_warp64_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int 
         }
     }
 
-#pragma unroll
-    for (int k = 0; k < 32; ++k)
-        if (livea && k <= rowa) Ab[lidx<UP>(rowa, k, lda)] = ra[k];
-#pragma unroll
-    for (int k = 0; k < 64; ++k)
-        if (liveb && k <= rowb) Ab[lidx<UP>(rowb, k, lda)] = rb[k];
+    // lda made opaque before the stores: otherwise the compiler keeps the load
+    // addresses alive across the whole factorization to reuse them here
+    // (n = 64: 211 against 153 registers a thread; two warps: 133 against 111)
+    asm volatile("" : "+r"(lda));
+    store_row<UP>(ra, Ab, rowa, 0, lda, livea, vec);
+    store_row<UP>(rb, Ab, rowb, 0, lda, liveb, vec);
     // diagonal entries from the pivots (sqrt(+Inf) = +Inf, like the definition)
     if (livea) Ab[lidx<UP>(rowa, rowa, lda)] = sqrt_approx(da);
     if (liveb) Ab[lidx<UP>(rowb, rowb, lda)] = sqrt_approx(db);
@@ -191,7 +250,7 @@ potrf_warp64_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int 
 // alone as the n <= 32 kernel does. One 64-thread barrier per column keeps the
 // two in step; the serial path per lane drops from 2.5k to 1.5k FMAs.
 template <bool UP>
-__global__ void __maxnreg__(136)
+__global__ void __launch_bounds__(64, 8)
 potrf_warp64x2_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int batch,
                       int *__restrict__ info)
 {
@@ -206,15 +265,15 @@ potrf_warp64x2_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, in
     pdl_trigger();
     const int rowb = lane + 32;
     const bool liveb = rowb < n;
+    const bool vec = UP && vec_ok(A, lda, strideA);
 
     if (warp == 0) {
         const int rowa = lane;  // < 32 < n
         float ra[32], rb[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-            ra[k] = (k <= rowa) ? Ab[lidx<UP>(rowa, k, lda)] : 0.0f;
-            rb[k] = liveb ? Ab[lidx<UP>(rowb, k, lda)] : 0.0f;
-        }
+        for (int k = 0; k < 32; ++k) ra[k] = rb[k] = 0.0f;
+        load_row<UP>(ra, Ab, rowa, 0, lda, true, vec);
+        load_row<UP>(rb, Ab, rowb, 0, lda, liveb, vec);
         float da = 1.0f;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
@@ -246,11 +305,9 @@ potrf_warp64x2_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, in
                 }
             }
         }
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-            if (k < rowa) Ab[lidx<UP>(rowa, k, lda)] = ra[k];
-            if (liveb) Ab[lidx<UP>(rowb, k, lda)] = rb[k];
-        }
+        asm volatile("" : "+r"(lda));  // no load address lives to the stores
+        store_row<UP>(ra, Ab, rowa, 0, lda, true, vec);  // its diagonal is rewritten below
+        store_row<UP>(rb, Ab, rowb, 0, lda, liveb, vec);
         Ab[lidx<UP>(rowa, rowa, lda)] = sqrt_approx(da);
         const unsigned bad = __ballot_sync(0xffffffffu, !pivot_ok(da));
         if (lane == 0) fail_a = bad;
@@ -258,11 +315,8 @@ potrf_warp64x2_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, in
         // rows 32..63 x columns 32..63; rows and columns n.. are the identity
         float rc[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-            float v = (k == lane) ? 1.0f : 0.0f;
-            if (liveb && k <= lane) v = Ab[lidx<UP>(rowb, (32 + k), lda)];
-            rc[k] = v;
-        }
+        for (int k = 0; k < 32; ++k) rc[k] = (k == lane) ? 1.0f : 0.0f;
+        load_row<UP>(rc, Ab, rowb, 32, lda, liveb, vec);
 #pragma unroll 1
         for (int j = 0; j < 32; ++j) {
             named_bar_sync(1, 64);
@@ -301,12 +355,9 @@ potrf_warp64x2_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, in
                 }
             }
         }
-        if (liveb) {
-#pragma unroll
-            for (int k = 0; k < 32; ++k)
-                if (k < lane) Ab[lidx<UP>(rowb, (32 + k), lda)] = rc[k];
-            Ab[lidx<UP>(rowb, rowb, lda)] = sqrt_approx(db);
-        }
+        asm volatile("" : "+r"(lda));  // no load address lives to the stores
+        store_row<UP>(rc, Ab, rowb, 32, lda, liveb, vec);  // its diagonal is rewritten below
+        if (liveb) Ab[lidx<UP>(rowb, rowb, lda)] = sqrt_approx(db);
         const unsigned bad = __ballot_sync(0xffffffffu, liveb && !pivot_ok(db));
         __syncwarp();
         named_bar_sync(2, 64);  // warp 0's failures are in fail_a
@@ -318,20 +369,6 @@ potrf_warp64x2_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, in
     }
     named_bar_sync(2, 64);
 }
-
-template <int N, bool UP>
-int launch_n(float *A, int n, int lda, int64_t strideA, int batch, int *info, cudaStream_t st)
-{
-    constexpr int G = 32 / N;
-    const int64_t per_block = (int64_t)kWarpsPerBlock * G;
-    const int64_t blocks = (batch + per_block - 1) / per_block;
-    return launch_pdl(potrf_warp_kernel<N, UP>, dim3((unsigned)blocks), dim3(32 * kWarpsPerBlock), 0,
-                      st, A, n, lda, strideA, batch, info);
-}
-
-// Blocks of the two-warp kernel that fit an SM (133 registers a thread: three
-// warps per sub-partition).
-constexpr int kX2BlocksPerSm = 6;
 
 int sm_count()
 {
@@ -346,18 +383,45 @@ int sm_count()
     return sms;
 }
 
-// n = 33 .. 64: two warps per matrix while the batch fits one wave of the
-// two-warp kernel (lower latency: 6.4 against 7.7 us for one matrix, 7.5
-// against 10.0 us for 152 on GB300); one warp per matrix above, where the
-// two-warp kernel would need a second wave (1024 matrices: 11.3 against 17.3 us).
+// Warps per block of the warp-per-matrix kernels. A warp runs on SM
+// sub-partition (its index in the block) mod 4, so blocks of four warps put
+// one warp on each; with single-warp blocks the block scheduler stacked three
+// warps on some sub-partitions while others held one (1024 matrices of order
+// 64: 14.4 against 10.9 us). Batches below four warps per SM keep one warp per
+// block so that every SM gets work.
+int warps_per_block(int64_t warps)
+{
+    return warps >= 4 * (int64_t)sm_count() ? 4 : 1;
+}
+
+template <int N, bool UP>
+int launch_n(float *A, int n, int lda, int64_t strideA, int batch, int *info, cudaStream_t st)
+{
+    constexpr int G = 32 / N;
+    const int wpb = warps_per_block((batch + G - 1) / G);
+    const int64_t per_block = (int64_t)wpb * G;
+    const int64_t blocks = (batch + per_block - 1) / per_block;
+    return launch_pdl(potrf_warp_kernel<N, UP>, dim3((unsigned)blocks), dim3(32 * wpb), 0,
+                      st, A, n, lda, strideA, batch, info);
+}
+
+// The two-warp kernel runs while its blocks put at most two warps on an SM
+// sub-partition (four blocks per SM); above, one warp per matrix is faster
+// (760 matrices of order 64: 10.3 against 12.6 us).
+constexpr int kX2BlocksPerSm = 4;
+
+// n = 33 .. 64: two warps per matrix for small batches (lower latency: one
+// matrix 6.4 against 7.7 us, 608 matrices 8.9 against 10.1 us on GB300), one
+// warp per matrix above.
 template <bool UP>
 int launch_64(float *A, int n, int lda, int64_t strideA, int batch, int *info, cudaStream_t st)
 {
     if ((int64_t)batch <= (int64_t)kX2BlocksPerSm * sm_count())
         return launch_pdl(potrf_warp64x2_kernel<UP>, dim3((unsigned)batch), dim3(64), 0, st, A,
                           n, lda, strideA, batch, info);
-    const int64_t blocks = (batch + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    return launch_pdl(potrf_warp64_kernel<UP>, dim3((unsigned)blocks), dim3(32 * kWarpsPerBlock), 0,
+    const int wpb = warps_per_block(batch);
+    const int64_t blocks = (batch + wpb - 1) / wpb;
+    return launch_pdl(potrf_warp64_kernel<UP>, dim3((unsigned)blocks), dim3(32 * wpb), 0,
                       st, A, n, lda, strideA, batch, info);
 }
 
@@ -387,7 +451,7 @@ int attrs_warp(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem)
     else if (n <= 16) e = cudaFuncGetAttributes(fa, potrf_warp_kernel<16, false>);
     else if (n <= 32) e = cudaFuncGetAttributes(fa, potrf_warp_kernel<32, false>);
     else e = cudaFuncGetAttributes(fa, potrf_warp64_kernel<false>);  // the large-batch kernel
-    *threads = 32 * kWarpsPerBlock;
+    *threads = 32 * kMaxWarpsPerBlock;
     *dyn_smem = 0;
     return (int)e;
 }

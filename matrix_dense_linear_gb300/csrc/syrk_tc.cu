@@ -21,7 +21,9 @@
 // 64(w/4)..) and subtracts it from A22 in place, lower triangle only.
 //
 // Every wait is bounded (about a second); a block that gives up marks the
-// matrix with info = -1 and still releases its tensor memory.
+// matrix with info = -1 and still releases its tensor memory. The upper
+// storage (uplo = 'U') changes only the addresses: a row of L is contiguous
+// there, so the 16-byte loads run along the rows and need no transpose.
 #include <mutex>
 
 #include "bl_common.cuh"
@@ -46,6 +48,7 @@ __device__ __forceinline__ uint32_t core_off(int r, int kq)
     return (uint32_t)(r >> 3) * kSbo + (uint32_t)kq * kLbo + (uint32_t)(r & 7) * 16;
 }
 
+template <bool UP>
 __global__ void __launch_bounds__(256, 2)
 syrk_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
                int *__restrict__ info)
@@ -71,14 +74,24 @@ syrk_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     const int m = n - c1;
     const int ri = I * 128, rk = K * 128;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // The MMA computes D[r][c] = sum_k L(tm + r, k) L(tn + c, k). Lower storage:
+    // (tm, tn) = (ri, rk), D is the tile itself. Upper storage: (tm, tn) =
+    // (rk, ri), D is the tile's transpose, so that in both storages the
+    // epilogue's element (r, c) lives at (c1 + tm + r) + (c1 + tn + c) lda: a
+    // warp's 32 rows r are contiguous in memory.
+    const int tm = UP ? rk : ri, tn = UP ? ri : rk;
 
-    // this thread stages one 4 x 4 block of one operand per slice
-    const int op = tid >> 7;            // 0: rows ri.. (A side), 1: rows rk.. (B side)
-    const int rq = tid & 31;            // row quad: rows 4rq .. 4rq+3
-    const int kq = (tid >> 5) & 3;      // k quad within the slice
-    const int rbase = op ? rk : ri;
+    // this thread stages one 4 x 4 block of one operand per slice; lower: a
+    // warp's lanes take 32 row quads (16-byte loads down a column), upper: 8
+    // row quads x 4 k quads (16-byte loads along the rows, 64 bytes a row)
+    const int op = tid >> 7;                            // 0: rows tm.. (A), 1: rows tn.. (B)
+    const int rq = UP ? (tid >> 2) & 31 : tid & 31;     // row quad: rows 4rq .. 4rq+3
+    const int kq = UP ? tid & 3 : (tid >> 5) & 3;       // k quad within the slice
+    const int rbase = op ? tn : tm;
     const int mrows = m - rbase;        // rows of this operand that exist
-    const float *src = Ab + c1 + rbase + 4 * rq + (int64_t)(c0 + 4 * kq) * lda;
+    // lower storage: src[c * lda + i] = (row 4rq + i, k = 4kq + c), 16 bytes down
+    // a column; upper storage: src[i * lda + c], 16 bytes along a row
+    const float *src = Ab + lidx<UP>(c1 + rbase + 4 * rq, c0 + 4 * kq, lda);
     const int valid_rows = max(0, min(4, mrows - 4 * rq));
 
     if (tid == 0) {
@@ -98,18 +111,24 @@ syrk_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     const uint32_t sbase = tc::smem_u32(smem);
     constexpr uint32_t idesc = tc::idesc_tf32(128, 128);
 
-    float4 cur[4], nxt[4], nxt2[4];
+    float4 cur[4], nxt[4], nxt2[4];  // lower: [k][4 rows]; upper: [row][4 k]
     auto load_slice = [&](int s, float4 (&v)[4]) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            const float *p = src + (int64_t)(s * kKs + c) * lda;
-            if (valid_rows == 4) {
-                v[c] = *reinterpret_cast<const float4 *>(p);
+            if constexpr (UP) {
+                const float *p = src + (int64_t)c * lda + s * kKs;
+                v[c] = valid_rows > c ? *reinterpret_cast<const float4 *>(p)
+                                      : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
             } else {
-                v[c].x = valid_rows > 0 ? p[0] : 0.0f;
-                v[c].y = valid_rows > 1 ? p[1] : 0.0f;
-                v[c].z = valid_rows > 2 ? p[2] : 0.0f;
-                v[c].w = 0.0f;
+                const float *p = src + (int64_t)(s * kKs + c) * lda;
+                if (valid_rows == 4) {
+                    v[c] = *reinterpret_cast<const float4 *>(p);
+                } else {
+                    v[c].x = valid_rows > 0 ? p[0] : 0.0f;
+                    v[c].y = valid_rows > 1 ? p[1] : 0.0f;
+                    v[c].z = valid_rows > 2 ? p[2] : 0.0f;
+                    v[c].w = 0.0f;
+                }
             }
         }
     };
@@ -128,12 +147,12 @@ syrk_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
         const float cv[4][4] = {{cur[0].x, cur[0].y, cur[0].z, cur[0].w},
                                 {cur[1].x, cur[1].y, cur[1].z, cur[1].w},
                                 {cur[2].x, cur[2].y, cur[2].z, cur[2].w},
-                                {cur[3].x, cur[3].y, cur[3].z, cur[3].w}};  // [k][row]
+                                {cur[3].x, cur[3].y, cur[3].z, cur[3].w}};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             float h[4], l[4];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tc::split_tf32(cv[c][i], h[c], l[c]);
+            for (int c = 0; c < 4; ++c) tc::split_tf32(UP ? cv[i][c] : cv[c][i], h[c], l[c]);
             const uint32_t off = core_off(4 * rq + i, kq);
             *reinterpret_cast<float4 *>(st + off) = make_float4(h[0], h[1], h[2], h[3]);
             *reinterpret_cast<float4 *>(st + kTileBytes + off) = make_float4(l[0], l[1], l[2], l[3]);
@@ -151,12 +170,17 @@ syrk_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
             for (int ks = 0; ks < kKs / 8; ++ks) {
                 const uint32_t ko = ks * 2 * kLbo;
                 const uint32_t acc0 = (s > 0 || ks > 0) ? 1u : 0u;
+                // the cross terms in the order hi_I lo_K, lo_I hi_K in both
+                // storages (the I side is A in the lower, B in the upper), so
+                // both round alike
+                const uint32_t x1a = UP ? a_lo : a_hi, x1b = UP ? b_hi : b_lo;
+                const uint32_t x2a = UP ? a_hi : a_lo, x2b = UP ? b_lo : b_hi;
                 tc::mma_tf32(tmem, tc::smem_desc(a_hi + ko, kLbo, kSbo),
                              tc::smem_desc(b_hi + ko, kLbo, kSbo), idesc, acc0);
-                tc::mma_tf32(tmem, tc::smem_desc(a_hi + ko, kLbo, kSbo),
-                             tc::smem_desc(b_lo + ko, kLbo, kSbo), idesc, 1u);
-                tc::mma_tf32(tmem, tc::smem_desc(a_lo + ko, kLbo, kSbo),
-                             tc::smem_desc(b_hi + ko, kLbo, kSbo), idesc, 1u);
+                tc::mma_tf32(tmem, tc::smem_desc(x1a + ko, kLbo, kSbo),
+                             tc::smem_desc(x1b + ko, kLbo, kSbo), idesc, 1u);
+                tc::mma_tf32(tmem, tc::smem_desc(x2a + ko, kLbo, kSbo),
+                             tc::smem_desc(x2b + ko, kLbo, kSbo), idesc, 1u);
             }
             tc::mma_commit(&mbar[b]);
         }
@@ -170,16 +194,21 @@ syrk_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
 
     // this thread's 64 entries of A22 (its tile row, its column half) are
     // loaded while the last MMAs run
+    // (gr, gc): trailing coordinates of D's row r and column c (lower: the
+    // element (gr, gc) of L; upper: the element (gc, gr)); it lives at
+    // Crow[gc * lda] either way, and is in the lower triangle of L when
+    // gr >= gc (lower) or gc >= gr (upper)
     const int q = warp & 3, h = warp >> 2;
     const int r = 32 * q + lane;  // tile row
-    const int gr = ri + r;        // trailing row
-    const int gcb = rk + 64 * h;  // first trailing column of this half
+    const int gr = tm + r;        // trailing row
+    const int gcb = tn + 64 * h;  // first trailing column of this half
     float *Crow = Ab + c1 + gr + (int64_t)c1 * lda;
+    auto inside = [&](int gc) { return gr < m && gc < m && (UP ? gc >= gr : gr >= gc); };
     float old[32];  // the first two 16-column chunks; the other two follow
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
         const int gc = gcb + j;
-        old[j] = (gr < m && gc < m && gr >= gc) ? Crow[(int64_t)gc * lda] : 0.0f;
+        old[j] = inside(gc) ? Crow[(int64_t)gc * lda] : 0.0f;
     }
 
     // all MMAs issued before the last commit are complete once it arrives; the
@@ -216,7 +245,7 @@ syrk_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int gc = gcb + 32 + j;
-                    old[j] = (gr < m && gc < m && gr >= gc) ? Crow[(int64_t)gc * lda] : 0.0f;
+                    old[j] = inside(gc) ? Crow[(int64_t)gc * lda] : 0.0f;
                 }
             }
 #pragma unroll
@@ -226,8 +255,7 @@ syrk_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int gc = gcb + 32 * half + 16 * c + j;
-                    if (gr < m && gc < m && gr >= gc)
-                        Crow[(int64_t)gc * lda] = old[16 * c + j] - v[j];
+                    if (inside(gc)) Crow[(int64_t)gc * lda] = old[16 * c + j] - v[j];
                 }
             }
         }
@@ -241,30 +269,39 @@ syrk_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     if (warp == 0) tc::tmem_dealloc(tmem, 128);
 }
 
-std::once_flag g_tc_once;
-cudaError_t g_tc_attr = cudaSuccess;
+template <bool UP>
+int launch_u(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
+             cudaStream_t stream)
+{
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(syrk_tc_kernel<UP>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    });
+    if (attr != cudaSuccess) return (int)attr;
+    const int m = n - c0 - kNbTc;
+    const int T = (m + 127) / 128;
+    dim3 grid((unsigned)batch, (unsigned)(T * (T + 1) / 2));
+    syrk_tc_kernel<UP><<<grid, 256, kSmemBytes, stream>>>(A, n, lda, strideA, c0, info);
+    return (int)cudaGetLastError();
+}
 
 }  // namespace
 
 // Returns 0 and launches when the tensor-core path applies (16-byte aligned
 // panels), 1 when the caller must use the FP32 path, or a cudaError_t.
 int launch_syrk_tc(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
-                   cudaStream_t stream)
+                   cudaStream_t stream, bool upper)
 {
     if (((reinterpret_cast<uintptr_t>(A) & 15) != 0) || (lda & 3) || (strideA & 3)) return 1;
-    std::call_once(g_tc_once, [] {
-        g_tc_attr = cudaFuncSetAttribute(syrk_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemBytes);
-    });
-    if (g_tc_attr != cudaSuccess) return (int)g_tc_attr;
-    const int m = n - c0 - kNbTc;
-    const int T = (m + 127) / 128;
-    dim3 grid((unsigned)batch, (unsigned)(T * (T + 1) / 2));
-    syrk_tc_kernel<<<grid, 256, kSmemBytes, stream>>>(A, n, lda, strideA, c0, info);
-    return (int)cudaGetLastError();
+    return upper ? launch_u<true>(A, n, lda, strideA, batch, info, c0, stream)
+                 : launch_u<false>(A, n, lda, strideA, batch, info, c0, stream);
 }
 
-int attrs_syrk_tc(cudaFuncAttributes *fa) { return (int)cudaFuncGetAttributes(fa, syrk_tc_kernel); }
+int attrs_syrk_tc(cudaFuncAttributes *fa)
+{
+    return (int)cudaFuncGetAttributes(fa, syrk_tc_kernel<false>);
+}
 
 }  // namespace bl

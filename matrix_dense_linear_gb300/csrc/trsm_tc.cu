@@ -16,7 +16,8 @@
 // into registers while the previous block is solved), which keeps the block's
 // shared memory at 75 KB: three blocks share an SM. Needs 16-byte aligned
 // panels (the caller falls back to the FP32 kernel otherwise). Every wait is
-// bounded; a block that gives up marks info = -1.
+// bounded; a block that gives up marks info = -1. The upper storage (uplo =
+// 'U') changes only the addresses: a row of L is contiguous there.
 #include <mutex>
 
 #include "bl_common.cuh"
@@ -49,12 +50,13 @@ __device__ __forceinline__ uint32_t core_off(int r, int q)
 }
 
 // Column block j of L11 below its diagonal block, L_{k,j} for k > j, in 4 x 4
-// pieces (rows i..i+3 of columns 4q..4q+3 of the block), row quads fastest so
-// that a warp's 16-byte loads run down one column. A thread owns pieces tid
-// and tid + 128: load() fetches them into registers, stage() splits them into
-// the K-major hi/lo operand tiles.
+// pieces (rows i..i+3 of columns 4q..4q+3 of the block), row quads fastest.
+// A thread owns pieces tid and tid + 128: load() fetches them into registers
+// as four 16-byte loads (down the columns in the lower storage, along the rows
+// in the upper one), stage() splits them into the K-major hi/lo operand tiles.
+template <bool UP>
 struct LtPieces {
-    float4 v[2][4];
+    float4 v[2][4];  // lower storage: [column][4 rows]; upper: [row][4 columns]
     __device__ __forceinline__ void load(const float *L11, int lda, int j, int tid)
     {
         const int nrq = (int)lt_rows(j) / 4;
@@ -63,7 +65,7 @@ struct LtPieces {
             const int b = tid + 128 * u;
             if (b < nrq * 8) {
                 const int rq = b % nrq, q = b / nrq;
-                const float *src = L11 + 32 * (j + 1) + 4 * rq + (int64_t)(32 * j + 4 * q) * lda;
+                const float *src = L11 + lidx<UP>(32 * (j + 1) + 4 * rq, 32 * j + 4 * q, lda);
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
                     v[u][c] = *reinterpret_cast<const float4 *>(src + (int64_t)c * lda);
@@ -82,12 +84,13 @@ struct LtPieces {
                 const float cv[4][4] = {{v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w},
                                         {v[u][1].x, v[u][1].y, v[u][1].z, v[u][1].w},
                                         {v[u][2].x, v[u][2].y, v[u][2].z, v[u][2].w},
-                                        {v[u][3].x, v[u][3].y, v[u][3].z, v[u][3].w}};  // [k][row]
+                                        {v[u][3].x, v[u][3].y, v[u][3].z, v[u][3].w}};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     float h[4], l[4];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) tc::split_tf32(cv[c][i], h[c], l[c]);
+                    for (int c = 0; c < 4; ++c)
+                        tc::split_tf32(UP ? cv[i][c] : cv[c][i], h[c], l[c]);
                     const uint32_t off = core_off(4 * rq + i, q);
                     *reinterpret_cast<float4 *>(hi + off) = make_float4(h[0], h[1], h[2], h[3]);
                     *reinterpret_cast<float4 *>(lo + off) = make_float4(l[0], l[1], l[2], l[3]);
@@ -97,6 +100,7 @@ struct LtPieces {
     }
 };
 
+template <bool UP>
 __global__ void __launch_bounds__(128, 3)
 trsm_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
                int *__restrict__ info)
@@ -112,7 +116,8 @@ trsm_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int R = c0 + 128 + (int)blockIdx.y * 128 + tid;  // this thread's row
     const bool live = R < n;
-    const float *L11 = Ab + c0 + (int64_t)c0 * lda;         // L11(i, k) = L11[i + k*lda]
+    const int64_t xs = UP ? 1 : lda;  // step between the columns of one row
+    const float *L11 = Ab + c0 + (int64_t)c0 * lda;         // L11(i, k) = L11[lidx(i, k)]
     float *Ld = reinterpret_cast<float *>(smem + kOffLd);    // Ld[j*1024 + t*32 + k] = L(32j+k, 32j+t)
     float *rinv = reinterpret_cast<float *>(smem + kOffRinv);
     uint8_t *Lt = smem + kOffLt;
@@ -131,12 +136,12 @@ trsm_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     for (int col = warp; col < 128; col += 4) {
         const int j = col >> 5, t = col & 31;
         for (int k = t + lane; k < 32; k += 32)
-            cp_async4(Ld + j * 1024 + t * 32 + k, L11 + (32 * j + k) + (int64_t)col * lda);
+            cp_async4(Ld + j * 1024 + t * 32 + k, L11 + lidx<UP>(32 * j + k, col, lda));
     }
     cp_async_commit();
 
     // the off-diagonal rows of column block 0
-    LtPieces pc;
+    LtPieces<UP> pc;
     pc.load(L11, lda, 0, tid);
     pc.stage(Lt, 0, tid);
 
@@ -148,14 +153,26 @@ trsm_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
 
     // -A21 rows into tensor memory (two 32-column chunks in flight)
     {
-        const float *g = Ab + R + (int64_t)c0 * lda;
+        const float *g = Ab + (live ? lidx<UP>(R, c0, lda) : 0);  // g[c * xs] = (R, c0 + c)
         float v0[32], v1[32];
 #pragma unroll 1
         for (int h = 0; h < 2; ++h) {
+            if constexpr (UP) {  // the row is contiguous: 16-byte loads
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                v0[c] = live ? -g[(int64_t)(64 * h + c) * lda] : 0.0f;
-                v1[c] = live ? -g[(int64_t)(64 * h + 32 + c) * lda] : 0.0f;
+                for (int c = 0; c < 32; c += 4) {
+                    const float4 a = live ? *reinterpret_cast<const float4 *>(g + 64 * h + c)
+                                          : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    const float4 b = live ? *reinterpret_cast<const float4 *>(g + 64 * h + 32 + c)
+                                          : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    v0[c] = -a.x; v0[c + 1] = -a.y; v0[c + 2] = -a.z; v0[c + 3] = -a.w;
+                    v1[c] = -b.x; v1[c + 1] = -b.y; v1[c + 2] = -b.z; v1[c + 3] = -b.w;
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    v0[c] = live ? -g[(int64_t)(64 * h + c) * xs] : 0.0f;
+                    v1[c] = live ? -g[(int64_t)(64 * h + 32 + c) * xs] : 0.0f;
+                }
             }
             tc::tmem_st32(tlane + 64 * h, v0);
             tc::tmem_st32(tlane + 64 * h + 32, v1);
@@ -202,9 +219,16 @@ trsm_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
             }
         }
         if (live) {
-            float *out = Ab + R + (int64_t)(c0 + 32 * j) * lda;
+            float *out = Ab + lidx<UP>(R, c0 + 32 * j, lda);
+            if constexpr (UP) {
 #pragma unroll
-            for (int t = 0; t < 32; ++t) out[(int64_t)t * lda] = x[t];
+                for (int t = 0; t < 32; t += 4)
+                    *reinterpret_cast<float4 *>(out + t) =
+                        make_float4(x[t], x[t + 1], x[t + 2], x[t + 3]);
+            } else {
+#pragma unroll
+                for (int t = 0; t < 32; ++t) out[(int64_t)t * xs] = x[t];
+            }
         }
         if (j == 3) break;
         // X_j as the A operand (K-major, hi/lo)
@@ -249,19 +273,20 @@ trsm_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     if (tid == 0 && sh_err) info[mat] = -1;
 }
 
+template <bool UP>
 int launch_k(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
              cudaStream_t stream)
 {
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(trsm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    kSmemBytes);
+        attr = cudaFuncSetAttribute(trsm_tc_kernel<UP>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     });
     if (attr != cudaSuccess) return (int)attr;
     const int m = n - c0 - 128;
     dim3 grid((unsigned)batch, (unsigned)((m + 127) / 128));
-    trsm_tc_kernel<<<grid, 128, kSmemBytes, stream>>>(A, n, lda, strideA, c0, info);
+    trsm_tc_kernel<UP><<<grid, 128, kSmemBytes, stream>>>(A, n, lda, strideA, c0, info);
     return (int)cudaGetLastError();
 }
 
@@ -270,10 +295,11 @@ int launch_k(float *A, int n, int lda, int64_t strideA, int batch, int *info, in
 // Returns 0 after launching, 1 when the caller must use the FP32 kernel
 // (unaligned panels), or a cudaError_t.
 int launch_trsm_tc(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
-                   cudaStream_t stream)
+                   cudaStream_t stream, bool upper)
 {
     if (((reinterpret_cast<uintptr_t>(A) & 15) != 0) || (lda & 3) || (strideA & 3)) return 1;
-    return launch_k(A, n, lda, strideA, batch, info, c0, stream);
+    return upper ? launch_k<true>(A, n, lda, strideA, batch, info, c0, stream)
+                 : launch_k<false>(A, n, lda, strideA, batch, info, c0, stream);
 }
 
 }  // namespace bl

@@ -139,7 +139,7 @@ def test_upper_misaligned_base():
 @pytest.mark.parametrize("n,batch", [(48, 2000), (64, 1000), (32, 4096)])
 def test_upper_large_batch_sampled(n, batch):
     """The batch sizes that take the one-warp kernel at n = 33 .. 64 (above
-    six blocks per SM) and the 4-per-warp packing at n <= 32."""
+    four two-warp blocks per SM) and four-warp blocks at n <= 32."""
     mats = _mats(n, 64, 960 + n)
     buf = _pack_upper([mats[b % 64] for b in range(batch)], n, n, n * n)
     out, info = _factor(buf, n, n, n * n, batch)
@@ -166,11 +166,11 @@ def test_upper_info(n):
 
 
 @pytest.mark.parametrize("n,route,lda", [(20, WARP, 20), (48, WARP, 48), (64, WARP, 64),
-                                         (100, CTA, 100), (128, CTA, 128), (200, BLOCKED, 203)])
+                                         (100, CTA, 100), (128, CTA, 128), (200, BLOCKED, 203),
+                                         (200, BLOCKED, 200), (384, BLOCKED, 388)])
 def test_upper_is_the_lower_transposed_bit_for_bit(n, route, lda):
-    """Same kernels, transposed addresses: U = L^T exactly. (n > 128 with an
-    lda that is not a multiple of 4, so the lower path takes the same FP32
-    panel kernels as the upper one.)"""
+    """Same kernels, transposed addresses: U = L^T exactly, on the FP32 panel
+    kernels (lda not a multiple of 4) and on the tensor-core ones."""
     batch = 9
     mats = _mats(n, batch, 990 + n)
     up = _pack_upper(mats, n, lda, lda * n)
