@@ -27,9 +27,7 @@
 namespace bl {
 namespace {
 
-// Up to four warps (four matrices, or four groups of them) per block; the
-// launcher picks 1 or 4 (warps_per_block).
-constexpr int kMaxWarpsPerBlock = 4;
+constexpr int kWarpsPerBlock = 1;  // one warp per block: blocks spread evenly over the SMs
 
 // Row `row` of L, entries k0 .. k0+K-1: r[k] = l(row, k0 + k) where
 // k0 + k <= row and `live`; other entries keep their values. Lower storage:
@@ -94,18 +92,18 @@ __device__ __forceinline__ bool vec_ok(const float *A, int lda, int64_t strideA)
 }
 
 template <int N, bool UP>
-__global__ void __launch_bounds__(32 * kMaxWarpsPerBlock)
+__global__ void __launch_bounds__(32 * kWarpsPerBlock)
 potrf_warp_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int batch,
                   int *__restrict__ info)
 {
     constexpr int G = 32 / N;  // matrices per warp
-    __shared__ __align__(16) float colbuf[kMaxWarpsPerBlock][2][32];
+    __shared__ __align__(16) float colbuf[kWarpsPerBlock][2][32];
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int grp = lane / N;
     const int row = lane - grp * N;
-    const int64_t mat = ((int64_t)blockIdx.x * (blockDim.x >> 5) + warp) * G + grp;
+    const int64_t mat = ((int64_t)blockIdx.x * kWarpsPerBlock + warp) * G + grp;
     const bool valid = mat < batch;
     const bool live = valid && row < n;
     float *__restrict__ Ab = A + (valid ? mat * strideA : 0);
@@ -163,23 +161,23 @@ potrf_warp_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int ba
 // the diagonal's square root are taken once at the end from each lane's own
 // pivot (info by a warp ballot: the lowest failing row).
 template <bool UP>
-__global__ void __launch_bounds__(32 * kMaxWarpsPerBlock)
+__global__ void __launch_bounds__(32 * kWarpsPerBlock)
 potrf_warp64_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int batch,
                     int *__restrict__ info)
 {
-    __shared__ __align__(16) float colbuf[kMaxWarpsPerBlock][2][64];
+    __shared__ __align__(16) float colbuf[kWarpsPerBlock][2][64];
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int64_t mat = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp;
+    const int64_t mat = (int64_t)blockIdx.x * kWarpsPerBlock + warp;
     const bool valid = mat < batch;
     const int rowa = lane, rowb = lane + 32;
     const bool livea = valid && rowa < n, liveb = valid && rowb < n;
     float *__restrict__ Ab = A + (valid ? mat * strideA : 0);
     // No early trigger here: the next launch's warps would take the free slots
     // of this one's SMs (up to three warps per sub-partition at 153 registers)
-    // and then start unevenly (1024 matrices: 14.4 against 12.2 us in a chain
-    // of launches); the implicit trigger at exit keeps them out.
+    // and then start unevenly (1024 matrices: 14.4 against 11.9 us a call in a
+    // chain of launches); the implicit trigger at exit keeps them out.
     pdl_wait();
 
     const bool vec = UP && vec_ok(A, lda, strideA);
@@ -229,7 +227,7 @@ potrf_warp64_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int 
 
     // lda made opaque before the stores: otherwise the compiler keeps the load
     // addresses alive across the whole factorization to reuse them here
-    // (n = 64: 211 against 153 registers a thread; two warps: 133 against 111)
+    // (n = 64: 211 against 153 registers a thread; two warps: 133 against 114)
     asm volatile("" : "+r"(lda));
     store_row<UP>(ra, Ab, rowa, 0, lda, livea, vec);
     store_row<UP>(rb, Ab, rowb, 0, lda, liveb, vec);
@@ -383,25 +381,14 @@ int sm_count()
     return sms;
 }
 
-// Warps per block of the warp-per-matrix kernels. A warp runs on SM
-// sub-partition (its index in the block) mod 4, so blocks of four warps put
-// one warp on each; with single-warp blocks the block scheduler stacked three
-// warps on some sub-partitions while others held one (1024 matrices of order
-// 64: 14.4 against 10.9 us). Batches below four warps per SM keep one warp per
-// block so that every SM gets work.
-int warps_per_block(int64_t warps)
-{
-    return warps >= 4 * (int64_t)sm_count() ? 4 : 1;
-}
-
 template <int N, bool UP>
 int launch_n(float *A, int n, int lda, int64_t strideA, int batch, int *info, cudaStream_t st)
 {
     constexpr int G = 32 / N;
-    const int wpb = warps_per_block((batch + G - 1) / G);
-    const int64_t per_block = (int64_t)wpb * G;
+    const int64_t per_block = (int64_t)kWarpsPerBlock * G;
     const int64_t blocks = (batch + per_block - 1) / per_block;
-    return launch_pdl(potrf_warp_kernel<N, UP>, dim3((unsigned)blocks), dim3(32 * wpb), 0,
+    return launch_pdl(potrf_warp_kernel<N, UP>, dim3((unsigned)blocks),
+                      dim3(32 * kWarpsPerBlock), 0,
                       st, A, n, lda, strideA, batch, info);
 }
 
@@ -419,9 +406,8 @@ int launch_64(float *A, int n, int lda, int64_t strideA, int batch, int *info, c
     if ((int64_t)batch <= (int64_t)kX2BlocksPerSm * sm_count())
         return launch_pdl(potrf_warp64x2_kernel<UP>, dim3((unsigned)batch), dim3(64), 0, st, A,
                           n, lda, strideA, batch, info);
-    const int wpb = warps_per_block(batch);
-    const int64_t blocks = (batch + wpb - 1) / wpb;
-    return launch_pdl(potrf_warp64_kernel<UP>, dim3((unsigned)blocks), dim3(32 * wpb), 0,
+    const int64_t blocks = (batch + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    return launch_pdl(potrf_warp64_kernel<UP>, dim3((unsigned)blocks), dim3(32 * kWarpsPerBlock), 0,
                       st, A, n, lda, strideA, batch, info);
 }
 
@@ -451,7 +437,7 @@ int attrs_warp(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem)
     else if (n <= 16) e = cudaFuncGetAttributes(fa, potrf_warp_kernel<16, false>);
     else if (n <= 32) e = cudaFuncGetAttributes(fa, potrf_warp_kernel<32, false>);
     else e = cudaFuncGetAttributes(fa, potrf_warp64_kernel<false>);  // the large-batch kernel
-    *threads = 32 * kMaxWarpsPerBlock;
+    *threads = 32 * kWarpsPerBlock;
     *dyn_smem = 0;
     return (int)e;
 }
