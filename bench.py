@@ -42,8 +42,11 @@ REPLICA_CAP_BYTES = 96 << 30
 # changed source reports null. Filled from the summaries under profiles/.
 TRAFFIC = {
     # workload: (source files, sha256 prefix over them, bytes per launch, summary file)
+    "n32": (("matrix_dense_linear_gb300/csrc/potrf_warp.cu",
+             "matrix_dense_linear_gb300/csrc/bl_common.cuh"), "b38f11e904fd317b", 4219904,
+            "profiles/potrf_warp_n32_b1024.md"),
     "n64": (("matrix_dense_linear_gb300/csrc/potrf_warp.cu",
-             "matrix_dense_linear_gb300/csrc/bl_common.cuh"), "ac9c7df2e63d7be8", 12661248,
+             "matrix_dense_linear_gb300/csrc/bl_common.cuh"), "b38f11e904fd317b", 12660224,
             "profiles/potrf_warp64_n64_b1024.md"),
 }
 
