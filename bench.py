@@ -359,6 +359,24 @@ def roofline_entry(name: str, n: int, batch: int, ms_per_call: float, pk: dict, 
             "unit": "TFLOP/s", "frac": (flops / t / 1e12) / fp32_peak, "roof_ms": t_alu * 1e3}
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest x over the ranks of the default process group (the slowest
+    rank's time); x itself when running alone."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, batch: int, steps: int, ms: float) -> float:
+    """Whole-job matrices/s: every rank factors `batch` matrices per step (weak
+    scaling), timed as the max over ranks of `steps` steps."""
+    return world * batch * steps / (ms / 1e3)
+
+
 def run_ours(args, rank: int, world: int, barrier) -> dict | None:
     import torch
 
@@ -387,12 +405,7 @@ def run_ours(args, rank: int, world: int, barrier) -> dict | None:
     t_s1 = time.time()
     if sampler:
         sampler.stop()
-    # max over ranks
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
 
     # check this run's output on its last replica (info only; parity is the tests')
     info = w.info.cpu().numpy()
@@ -400,15 +413,11 @@ def run_ours(args, rank: int, world: int, barrier) -> dict | None:
 
     lat_us = single_call_us(w) if rank == 0 else None
     e2e = e2e_steps(w, args.steps, min(args.warmup, 3), barrier)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e["ms"]], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e["ms"] = float(t.item())
+    e2e["ms"] = max_over_ranks(e2e["ms"], world, dev)
 
     n, batch = bt.n, bt.batch
     per_call = ms / args.steps
-    value = world * batch * args.steps / (ms / 1e3)
+    value = job_rate(world, batch, args.steps, ms)
     rf = roofline_entry(args.workload, n, batch, per_call, pk, sms)
     nl = launches_per_call(n)
     roof = {"bound": rf["bound"], "achieved": rf["achieved"], "peak": rf["peak"],
@@ -436,7 +445,7 @@ def run_ours(args, rank: int, world: int, barrier) -> dict | None:
                    "timing": "CUDA events around the replay of a CUDA graph of the K calls",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roof,
-        "e2e": {"value": world * batch * args.steps / (e2e["ms"] / 1e3), "unit": UNIT,
+        "e2e": {"value": job_rate(world, batch, args.steps, e2e["ms"]), "unit": UNIT,
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "ms_per_step": e2e["ms"] / args.steps},
         "gpu_launches": nl * args.steps,
