@@ -70,17 +70,17 @@ __device__ __forceinline__ int64_t lidx(int i, int k, int lda)
     return UP ? (int64_t)k + (int64_t)i * lda : (int64_t)i + (int64_t)k * lda;
 }
 
+// Programmatic dependent launch. Kernels launched with launch_pdl may start
+// while the previous kernel in the stream is still running; they call
+// pdl_wait() before their first access to global memory (it returns once the
+// previous grid has completed and its writes are visible) and pdl_trigger()
+// to let the next kernel start launching early.
 // Named barrier 1..15 over nthreads threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// Programmatic dependent launch. Kernels launched with launch_pdl may start
-// while the previous kernel in the stream is still running; they call
-// pdl_wait() before their first access to global memory (it returns once the
-// previous grid has completed and its writes are visible) and pdl_trigger()
-// to let the next kernel start launching early.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger()
 {
