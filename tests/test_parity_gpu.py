@@ -212,6 +212,80 @@ def test_nondefault_stream():
     compare(bt, out, info, what="stream")
 
 
+@pytest.mark.parametrize("n,batch", [(32, 300), (64, 1000), (128, 50), (300, 6)])
+def test_cuda_graph_capture_replays_the_same_bits(n, batch):
+    """The call is stream-ordered and allocates nothing, so it can be captured
+    into a CUDA graph; a replay gives the eager call's bits."""
+    import torch
+
+    import matrix_dense_linear_gb300 as bl
+    bt = _gram_batch(n, batch, 820 + n, fill="nan")
+    src = torch.from_numpy(bt.buf.copy()).cuda()
+    eager, work = src.clone(), src.clone()
+    info_e = torch.full((batch,), -7, dtype=torch.int32, device="cuda")
+    info_g = torch.full((batch,), -7, dtype=torch.int32, device="cuda")
+    bl.factor(eager, n, bt.lda, bt.strideA, batch, info_e)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        bl.factor(work, n, bt.lda, bt.strideA, batch, info_g, stream=torch.cuda.current_stream())
+    for _ in range(2):  # replays start from the pristine input
+        work.copy_(src)
+        info_g.fill_(-7)
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(info_e, info_g) and not info_e.any()
+    assert torch.equal(eager.view(torch.int32), work.view(torch.int32))
+
+
+def test_concurrent_calls_from_host_threads():
+    """Reentrant and safe across streams: four host threads, each with its own
+    stream and buffers, factor at the same time; every result equals the one
+    factored alone."""
+    import threading
+
+    import torch
+
+    import matrix_dense_linear_gb300 as bl
+    cases = [(20, 500), (64, 700), (100, 40), (256, 5)]
+    bts = [_gram_batch(n, b, 840 + n, fill="nan") for n, b in cases]
+    srcs = [torch.from_numpy(bt.buf.copy()).cuda() for bt in bts]
+    alone = []
+    for bt, src in zip(bts, srcs):
+        a = src.clone()
+        info = torch.empty(bt.batch, dtype=torch.int32, device="cuda")
+        bl.factor(a, bt.n, bt.lda, bt.strideA, bt.batch, info)
+        alone.append((a, info))
+    torch.cuda.synchronize()
+    outs = [src.clone() for src in srcs]
+    infos = [torch.full((bt.batch,), -7, dtype=torch.int32, device="cuda") for bt in bts]
+    errors = []
+
+    def work(t):
+        try:
+            st = torch.cuda.Stream()
+            bt = bts[t]
+            for _ in range(3):
+                with torch.cuda.stream(st):
+                    outs[t].copy_(srcs[t])
+                    bl.factor(outs[t], bt.n, bt.lda, bt.strideA, bt.batch, infos[t], stream=st)
+            st.synchronize()
+        except Exception as e:  # noqa: BLE001
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(t,)) for t in range(len(bts))]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    torch.cuda.synchronize()
+    for (a, info), o, i in zip(alone, outs, infos):
+        assert torch.equal(info, i)
+        assert torch.equal(a.view(torch.int32), o.view(torch.int32))
+
+
 @pytest.mark.parametrize("route,n", [(1, 8), (1, 16), (1, 32), (1, 64), (2, 32), (2, 64),
                                      (2, 96), (2, 128), (3, 256), (4, 100), (4, 128)])
 def test_kernels_use_no_local_memory(route, n):
