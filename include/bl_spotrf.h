@@ -137,6 +137,13 @@ int bl_spotrf_kernel_info(int route, int n, int *regs, int *local_bytes, int *st
  *                      synchronize: the results are on the host once every
  *                      stream is done.
  *
+ * For n <= 128 with page-locked host buffers that the device maps (memory
+ * from cudaHostAlloc / cudaMallocHost / cudaHostRegister, e.g. a pinned torch
+ * tensor) there are no copies: the one kernel of those orders reads each
+ * lower-triangle element from host memory and writes its result back there,
+ * on streams[0] (A_dev and info_dev are not touched). Other buffers take the
+ * copy path above.
+ *
  * Returns what bl_spotrf_batched returns (argument indices as there, with the
  * device buffers checked as A and info; -11 when streams is NULL or nstreams
  * < 1), or the cudaError_t of a failed copy.

@@ -198,14 +198,16 @@ def factor(A, n: int, lda: int, strideA: int, batch: int, info, stream=None,
 
 
 def factor_host(A_host, n: int, lda: int, strideA: int, batch: int, info_host,
-                A_dev=None, info_dev=None, streams=None, chunks: int = 0) -> None:
+                A_dev=None, info_dev=None, streams=None, chunks: int = 0,
+                synchronize: bool = True) -> None:
     """Factor a batch that lives in (pinned) host memory through
     bl_spotrf_batched_host: slices of the batch go host -> device, are factored
     and come back, one stream per slice, so copies and factorization overlap.
     The device buffers are the caller's if given, else allocated by torch; the
     streams are the caller's (torch streams) or two made here (two slices
-    measured best for the 16.8 MB n = 64 batch on GB300). Waits for all
-    streams before returning."""
+    measured best for the 16.8 MB n = 64 batch on GB300). The current stream
+    waits for all of them; with `synchronize` the host waits too (else the
+    results are on the host once the current stream's work is done)."""
     import torch
     if A_dev is None:
         A_dev = torch.empty_like(A_host, device="cuda")
@@ -224,4 +226,5 @@ def factor_host(A_host, n: int, lda: int, strideA: int, batch: int, info_host,
         raise BLError(code, "host")
     for s in streams:
         cur.wait_stream(s)
-    cur.synchronize()
+    if synchronize:
+        cur.synchronize()

@@ -62,7 +62,7 @@ bool route_can_run(int route, int n, bool upper)
 }
 
 int run(float *A, int n, int lda, int64_t strideA, int batch, int *info, cudaStream_t stream,
-        int route, bool upper = false)
+        int route, bool upper = false, bool host_mapped = false)
 {
     int e = check_args(A, n, lda, strideA, batch, info);
     if (e) return e;
@@ -76,11 +76,27 @@ int run(float *A, int n, int lda, int64_t strideA, int batch, int *info, cudaStr
     switch (route) {
     case BL_ROUTE_WARP: return bl::launch_warp(A, n, lda, strideA, batch, info, stream, upper);
     case BL_ROUTE_CTA:
-        return bl::launch_cta(A, n, lda, strideA, batch, info, stream, bl::InfoMode{-1}, upper);
+        return bl::launch_cta(A, n, lda, strideA, batch, info, stream, bl::InfoMode{-1}, upper,
+                              host_mapped);
     case BL_ROUTE_TMEM:
         return bl::launch_tmem(A, n, lda, strideA, batch, info, stream, bl::InfoMode{-1});
     default: return bl::launch_blocked(A, n, lda, strideA, batch, info, stream, upper);
     }
+}
+
+// The device address of a page-locked host allocation the device maps (with
+// unified addressing every cudaHostAlloc / cudaHostRegister allocation is),
+// else nullptr (pageable memory, device memory, or no information).
+template <typename T>
+T *mapped_host(T *p)
+{
+    cudaPointerAttributes at{};
+    if (p == nullptr || cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();  // clear a failed query
+        return nullptr;
+    }
+    if (at.type != cudaMemoryTypeHost || at.devicePointer == nullptr) return nullptr;
+    return static_cast<T *>(at.devicePointer);
 }
 
 // uplo argument: 0 lower, 1 upper, -1 invalid
@@ -125,6 +141,17 @@ int bl_spotrf_batched_host(float *A_host, int n, int lda, int64_t strideA, int b
     if (batch > 0 && info_host == nullptr) return -6;
     if (streams == nullptr || nstreams < 1) return -11;
     if (batch == 0) return 0;
+    // Page-locked host buffers of a one-kernel order (n <= 128): the kernel
+    // reads and writes them in place over the host link (lower triangles only,
+    // each element once each way), with no staging copies; on GB300 the
+    // NVLink-C2C link carries that at about 1.5 times the rate of the copy
+    // engines (1024 matrices of order 64: 137 against 207 us).
+    if (n <= kCtaMaxN) {
+        float *Am = mapped_host(A_host);
+        int *im = mapped_host(info_host);
+        if (Am && im)
+            return run(Am, n, lda, strideA, batch, im, streams[0], BL_ROUTE_AUTO, false, true);
+    }
     const int64_t span = (int64_t)lda * n;  // floats of one matrix
     if (chunks <= 0) chunks = nstreams;
     if (chunks > batch) chunks = batch;

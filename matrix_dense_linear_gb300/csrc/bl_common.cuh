@@ -118,8 +118,9 @@ struct InfoMode {
 // `upper`: the factor is stored in the upper triangle (uplo = 'U', see lidx).
 int launch_warp(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                 cudaStream_t stream, bool upper);
+// no_bulk: A may be host memory the device maps (no bulk copies then)
 int launch_cta(float *A, int n, int lda, int64_t strideA, int batch, int *info,
-               cudaStream_t stream, InfoMode mode, bool upper);
+               cudaStream_t stream, InfoMode mode, bool upper, bool no_bulk = false);
 int launch_tmem(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                 cudaStream_t stream, InfoMode mode);
 int launch_blocked(float *A, int n, int lda, int64_t strideA, int batch, int *info,

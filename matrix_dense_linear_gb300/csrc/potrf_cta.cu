@@ -322,12 +322,12 @@ int launch_v(float *A, int n, int lda, int64_t strideA, int batch, int *info, cu
 
 template <int NB, int NT>
 int launch_nb(float *A, int n, int lda, int64_t strideA, int batch, int *info, cudaStream_t st,
-              int info_off, bool upper)
+              int info_off, bool upper, bool no_bulk)
 {
     if (upper) return launch_v<NB, NT, false, true>(A, n, lda, strideA, batch, info, st, info_off);
     const bool vec = ((reinterpret_cast<uintptr_t>(A) & 15) == 0) && ((lda & 3) == 0) &&
                      ((strideA & 3) == 0);
-    if (vec && n == CtaGeom<NB>::NP)
+    if (vec && n == CtaGeom<NB>::NP && !no_bulk)
         return launch_v<NB, NT, true, false>(A, n, lda, strideA, batch, info, st, info_off);
     return launch_v<NB, NT, false, false>(A, n, lda, strideA, batch, info, st, info_off);
 }
@@ -344,13 +344,14 @@ int attrs_nb(cudaFuncAttributes *fa, int *threads, int *dyn)
 }  // namespace
 
 int launch_cta(float *A, int n, int lda, int64_t strideA, int batch, int *info,
-               cudaStream_t stream, InfoMode mode, bool upper)
+               cudaStream_t stream, InfoMode mode, bool upper, bool no_bulk)
 {
     const int o = mode.off;
-    if (n <= 32) return launch_nb<1, 32>(A, n, lda, strideA, batch, info, stream, o, upper);
-    if (n <= 64) return launch_nb<2, 64>(A, n, lda, strideA, batch, info, stream, o, upper);
-    if (n <= 96) return launch_nb<3, 128>(A, n, lda, strideA, batch, info, stream, o, upper);
-    return launch_nb<4, 128>(A, n, lda, strideA, batch, info, stream, o, upper);
+    const bool nb = no_bulk;
+    if (n <= 32) return launch_nb<1, 32>(A, n, lda, strideA, batch, info, stream, o, upper, nb);
+    if (n <= 64) return launch_nb<2, 64>(A, n, lda, strideA, batch, info, stream, o, upper, nb);
+    if (n <= 96) return launch_nb<3, 128>(A, n, lda, strideA, batch, info, stream, o, upper, nb);
+    return launch_nb<4, 128>(A, n, lda, strideA, batch, info, stream, o, upper, nb);
 }
 
 int attrs_cta(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem)

@@ -192,6 +192,31 @@ def test_host_buffer_call(n, batch, chunks):
     assert_untouched(out, bt.buf, bt, what=f"host n={n}")
 
 
+@pytest.mark.parametrize("n,batch", [(20, 100), (64, 1000), (100, 30), (128, 40)])
+def test_host_call_pinned_and_pageable_agree(n, batch):
+    """Pinned host buffers of n <= 128 are factored in place by the kernel over
+    the host link; pageable ones take the copy path. Both give the bits of
+    the device call."""
+    import torch
+
+    import matrix_dense_linear_gb300 as bl
+    bt = _gram_batch(n, batch, 860 + n, fill="nan")
+    dev = torch.from_numpy(bt.buf.copy()).cuda()
+    info_d = torch.empty(batch, dtype=torch.int32, device="cuda")
+    bl.factor(dev, n, bt.lda, bt.strideA, batch, info_d)
+    want = dev.cpu().numpy()
+    for pinned in (True, False):
+        host = torch.from_numpy(bt.buf.copy())
+        info_h = torch.full((batch,), -7, dtype=torch.int32)
+        if pinned:
+            host, info_h = host.pin_memory(), info_h.pin_memory()
+        bl.factor_host(host, n, bt.lda, bt.strideA, batch, info_h)
+        assert np.array_equal(info_h.numpy(), info_d.cpu().numpy()), pinned
+        assert np.array_equal(host.numpy().view(np.uint32), want.view(np.uint32)), pinned
+    compare(bt, want, info_d.cpu().numpy(), indices=list(range(min(batch, 40))),
+            what=f"host n={n}")
+
+
 def test_n_zero_and_batch_zero():
     import torch
 
