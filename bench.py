@@ -615,6 +615,76 @@ def run_shapes(args) -> list:
     return rows
 
 
+# FP64 peak of one GB300: NVIDIA's nominal figure (an FMA-throughput probe
+# on the GB300s measured 1.06 TFLOP/s); FP64 is not in the measured peaks
+FP64_PEAK_TFLOPS = 1.25
+
+
+def run_shapes_f64(args) -> list:
+    """--shapes with --dtype f64: the double-precision factorization (DPOTRF)
+    on A = G G^T / n + I in float64 (64 distinct matrices repeated), the same
+    timing as run_shapes, against the FP64 roofline."""
+    import torch
+
+    import matrix_dense_linear_gb300 as bl
+    import synth
+    bl.library()
+    dev = torch.device("cuda", 0)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    rows = []
+    for spec in args.shapes.split(","):
+        n, batch = (int(x) for x in spec.lower().split("x"))
+        distinct = min(batch, 64)
+        mats = [synth.gram(n, synth.rng(6, b), "normal", float(n), 1.0) for b in range(distinct)]
+        one = np.concatenate([np.asfortranarray(m).ravel(order="F") for m in mats])
+        buf = np.tile(one, -(-batch // distinct))[: batch * n * n]
+        src = torch.from_numpy(np.ascontiguousarray(buf)).to(dev)
+        nbytes = src.numel() * 8
+        nrep = int(max(1, min(max(args.steps, -(-2 * l2 // nbytes)),
+                              REPLICA_CAP_BYTES // max(nbytes, 1))))
+        reps = torch.empty((nrep, src.numel()), dtype=torch.float64, device=dev)
+        info = torch.zeros(batch, dtype=torch.int32, device=dev)
+        st = torch.cuda.current_stream()
+        for i in range(min(args.warmup, nrep)):
+            reps[i].copy_(src)
+            bl.factor_double(reps[i], n, n, n * n, batch, info, st, uplo=args.uplo)
+        torch.cuda.synchronize()
+        k = min(args.steps, nrep)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(k):
+                bl.factor_double(reps[i], n, n, n * n, batch, info,
+                                 torch.cuda.current_stream(), uplo=args.uplo)
+        ts = []
+        for _ in range(3):
+            for i in range(k):
+                reps[i].copy_(src)
+            flush.fill_(1.0)
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            g.replay()
+            e1.record(st)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) / k)
+        assert not info.cpu().numpy().any()
+        ms = statistics.median(ts)
+        tflops = flops_per_matrix(n) * batch / (ms / 1e3) / 1e12
+        row = {"shape": spec, "dtype": "f64", "uplo": args.uplo, "n": n, "batch": batch,
+               "ms_per_call": ms, "us_per_call": ms * 1e3, "matrices_per_s": batch / (ms / 1e3),
+               "tflops": tflops,
+               "roofline": {"bound": "alu", "peak": FP64_PEAK_TFLOPS, "unit": "TFLOP/s",
+                            "frac": tflops / FP64_PEAK_TFLOPS, "peak_source": "nominal"},
+               "calls_timed": k}
+        print(json.dumps(row), flush=True)
+        rows.append(row)
+        del reps, g
+        torch.cuda.empty_cache()
+    return rows
+
+
 def run_potrs(args) -> dict:
     """Batched SPOTRS (solve with the factor) on a workload's factors: the
     batch is factored once on the device, then each timed step solves nrhs
@@ -754,6 +824,8 @@ def main():
     ap.add_argument("--shapes", default=None, metavar="NxB,...",
                     help="time these (n, batch) shapes (one JSON line each); 'pages' = "
                          "the shapes the pages quote timings for")
+    ap.add_argument("--dtype", choices=["f32", "f64"], default="f32",
+                    help="f64: time the double-precision factorization for --shapes")
     ap.add_argument("--uplo", choices=["L", "U"], default="L",
                     help="storage of the factor for --shapes (U: upper triangle)")
     args = ap.parse_args()
@@ -769,7 +841,10 @@ def main():
     if args.shapes:
         if args.shapes == "pages":
             args.shapes = PAGES_SHAPES
-        run_shapes(args)
+        if args.dtype == "f64":
+            run_shapes_f64(args)
+        else:
+            run_shapes(args)
         return
     if args.op == "potrs":
         print(json.dumps(run_potrs(args)), flush=True)

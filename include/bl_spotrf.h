@@ -227,6 +227,20 @@ int bl_sposv_batched_uplo(char uplo, float *A, int n, int lda, int64_t strideA, 
                           int nrhs, int ldb, int64_t strideB, int batch, int *info,
                           cudaStream_t stream);
 
+/*
+ * bl_dpotrf_batched / bl_dpotrf_batched_uplo - the same factorization for a
+ * double-precision batch (DPOTRF): A is double*, everything else (layout,
+ * lda and strideA in elements, the triangle read and written, info, quick
+ * returns, argument indices and their order, stream ordering, ownership) as
+ * bl_spotrf_batched and bl_spotrf_batched_uplo. IEEE double arithmetic with
+ * FMA contraction, IEEE square root and division. On GB300 the FP64 rate is
+ * about 1/66 of the FP32 rate, so these calls are bound by their n^3/3 flops.
+ */
+int bl_dpotrf_batched(double *A, int n, int lda, int64_t strideA, int batch, int *info,
+                      cudaStream_t stream);
+int bl_dpotrf_batched_uplo(char uplo, double *A, int n, int lda, int64_t strideA, int batch,
+                           int *info, cudaStream_t stream);
+
 /* Version string of the library ("bl_spotrf <major>.<minor> sm_103a"). */
 const char *bl_spotrf_version(void);
 

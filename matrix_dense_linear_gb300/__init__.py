@@ -36,6 +36,8 @@ SYMBOLS = {
     "bl_spotrs_batched": (_I, [_VP, _I, _I, _I64, _VP, _I, _I, _I64, _I, _VP]),
     "bl_sposv_batched": (_I, [_VP, _I, _I, _I64, _VP, _I, _I, _I64, _I, _VP, _VP]),
     "bl_spotrf_batched_uplo": (_I, [_C, _VP, _I, _I, _I64, _I, _VP, _VP]),
+    "bl_dpotrf_batched": (_I, [_VP, _I, _I, _I64, _I, _VP, _VP]),
+    "bl_dpotrf_batched_uplo": (_I, [_C, _VP, _I, _I, _I64, _I, _VP, _VP]),
     "bl_spotrf_batched_uplo_ex": (_I, [_C, _VP, _I, _I, _I64, _I, _VP, _VP, _I]),
     "bl_spotrs_batched_uplo": (_I, [_C, _VP, _I, _I, _I64, _VP, _I, _I, _I64, _I, _VP]),
     "bl_sposv_batched_uplo": (_I, [_C, _VP, _I, _I, _I64, _VP, _I, _I, _I64, _I, _VP, _VP]),
@@ -127,6 +129,24 @@ def sposv_batched_uplo(uplo, A, n: int, lda: int, strideA: int, B, nrhs: int, ld
     """bl_sposv_batched_uplo: factor (upper or lower storage) and solve."""
     return library().bl_sposv_batched_uplo(_uplo(uplo), _ptr(A), n, lda, strideA, _ptr(B), nrhs,
                                            ldb, strideB, batch, _ptr(info), _stream(stream))
+
+
+def dpotrf_batched(A, n: int, lda: int, strideA: int, batch: int, info, stream=None,
+                   uplo="L") -> int:
+    """bl_dpotrf_batched(_uplo): A is a float64 device tensor (or pointer)."""
+    if uplo in ("L", b"L"):
+        return library().bl_dpotrf_batched(_ptr(A), n, lda, strideA, batch, _ptr(info),
+                                           _stream(stream))
+    return library().bl_dpotrf_batched_uplo(_uplo(uplo), _ptr(A), n, lda, strideA, batch,
+                                            _ptr(info), _stream(stream))
+
+
+def factor_double(A, n: int, lda: int, strideA: int, batch: int, info, stream=None,
+                  uplo="L") -> None:
+    """dpotrf_batched, raising BLError on a nonzero status."""
+    code = dpotrf_batched(A, n, lda, strideA, batch, info, stream, uplo)
+    if code:
+        raise BLError(code, "dpotrf")
 
 
 def route(n: int, batch: int) -> int:

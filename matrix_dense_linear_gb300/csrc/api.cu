@@ -31,7 +31,7 @@ bool trace_enabled()
     return on;
 }
 
-int check_args(const float *A, int n, int lda, int64_t strideA, int batch, const int *info)
+int check_args(const void *A, int n, int lda, int64_t strideA, int batch, const int *info)
 {
     if (n < 0) return -2;
     if (batch < 0) return -5;
@@ -255,6 +255,28 @@ int bl_spotrf_batched_uplo(char uplo, float *A, int n, int lda, int64_t strideA,
     const int u = parse_uplo(uplo);
     if (u < 0) return -1;
     return shift_arg(run(A, n, lda, strideA, batch, info, stream, BL_ROUTE_AUTO, u == 1));
+}
+
+int bl_dpotrf_batched_uplo(char uplo, double *A, int n, int lda, int64_t strideA, int batch,
+                           int *info, cudaStream_t stream)
+{
+    const int u = parse_uplo(uplo);
+    if (u < 0) return -1;
+    const int e = check_args(A, n, lda, strideA, batch, info);
+    if (e) return shift_arg(e);
+    if (batch == 0) return 0;
+    if (n == 0) return (int)cudaMemsetAsync(info, 0, sizeof(int) * (size_t)batch, stream);
+    if (trace_enabled())
+        std::fprintf(stderr, "bl_dpotrf: uplo=%c n=%d lda=%d strideA=%lld batch=%d\n",
+                     u ? 'U' : 'L', n, lda, (long long)strideA, batch);
+    return bl::launch_dpotrf(A, n, lda, strideA, batch, info, stream, u == 1);
+}
+
+int bl_dpotrf_batched(double *A, int n, int lda, int64_t strideA, int batch, int *info,
+                      cudaStream_t stream)
+{
+    const int e = bl_dpotrf_batched_uplo('L', A, n, lda, strideA, batch, info, stream);
+    return e < 0 ? e + 1 : e;  // argument indices without the uplo argument
 }
 
 int bl_spotrf_batched_uplo_ex(char uplo, float *A, int n, int lda, int64_t strideA, int batch,
