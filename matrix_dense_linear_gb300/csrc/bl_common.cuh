@@ -129,8 +129,9 @@ int launch_blocked(float *A, int n, int lda, int64_t strideA, int batch, int *in
 int launch_syrk_tc(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
                    cudaStream_t stream, bool upper);
 int attrs_syrk_tc(cudaFuncAttributes *fa);
+// fused: also A22 -= L21 L21^T (only when the trailing matrix is one tile, m <= 128)
 int launch_trsm_tc(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
-                   cudaStream_t stream, bool upper);
+                   cudaStream_t stream, bool upper, bool fused);
 
 int launch_dpotrf(double *A, int n, int lda, int64_t strideA, int batch, int *info,
                   cudaStream_t stream, bool upper);

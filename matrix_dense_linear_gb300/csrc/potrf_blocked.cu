@@ -325,8 +325,16 @@ int launch_blocked(float *A, int n, int lda, int64_t strideA, int batch, int *in
         if (e) return e;
         const int m = n - c0 - nb;
         if (m <= 0) break;
-        // block updates of the panel solve on the tensor cores when aligned
-        e = launch_trsm_tc(A, n, lda, strideA, batch, info, c0, stream, upper);
+        // block updates of the panel solve on the tensor cores when aligned;
+        // a one-tile trailing matrix is updated by the same launch where that
+        // measured faster on GB300: the upper storage (4096 matrices of order
+        // 256: 1.02 against 1.10 ms), a ragged tile (order 200: 0.77 against
+        // 0.80 ms) and smaller batches (64 of order 256: 63 against 67 us), but
+        // not a full tile of a large batch (4096 of order 256: 0.80 either way,
+        // 1 % slower fused)
+        const bool fuse = m <= kTile && (upper || m < kTile || batch <= 2048);
+        e = launch_trsm_tc(A, n, lda, strideA, batch, info, c0, stream, upper, fuse);
+        if (e == 0 && fuse) continue;
         if (e == 1) {
             dim3 gt((unsigned)batch, (unsigned)((m + kTrsmRows - 1) / kTrsmRows));
             if (upper)

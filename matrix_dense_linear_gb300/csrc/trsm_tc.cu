@@ -100,8 +100,13 @@ struct LtPieces {
     }
 };
 
-template <bool UP>
-__global__ void __launch_bounds__(128, 3)
+// FUSED (the panel's rows are the whole trailing matrix, m <= 128): the
+// trailing update A22 -= L21 L21^T is done here too, as one more MMA group per
+// column block, D += X_j X_j^T in a second 128-column accumulator, subtracted
+// from A22's lower triangle at the end (no separate update launch; L21 is not
+// read back).
+template <bool UP, bool FUSED>
+__global__ void __launch_bounds__(128, FUSED ? 2 : 3)
 trsm_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
                int *__restrict__ info)
 {
@@ -127,8 +132,9 @@ trsm_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
         tc::mbar_init(&mbar, 1);
         tc::fence_mbar_init();
     }
+    constexpr uint32_t kCols = FUSED ? 256 : 128;
     if (warp == 0) {
-        tc::tmem_alloc(&tmem_base, 128);
+        tc::tmem_alloc(&tmem_base, kCols);
         tc::tmem_relinquish();
     }
 
@@ -230,7 +236,7 @@ trsm_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
                 for (int t = 0; t < 32; ++t) out[(int64_t)t * xs] = x[t];
             }
         }
-        if (j == 3) break;
+        if (j == 3 && !FUSED) break;
         // X_j as the A operand (K-major, hi/lo)
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
@@ -246,7 +252,7 @@ trsm_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
-        if (tid == 0) {
+        if (tid == 0 && j < 3) {
             // -A[:, 32(j+1):] += X_j L_{k,j}^T   (M = 128, N = 96 - 32j, K = 32)
             const uint32_t N = lt_rows(j);
             const uint32_t idesc = tc::idesc_tf32(128, N);
@@ -263,30 +269,92 @@ trsm_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
                 tc::mma_tf32(d, tc::smem_desc(xl + ko, kLbo, kSbo),
                              tc::smem_desc(bh + ko, kLbo, kSbo), idesc, 1u);
             }
-            tc::mma_commit(&mbar);
+        }
+        if constexpr (FUSED) {
+            if (tid == 0) {
+                // D += X_j X_j^T (M = N = 128, K = 32); the cross terms in the
+                // order that makes the upper storage's D the transpose, bit for
+                // bit, of the lower storage's
+                const uint32_t xh = sbase + kOffX, xl = xh + kXTile;
+                const uint32_t p2a = UP ? xl : xh, p2b = UP ? xh : xl;
+                const uint32_t p3a = UP ? xh : xl, p3b = UP ? xl : xh;
+                constexpr uint32_t idesc = tc::idesc_tf32(128, 128);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint32_t ko = ks * 2 * kLbo;
+                    tc::mma_tf32(tmem + 128, tc::smem_desc(xh + ko, kLbo, kSbo),
+                                 tc::smem_desc(xh + ko, kLbo, kSbo), idesc,
+                                 (j > 0 || ks > 0) ? 1u : 0u);
+                    tc::mma_tf32(tmem + 128, tc::smem_desc(p2a + ko, kLbo, kSbo),
+                                 tc::smem_desc(p2b + ko, kLbo, kSbo), idesc, 1u);
+                    tc::mma_tf32(tmem + 128, tc::smem_desc(p3a + ko, kLbo, kSbo),
+                                 tc::smem_desc(p3b + ko, kLbo, kSbo), idesc, 1u);
+                }
+            }
+        }
+        if (tid == 0) tc::mma_commit(&mbar);
+    }
+
+    if constexpr (FUSED) {
+        // the last group's completion (the fourth commit), then
+        // A22 -= D on the lower triangle of L's trailing block: thread r holds
+        // D's row r; lower storage: it updates the entries (r, c), c <= r,
+        // coalesced over r; upper storage: the entries (c, r), c >= r, whose
+        // memory (c1 + r) + (c1 + c) lda is coalesced over r too
+        if (tid == 0 && !sh_err && !tc::mbar_wait(&mbar, 1, kWaitCycles)) sh_err = 1;
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+        const int m = n - c0 - 128, r = tid, c1 = c0 + 128;
+        if (!sh_err) {  // uniform: the tensor-memory loads are warp-wide
+            float *Cr = Ab + (int64_t)c1 * lda + c1 + r;  // Cr[c * lda] = memory (c1 + r, c1 + c)
+#pragma unroll 1
+            for (int h = 0; h < 4; ++h) {
+                float v[32], old[32];
+#pragma unroll
+                for (int t = 0; t < 32; ++t) {
+                    const int c = 32 * h + t;
+                    const bool in = r < m && c < m && (UP ? c >= r : c <= r);
+                    old[t] = in ? Cr[(int64_t)c * lda] : 0.0f;
+                }
+                tc::tmem_ld32(tlane + 128 + 32 * h, v);
+#pragma unroll
+                for (int t = 0; t < 32; ++t) {
+                    const int c = 32 * h + t;
+                    const bool in = r < m && c < m && (UP ? c >= r : c <= r);
+                    if (in) Cr[(int64_t)c * lda] = old[t] - v[t];
+                }
+            }
         }
     }
 
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tmem, 128);
+    if (warp == 0) tc::tmem_dealloc(tmem, kCols);
     if (tid == 0 && sh_err) info[mat] = -1;
 }
 
-template <bool UP>
+// The fused form keeps three blocks per SM although three 256-column
+// accumulators exceed the SM's 512 columns: the third block's allocation
+// waits for one of the others to finish (measured: 4096 matrices of order 200
+// 771 us, against 780 us with two blocks per SM)
+constexpr int kSmemFused = kSmemBytes;
+
+template <bool UP, bool FUSED>
 int launch_k(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
              cudaStream_t stream)
 {
+    constexpr int smem = FUSED ? kSmemFused : kSmemBytes;
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(trsm_tc_kernel<UP>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        attr = cudaFuncSetAttribute(trsm_tc_kernel<UP, FUSED>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     });
     if (attr != cudaSuccess) return (int)attr;
     const int m = n - c0 - 128;
     dim3 grid((unsigned)batch, (unsigned)((m + 127) / 128));
-    trsm_tc_kernel<UP><<<grid, 128, kSmemBytes, stream>>>(A, n, lda, strideA, c0, info);
+    trsm_tc_kernel<UP, FUSED><<<grid, 128, smem, stream>>>(A, n, lda, strideA, c0, info);
     return (int)cudaGetLastError();
 }
 
@@ -295,11 +363,15 @@ int launch_k(float *A, int n, int lda, int64_t strideA, int batch, int *info, in
 // Returns 0 after launching, 1 when the caller must use the FP32 kernel
 // (unaligned panels), or a cudaError_t.
 int launch_trsm_tc(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
-                   cudaStream_t stream, bool upper)
+                   cudaStream_t stream, bool upper, bool fused)
 {
     if (((reinterpret_cast<uintptr_t>(A) & 15) != 0) || (lda & 3) || (strideA & 3)) return 1;
-    return upper ? launch_k<true>(A, n, lda, strideA, batch, info, c0, stream)
-                 : launch_k<false>(A, n, lda, strideA, batch, info, c0, stream);
+    if (fused && n - c0 - 128 > 128) return -1;
+    if (fused)
+        return upper ? launch_k<true, true>(A, n, lda, strideA, batch, info, c0, stream)
+                     : launch_k<false, true>(A, n, lda, strideA, batch, info, c0, stream);
+    return upper ? launch_k<true, false>(A, n, lda, strideA, batch, info, c0, stream)
+                 : launch_k<false, false>(A, n, lda, strideA, batch, info, c0, stream);
 }
 
 }  // namespace bl
