@@ -7,6 +7,7 @@
 
 #include "../../include/bl_spotrf.h"
 #include "bl_common.cuh"
+#include "launch.cuh"
 
 namespace {
 

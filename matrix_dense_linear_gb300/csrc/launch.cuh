@@ -1,0 +1,49 @@
+// Host-side launchers of the kernels of libbl_spotrf and the info convention
+// of a launch (internal, not installed).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace bl {
+
+// info handling of one launch over a strided batch.
+//   info_off < 0 : the launch factors whole matrices and writes info[b]
+//                  unconditionally (0 or the failing pivot).
+//   info_off >= 0: the launch factors the diagonal block at (info_off,
+//                  info_off) of a larger matrix; it skips matrices whose
+//                  info[b] is already nonzero and writes info[b] only on a
+//                  failure, as info_off + local index.
+struct InfoMode {
+    int off;
+};
+
+// `upper`: the factor is stored in the upper triangle (uplo = 'U', see lidx).
+int launch_warp(float *A, int n, int lda, int64_t strideA, int batch, int *info,
+                cudaStream_t stream, bool upper);
+// no_bulk: A may be host memory the device maps (no bulk copies then)
+int launch_cta(float *A, int n, int lda, int64_t strideA, int batch, int *info,
+               cudaStream_t stream, InfoMode mode, bool upper, bool no_bulk = false);
+int launch_tmem(float *A, int n, int lda, int64_t strideA, int batch, int *info,
+                cudaStream_t stream, InfoMode mode);
+int launch_blocked(float *A, int n, int lda, int64_t strideA, int batch, int *info,
+                   cudaStream_t stream, bool upper);
+
+int launch_syrk_tc(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
+                   cudaStream_t stream, bool upper);
+int attrs_syrk_tc(cudaFuncAttributes *fa);
+// fused: also A22 -= L21 L21^T (only when the trailing matrix is one tile, m <= 128)
+int launch_trsm_tc(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
+                   cudaStream_t stream, bool upper, bool fused);
+
+int launch_dpotrf(double *A, int n, int lda, int64_t strideA, int batch, int *info,
+                  cudaStream_t stream, bool upper);
+int launch_potrs(const float *L, int n, int lda, int64_t strideA, float *B, int nrhs, int ldb,
+                 int64_t strideB, int batch, const int *info, cudaStream_t stream, bool upper);
+int attrs_potrs(cudaFuncAttributes *fa, int *threads, int *dyn_smem);
+int attrs_warp(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem);
+int attrs_cta(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem);
+int attrs_tmem(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem);
+int attrs_blocked(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem);
+
+}  // namespace bl

@@ -17,6 +17,7 @@
 #include <mutex>
 
 #include "bl_common.cuh"
+#include "launch.cuh"
 
 namespace bl {
 namespace {

@@ -29,6 +29,7 @@
 #include <mutex>
 
 #include "cta_common.cuh"
+#include "launch.cuh"
 
 namespace bl {
 namespace {

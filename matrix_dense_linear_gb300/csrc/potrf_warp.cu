@@ -23,6 +23,7 @@
 #include <mutex>
 
 #include "bl_common.cuh"
+#include "launch.cuh"
 
 namespace bl {
 namespace {

@@ -26,6 +26,7 @@
 // nonzero is left untouched (the posv path).
 
 #include "bl_common.cuh"
+#include "launch.cuh"
 
 namespace bl {
 namespace {

@@ -27,6 +27,7 @@
 #include <mutex>
 
 #include "bl_common.cuh"
+#include "launch.cuh"
 #include "tc_sm100.cuh"
 
 namespace bl {
