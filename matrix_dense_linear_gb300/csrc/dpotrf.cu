@@ -32,7 +32,10 @@ constexpr int kDKc = 16;     // k staged per round of the update
 // One block per matrix (or per diagonal block at (c0, c0) of a larger one
 // when info_off >= 0: then matrices already failed are skipped and a failure
 // is reported as info_off + its local index). The block's lower triangle sits
-// column-major in shared memory with leading dimension n.
+// packed column by column in shared memory (column k from k(2n - k + 1)/2),
+// 66 KB at n = 128: three blocks share an SM and keep its FP64 pipe fed.
+__device__ __forceinline__ int pk(int i, int k, int n) { return k * n - (k * (k - 1) >> 1) + (i - k); }
+
 template <bool UP>
 __global__ void __launch_bounds__(128)
 dpotrf_cta_kernel(double *__restrict__ A, int n, int lda, int64_t strideA, int batch,
@@ -40,27 +43,34 @@ dpotrf_cta_kernel(double *__restrict__ A, int n, int lda, int64_t strideA, int b
 {
     extern __shared__ __align__(16) double Sd[];
     __shared__ int sh_fail;
+    __shared__ double sh_rinv;
     const int64_t mat = blockIdx.x;
     if (info_off >= 0 && info[mat] != 0) return;
     double *__restrict__ Ab = A + mat * strideA;
     const int tid = threadIdx.x;
     if (tid == 0) sh_fail = 0;
     for (int j = 0; j < n; ++j)
-        for (int i = j + tid; i < n; i += blockDim.x) Sd[i + j * n] = Ab[lidx<UP>(i, j, lda)];
+        for (int i = j + tid; i < n; i += blockDim.x) Sd[pk(i, j, n)] = Ab[lidx<UP>(i, j, lda)];
     __syncthreads();
 
-    int fail = 0;
     for (int j = 0; j < n; ++j) {
-        const double d = Sd[j + j * n];
-        if (!(d > 0.0)) {  // every thread reads the same pivot: a uniform exit
-            fail = j + 1;
-            break;
+        // one thread takes the pivot's root and reciprocal (FP64 square root
+        // and division are long sequences on this GPU's slow FP64 pipe)
+        if (tid == 0) {
+            const double d = Sd[pk(j, j, n)];
+            if (!(d > 0.0)) {
+                sh_fail = j + 1;
+            } else {
+                const double ljj = sqrt(d);
+                Sd[pk(j, j, n)] = ljj;
+                sh_rinv = 1.0 / ljj;
+            }
         }
-        const double ljj = sqrt(d);
-        const double rinv = 1.0 / ljj;
-        for (int i = j + 1 + tid; i < n; i += blockDim.x) Sd[i + j * n] *= rinv;
         __syncthreads();
-        if (tid == 0) Sd[j + j * n] = ljj;
+        if (sh_fail) break;  // uniform
+        const double rinv = sh_rinv;
+        for (int i = j + 1 + tid; i < n; i += blockDim.x) Sd[pk(i, j, n)] *= rinv;
+        __syncthreads();
         // trailing lower triangle, balanced: thread pair p takes rows j+1+p
         // and n-1-p (m+1 entries together), each thread every other column
         // of both; n <= 128 leaves at most 64 pairs for the 128 threads
@@ -68,24 +78,28 @@ dpotrf_cta_kernel(double *__restrict__ A, int n, int lda, int64_t strideA, int b
             const int p = tid >> 1, h = tid & 1;
             const int ra = j + 1 + p, rb = n - 1 - p;
             if (ra <= rb) {
-                const double la = Sd[ra + j * n];
+                const double *cj = Sd + pk(j, j, n) - j;  // cj[k] = element (k, j)
+                const double la = cj[ra];
 #pragma unroll 4
-                for (int k = j + 1 + h; k <= ra; k += 2)
-                    Sd[ra + k * n] = fma(-la, Sd[k + j * n], Sd[ra + k * n]);
+                for (int k = j + 1 + h; k <= ra; k += 2) {
+                    double *e = Sd + pk(ra, k, n);
+                    *e = fma(-la, cj[k], *e);
+                }
                 if (rb > ra) {
-                    const double lb = Sd[rb + j * n];
+                    const double lb = cj[rb];
 #pragma unroll 4
-                    for (int k = j + 1 + h; k <= rb; k += 2)
-                        Sd[rb + k * n] = fma(-lb, Sd[k + j * n], Sd[rb + k * n]);
+                    for (int k = j + 1 + h; k <= rb; k += 2) {
+                        double *e = Sd + pk(rb, k, n);
+                        *e = fma(-lb, cj[k], *e);
+                    }
                 }
             }
         }
         __syncthreads();
     }
-    if (tid == 0) sh_fail = fail;
     __syncthreads();
     for (int j = 0; j < n; ++j)
-        for (int i = j + tid; i < n; i += blockDim.x) Ab[lidx<UP>(i, j, lda)] = Sd[i + j * n];
+        for (int i = j + tid; i < n; i += blockDim.x) Ab[lidx<UP>(i, j, lda)] = Sd[pk(i, j, n)];
     if (tid == 0) {
         if (info_off < 0) info[mat] = sh_fail;
         else if (sh_fail) info[mat] = info_off + sh_fail;
@@ -103,6 +117,7 @@ dtrsm_rows_kernel(double *__restrict__ A, int n, int lda, int64_t strideA, int c
                   const int *__restrict__ info)
 {
     extern __shared__ __align__(16) double Ld[];  // Ld[i + k * 128] = L11(i, k), i >= k
+    __shared__ double rdiag[kDNb];                // 1 / L11(j, j)
     const int64_t mat = blockIdx.x;
     if (info[mat] != 0) return;
     double *__restrict__ Ab = A + mat * strideA;
@@ -110,6 +125,8 @@ dtrsm_rows_kernel(double *__restrict__ A, int n, int lda, int64_t strideA, int c
     for (int k = 0; k < kDNb; ++k)
         for (int i = k + tid; i < kDNb; i += blockDim.x)
             Ld[i + k * kDNb] = Ab[lidx<UP>(c0 + i, c0 + k, lda)];
+    __syncthreads();
+    for (int j = tid; j < kDNb; j += blockDim.x) rdiag[j] = 1.0 / Ld[j + j * kDNb];
     __syncthreads();
     const int row = c0 + kDNb + blockIdx.y * blockDim.x + tid;
     if (row >= n) return;
@@ -130,7 +147,7 @@ dtrsm_rows_kernel(double *__restrict__ A, int n, int lda, int64_t strideA, int c
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
             const int j = 32 * jb + c;
-            x[c] /= Ld[j + j * kDNb];
+            x[c] *= rdiag[j];
 #pragma unroll
             for (int t = c + 1; t < 32; ++t) x[t] = fma(-x[c], Ld[32 * jb + t + j * kDNb], x[t]);
         }
@@ -208,8 +225,9 @@ int launch_dcta(double *A, int n, int lda, int64_t strideA, int batch, int *info
                                     kDNb * kDNb * 8);
     });
     if (attr != cudaSuccess) return (int)attr;
-    dpotrf_cta_kernel<UP><<<(unsigned)batch, 128, (size_t)n * n * 8, st>>>(A, n, lda, strideA,
-                                                                            batch, info, info_off);
+    const size_t smem = (size_t)n * (n + 1) / 2 * 8;
+    dpotrf_cta_kernel<UP><<<(unsigned)batch, 128, smem, st>>>(A, n, lda, strideA, batch, info,
+                                                             info_off);
     return (int)cudaGetLastError();
 }
 
