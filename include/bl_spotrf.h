@@ -241,6 +241,18 @@ int bl_dpotrf_batched(double *A, int n, int lda, int64_t strideA, int batch, int
 int bl_dpotrf_batched_uplo(char uplo, double *A, int n, int lda, int64_t strideA, int batch,
                            int *info, cudaStream_t stream);
 
+/*
+ * bl_fma_probe - the FMA throughput this device reaches (TFLOP/s, 2 flops an
+ * FMA) with eight independent FMA chains a thread, 256 threads a block and
+ * eight blocks an SM: the compute peak the factorizations are read against
+ * (precision 32 or 64). out: a device pointer to one element of that
+ * precision (written only in a case that does not occur; it keeps the chains
+ * from being removed). Synchronizes `stream` (it times two launches with
+ * events). Returns 0, -1 (precision), -2 (out NULL), -3 (tflops NULL) or a
+ * cudaError_t.
+ */
+int bl_fma_probe(int precision, void *out, double *tflops, cudaStream_t stream);
+
 /* Version string of the library ("bl_spotrf <major>.<minor> sm_103a"). */
 const char *bl_spotrf_version(void);
 

@@ -37,6 +37,7 @@ SYMBOLS = {
     "bl_sposv_batched": (_I, [_VP, _I, _I, _I64, _VP, _I, _I, _I64, _I, _VP, _VP]),
     "bl_spotrf_batched_uplo": (_I, [_C, _VP, _I, _I, _I64, _I, _VP, _VP]),
     "bl_dpotrf_batched": (_I, [_VP, _I, _I, _I64, _I, _VP, _VP]),
+    "bl_fma_probe": (_I, [_I, _VP, _VP, _VP]),
     "bl_dpotrf_batched_uplo": (_I, [_C, _VP, _I, _I, _I64, _I, _VP, _VP]),
     "bl_spotrf_batched_uplo_ex": (_I, [_C, _VP, _I, _I, _I64, _I, _VP, _VP, _I]),
     "bl_spotrs_batched_uplo": (_I, [_C, _VP, _I, _I, _I64, _VP, _I, _I, _I64, _I, _VP]),
@@ -147,6 +148,18 @@ def factor_double(A, n: int, lda: int, strideA: int, batch: int, info, stream=No
     code = dpotrf_batched(A, n, lda, strideA, batch, info, stream, uplo)
     if code:
         raise BLError(code, "dpotrf")
+
+
+def fma_probe(precision: int = 32, stream=None) -> float:
+    """bl_fma_probe: this device's FMA throughput in TFLOP/s (32 or 64 bit)."""
+    import torch
+    out = torch.zeros(1, dtype=torch.float64 if precision == 64 else torch.float32,
+                      device="cuda")
+    v = ctypes.c_double(0.0)
+    code = library().bl_fma_probe(precision, _ptr(out), ctypes.byref(v), _stream(stream))
+    if code:
+        raise BLError(code, "fma_probe")
+    return v.value
 
 
 def route(n: int, batch: int) -> int:

@@ -217,6 +217,22 @@ def test_host_call_pinned_and_pageable_agree(n, batch):
             what=f"host n={n}")
 
 
+def test_fma_probe():
+    """The probe's rates are positive and FP64 is far below FP32 on this GPU
+    (and below the FP32 roofline's unit count times the clock)."""
+    import torch
+
+    import matrix_dense_linear_gb300 as bl
+    f32, f64 = bl.fma_probe(32), bl.fma_probe(64)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert 0 < f64 < f32 <= sms * 128 * 2 * 2.2e9 / 1e12
+    out = torch.zeros(1, device="cuda")
+    import ctypes
+    v = ctypes.c_double(0.0)
+    assert bl.library().bl_fma_probe(16, out.data_ptr(), ctypes.byref(v), None) == -1
+    assert bl.library().bl_fma_probe(32, None, ctypes.byref(v), None) == -2
+
+
 def test_n_zero_and_batch_zero():
     import torch
 
