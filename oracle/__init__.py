@@ -7,7 +7,8 @@ links, loads or calls it, and it never calls the CUDA library.
 
 The arithmetic lives in ``chol_ref.c`` (plain C, IEEE double, unblocked
 Cholesky-Crout), ``dchol_ref.c`` (the same for a double-precision input) and
-``potrs_ref.c`` (forward and backward substitution with the factor); this
+``potrs_ref.c`` (forward and backward substitution with the factor) and
+``cchol_ref.c`` (the Hermitian factorization of a complex input); this
 module only compiles them with gcc into
 ``oracle/_build/liboracle.so`` and marshals numpy arrays through ctypes.
 """
@@ -23,7 +24,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRCS = [os.path.join(_HERE, "chol_ref.c"), os.path.join(_HERE, "potrs_ref.c"),
-         os.path.join(_HERE, "dchol_ref.c")]
+         os.path.join(_HERE, "dchol_ref.c"), os.path.join(_HERE, "cchol_ref.c")]
 _BUILD = os.path.join(_HERE, "_build")
 _SO = os.path.join(_BUILD, "liboracle.so")
 _lock = threading.Lock()
@@ -64,6 +65,12 @@ def _load():
         lib.oracle_dpotrf_upper_one.argtypes = lib.oracle_potrf_one.argtypes
         lib.oracle_dpotrf_batched_uplo.restype = ctypes.c_int
         lib.oracle_dpotrf_batched_uplo.argtypes = lib.oracle_potrf_batched_uplo.argtypes
+        lib.oracle_cpotrf_one.restype = ctypes.c_int
+        lib.oracle_cpotrf_one.argtypes = lib.oracle_potrf_one.argtypes
+        lib.oracle_cpotrf_upper_one.restype = ctypes.c_int
+        lib.oracle_cpotrf_upper_one.argtypes = lib.oracle_potrf_one.argtypes
+        lib.oracle_cpotrf_batched_uplo.restype = ctypes.c_int
+        lib.oracle_cpotrf_batched_uplo.argtypes = lib.oracle_potrf_batched_uplo.argtypes
         lib.oracle_potrs_one.restype = None
         lib.oracle_potrs_one.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
@@ -138,6 +145,46 @@ def dpotrf_batched(buf: np.ndarray, n: int, lda: int, strideA: int, batch: int,
     info = np.zeros(m, dtype=np.int32)
     th = default_threads() if nthreads is None else nthreads
     used = lib.oracle_dpotrf_batched_uplo(b"U" if _upper(uplo) else b"L", src.ctypes.data, n,
+                                          lda, sA, m, L.ctypes.data, n * n, info.ctypes.data,
+                                          th)
+    return L.transpose(0, 2, 1), info, int(used)
+
+
+def cpotrf_one(A: np.ndarray, uplo: str = "L") -> tuple[np.ndarray, int]:
+    """Factor one Hermitian matrix A = L L^H (``uplo="U"``: A = U^H U). ``A``
+    is rounded to complex64 (the input type); only its lower (upper) triangle
+    is read, and the diagonal's imaginary part is ignored. Returns (the factor
+    as complex128 n x n, info)."""
+    a64 = np.asfortranarray(np.asarray(A, dtype=np.complex64))
+    n = a64.shape[0]
+    L = np.zeros((n, n), dtype=np.complex128, order="F")
+    lib = _load()
+    fn = lib.oracle_cpotrf_upper_one if _upper(uplo) else lib.oracle_cpotrf_one
+    info = fn(a64.ctypes.data, n, max(1, n), L.ctypes.data, max(1, n))
+    return np.ascontiguousarray(L), int(info)
+
+
+def cpotrf_batched(buf: np.ndarray, n: int, lda: int, strideA: int, batch: int,
+                   indices: Optional[Sequence[int]] = None, nthreads: Optional[int] = None,
+                   uplo: str = "L") -> tuple[np.ndarray, np.ndarray, int]:
+    """``potrf_batched`` for a flat complex64 batch (element (i, j) of matrix b
+    at ``buf[b*strideA + i + j*lda]``)."""
+    lib = _load()
+    buf = np.ascontiguousarray(buf, dtype=np.complex64)
+    if indices is None:
+        src, sA, m = buf, strideA, batch
+    else:
+        idx = list(indices)
+        m = len(idx)
+        span = lda * n
+        src = np.empty(max(1, m * span), dtype=np.complex64)
+        for t, b in enumerate(idx):
+            src[t * span:(t + 1) * span] = buf[b * strideA: b * strideA + span]
+        sA = span
+    L = np.zeros((m, n, n), dtype=np.complex128)
+    info = np.zeros(m, dtype=np.int32)
+    th = default_threads() if nthreads is None else nthreads
+    used = lib.oracle_cpotrf_batched_uplo(b"U" if _upper(uplo) else b"L", src.ctypes.data, n,
                                           lda, sA, m, L.ctypes.data, n * n, info.ctypes.data,
                                           th)
     return L.transpose(0, 2, 1), info, int(used)
