@@ -622,45 +622,62 @@ FP64_PEAK_TFLOPS = 1.25
 
 
 def run_shapes_f64(args) -> list:
-    """--shapes with --dtype f64: the double-precision factorization (DPOTRF)
-    on A = G G^T / n + I in float64 (64 distinct matrices repeated), the same
-    timing as run_shapes, against the FP64 roofline."""
+    """--shapes with --dtype f64 or c64: the double-precision (DPOTRF) or the
+    complex Hermitian (CPOTRF) factorization of A = G G^H / n + I (G iid
+    normal, complex for c64; 64 distinct matrices repeated), the same timing
+    as run_shapes; f64 against the measured FP64 rate, c64 (4 n^3 / 3 real
+    flops a matrix) against the FP32 roofline."""
     import torch
 
     import matrix_dense_linear_gb300 as bl
     import synth
     bl.library()
     dev = torch.device("cuda", 0)
-    try:
-        peak, peak_src = bl.fma_probe(64), "measured (bl_fma_probe)"
-    except Exception:  # noqa: BLE001
-        peak, peak_src = FP64_PEAK_TFLOPS, "nominal"
+    cplx = args.dtype == "c64"
+    if cplx:
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        peak = sms * 128 * 2 * peaks()["sm_max_mhz"] * 1e6 / 1e12
+        peak_src = "FP32: SMs x 128 FMA x 2 x max clock"
+    else:
+        try:
+            peak, peak_src = bl.fma_probe(64), "measured (bl_fma_probe)"
+        except Exception:  # noqa: BLE001
+            peak, peak_src = FP64_PEAK_TFLOPS, "nominal"
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     rows = []
     for spec in args.shapes.split(","):
         n, batch = (int(x) for x in spec.lower().split("x"))
         distinct = min(batch, 64)
-        mats = [synth.gram(n, synth.rng(6, b), "normal", float(n), 1.0) for b in range(distinct)]
+        if cplx:
+            mats = []
+            for b in range(distinct):
+                g = synth.rng(7, b)
+                G = g.standard_normal((n, n)) + 1j * g.standard_normal((n, n))
+                mats.append((G @ G.conj().T / n + np.eye(n)).astype(np.complex64))
+        else:
+            mats = [synth.gram(n, synth.rng(6, b), "normal", float(n), 1.0)
+                    for b in range(distinct)]
         one = np.concatenate([np.asfortranarray(m).ravel(order="F") for m in mats])
         buf = np.tile(one, -(-batch // distinct))[: batch * n * n]
         src = torch.from_numpy(np.ascontiguousarray(buf)).to(dev)
         nbytes = src.numel() * 8
         nrep = int(max(1, min(max(args.steps, -(-2 * l2 // nbytes)),
                               REPLICA_CAP_BYTES // max(nbytes, 1))))
-        reps = torch.empty((nrep, src.numel()), dtype=torch.float64, device=dev)
+        reps = torch.empty((nrep, src.numel()), dtype=src.dtype, device=dev)
+        fac = bl.factor_complex if cplx else bl.factor_double
         info = torch.zeros(batch, dtype=torch.int32, device=dev)
         st = torch.cuda.current_stream()
         for i in range(min(args.warmup, nrep)):
             reps[i].copy_(src)
-            bl.factor_double(reps[i], n, n, n * n, batch, info, st, uplo=args.uplo)
+            fac(reps[i], n, n, n * n, batch, info, st, uplo=args.uplo)
         torch.cuda.synchronize()
         k = min(args.steps, nrep)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             for i in range(k):
-                bl.factor_double(reps[i], n, n, n * n, batch, info,
-                                 torch.cuda.current_stream(), uplo=args.uplo)
+                fac(reps[i], n, n, n * n, batch, info, torch.cuda.current_stream(),
+                    uplo=args.uplo)
         ts = []
         for _ in range(3):
             for i in range(k):
@@ -676,8 +693,8 @@ def run_shapes_f64(args) -> list:
             ts.append(e0.elapsed_time(e1) / k)
         assert not info.cpu().numpy().any()
         ms = statistics.median(ts)
-        tflops = flops_per_matrix(n) * batch / (ms / 1e3) / 1e12
-        row = {"shape": spec, "dtype": "f64", "uplo": args.uplo, "n": n, "batch": batch,
+        tflops = (4 if cplx else 1) * flops_per_matrix(n) * batch / (ms / 1e3) / 1e12
+        row = {"shape": spec, "dtype": args.dtype, "uplo": args.uplo, "n": n, "batch": batch,
                "ms_per_call": ms, "us_per_call": ms * 1e3, "matrices_per_s": batch / (ms / 1e3),
                "tflops": tflops,
                "roofline": {"bound": "alu", "peak": peak, "unit": "TFLOP/s",
@@ -829,8 +846,8 @@ def main():
     ap.add_argument("--shapes", default=None, metavar="NxB,...",
                     help="time these (n, batch) shapes (one JSON line each); 'pages' = "
                          "the shapes the pages quote timings for")
-    ap.add_argument("--dtype", choices=["f32", "f64"], default="f32",
-                    help="f64: time the double-precision factorization for --shapes")
+    ap.add_argument("--dtype", choices=["f32", "f64", "c64"], default="f32",
+                    help="f64 / c64: time the double / complex factorization for --shapes")
     ap.add_argument("--uplo", choices=["L", "U"], default="L",
                     help="storage of the factor for --shapes (U: upper triangle)")
     args = ap.parse_args()
@@ -846,7 +863,7 @@ def main():
     if args.shapes:
         if args.shapes == "pages":
             args.shapes = PAGES_SHAPES
-        if args.dtype == "f64":
+        if args.dtype in ("f64", "c64"):
             run_shapes_f64(args)
         else:
             run_shapes(args)

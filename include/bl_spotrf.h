@@ -242,6 +242,24 @@ int bl_dpotrf_batched_uplo(char uplo, double *A, int n, int lda, int64_t strideA
                            int *info, cudaStream_t stream);
 
 /*
+ * bl_cpotrf_batched / bl_cpotrf_batched_uplo - the factorization of a
+ * single-precision complex Hermitian batch (CPOTRF): A = L L^H with L lower
+ * triangular and a real positive diagonal (uplo 'U': A = U^H U, U = L^H, in
+ * the upper triangle). A points at interleaved complex floats (real,
+ * imaginary; the layout of std::complex<float> / cuFloatComplex), 8-byte
+ * aligned (else -1, or -2 for the uplo form); lda and strideA count complex
+ * elements. The imaginary part of the diagonal is not read (taken as zero),
+ * and the factor's diagonal is written with a zero imaginary part. Pivots
+ * d_j = re(a_jj) - sum_k |l_jk|^2 are tested as in bl_spotrf_batched. All
+ * other conventions (info, argument indices, quick returns, ownership,
+ * streams) as bl_spotrf_batched / bl_spotrf_batched_uplo.
+ */
+int bl_cpotrf_batched(float *A, int n, int lda, int64_t strideA, int batch, int *info,
+                      cudaStream_t stream);
+int bl_cpotrf_batched_uplo(char uplo, float *A, int n, int lda, int64_t strideA, int batch,
+                           int *info, cudaStream_t stream);
+
+/*
  * bl_fma_probe - the FMA throughput this device reaches (TFLOP/s, 2 flops an
  * FMA) with eight independent FMA chains a thread, 256 threads a block and
  * eight blocks an SM: the compute peak the factorizations are read against

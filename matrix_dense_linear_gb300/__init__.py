@@ -38,6 +38,8 @@ SYMBOLS = {
     "bl_spotrf_batched_uplo": (_I, [_C, _VP, _I, _I, _I64, _I, _VP, _VP]),
     "bl_dpotrf_batched": (_I, [_VP, _I, _I, _I64, _I, _VP, _VP]),
     "bl_fma_probe": (_I, [_I, _VP, _VP, _VP]),
+    "bl_cpotrf_batched": (_I, [_VP, _I, _I, _I64, _I, _VP, _VP]),
+    "bl_cpotrf_batched_uplo": (_I, [_C, _VP, _I, _I, _I64, _I, _VP, _VP]),
     "bl_dpotrf_batched_uplo": (_I, [_C, _VP, _I, _I, _I64, _I, _VP, _VP]),
     "bl_spotrf_batched_uplo_ex": (_I, [_C, _VP, _I, _I, _I64, _I, _VP, _VP, _I]),
     "bl_spotrs_batched_uplo": (_I, [_C, _VP, _I, _I, _I64, _VP, _I, _I, _I64, _I, _VP]),
@@ -140,6 +142,24 @@ def dpotrf_batched(A, n: int, lda: int, strideA: int, batch: int, info, stream=N
                                            _stream(stream))
     return library().bl_dpotrf_batched_uplo(_uplo(uplo), _ptr(A), n, lda, strideA, batch,
                                             _ptr(info), _stream(stream))
+
+
+def cpotrf_batched(A, n: int, lda: int, strideA: int, batch: int, info, stream=None,
+                   uplo="L") -> int:
+    """bl_cpotrf_batched(_uplo): A is a complex64 device tensor (or pointer)."""
+    if uplo in ("L", b"L"):
+        return library().bl_cpotrf_batched(_ptr(A), n, lda, strideA, batch, _ptr(info),
+                                           _stream(stream))
+    return library().bl_cpotrf_batched_uplo(_uplo(uplo), _ptr(A), n, lda, strideA, batch,
+                                            _ptr(info), _stream(stream))
+
+
+def factor_complex(A, n: int, lda: int, strideA: int, batch: int, info, stream=None,
+                   uplo="L") -> None:
+    """cpotrf_batched, raising BLError on a nonzero status."""
+    code = cpotrf_batched(A, n, lda, strideA, batch, info, stream, uplo)
+    if code:
+        raise BLError(code, "cpotrf")
 
 
 def factor_double(A, n: int, lda: int, strideA: int, batch: int, info, stream=None,

@@ -165,6 +165,18 @@ def test_dpotrf_argument_codes(bl):
     assert lib.bl_dpotrf_batched(None, 4, 4, 16, 0, None, None) == 0
 
 
+def test_cpotrf_argument_codes(bl):
+    lib = bl.library()
+    cases = [((8, -1, 1, 1, 1, 8), -2), ((8, 4, 4, 16, -1, 8), -5), ((8, 4, 3, 16, 2, 8), -3),
+             ((8, 4, 4, 15, 2, 8), -4), ((None, 4, 4, 16, 2, 8), -1),
+             ((8, 4, 4, 16, 2, None), -6), ((8, 4097, 4097, 4097 * 4097, 2, 8), -7),
+             ((12, 4, 4, 16, 2, 8), -1)]  # not 8-byte aligned
+    for args, code in cases:
+        assert lib.bl_cpotrf_batched(*args, None) == code
+        assert lib.bl_cpotrf_batched_uplo(b"L", *args, None) == code - 1
+    assert lib.bl_cpotrf_batched_uplo(b"?", 8, 4, 4, 16, 1, 8, None) == -1
+
+
 def test_forced_route_that_cannot_run(bl):
     lib = bl.library()
     assert lib.bl_spotrf_batched_ex(8, 65, 65, 65 * 65, 1, 8, None, bl.ROUTE_WARP) == -8
