@@ -71,6 +71,12 @@ def _load():
         lib.oracle_cpotrf_upper_one.argtypes = lib.oracle_potrf_one.argtypes
         lib.oracle_cpotrf_batched_uplo.restype = ctypes.c_int
         lib.oracle_cpotrf_batched_uplo.argtypes = lib.oracle_potrf_batched_uplo.argtypes
+        lib.oracle_zpotrf_one.restype = ctypes.c_int
+        lib.oracle_zpotrf_one.argtypes = lib.oracle_potrf_one.argtypes
+        lib.oracle_zpotrf_upper_one.restype = ctypes.c_int
+        lib.oracle_zpotrf_upper_one.argtypes = lib.oracle_potrf_one.argtypes
+        lib.oracle_zpotrf_batched_uplo.restype = ctypes.c_int
+        lib.oracle_zpotrf_batched_uplo.argtypes = lib.oracle_potrf_batched_uplo.argtypes
         lib.oracle_potrs_one.restype = None
         lib.oracle_potrs_one.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
@@ -164,27 +170,42 @@ def cpotrf_one(A: np.ndarray, uplo: str = "L") -> tuple[np.ndarray, int]:
     return np.ascontiguousarray(L), int(info)
 
 
+def zpotrf_one(A: np.ndarray, uplo: str = "L") -> tuple[np.ndarray, int]:
+    """``cpotrf_one`` for a double-precision complex input (taken as
+    complex128, no rounding)."""
+    a = np.asfortranarray(np.asarray(A, dtype=np.complex128))
+    n = a.shape[0]
+    L = np.zeros((n, n), dtype=np.complex128, order="F")
+    lib = _load()
+    fn = lib.oracle_zpotrf_upper_one if _upper(uplo) else lib.oracle_zpotrf_one
+    info = fn(a.ctypes.data, n, max(1, n), L.ctypes.data, max(1, n))
+    return np.ascontiguousarray(L), int(info)
+
+
 def cpotrf_batched(buf: np.ndarray, n: int, lda: int, strideA: int, batch: int,
                    indices: Optional[Sequence[int]] = None, nthreads: Optional[int] = None,
                    uplo: str = "L") -> tuple[np.ndarray, np.ndarray, int]:
     """``potrf_batched`` for a flat complex64 batch (element (i, j) of matrix b
-    at ``buf[b*strideA + i + j*lda]``)."""
+    at ``buf[b*strideA + i + j*lda]``); a complex128 batch is factored by the
+    double-precision-input form (ZPOTRF)."""
     lib = _load()
-    buf = np.ascontiguousarray(buf, dtype=np.complex64)
+    dbl = np.asarray(buf).dtype == np.complex128
+    buf = np.ascontiguousarray(buf, dtype=np.complex128 if dbl else np.complex64)
     if indices is None:
         src, sA, m = buf, strideA, batch
     else:
         idx = list(indices)
         m = len(idx)
         span = lda * n
-        src = np.empty(max(1, m * span), dtype=np.complex64)
+        src = np.empty(max(1, m * span), dtype=buf.dtype)
         for t, b in enumerate(idx):
             src[t * span:(t + 1) * span] = buf[b * strideA: b * strideA + span]
         sA = span
     L = np.zeros((m, n, n), dtype=np.complex128)
     info = np.zeros(m, dtype=np.int32)
     th = default_threads() if nthreads is None else nthreads
-    used = lib.oracle_cpotrf_batched_uplo(b"U" if _upper(uplo) else b"L", src.ctypes.data, n,
+    fn = lib.oracle_zpotrf_batched_uplo if dbl else lib.oracle_cpotrf_batched_uplo
+    used = fn(b"U" if _upper(uplo) else b"L", src.ctypes.data, n,
                                           lda, sA, m, L.ctypes.data, n * n, info.ctypes.data,
                                           th)
     return L.transpose(0, 2, 1), info, int(used)

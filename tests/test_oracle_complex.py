@@ -1,4 +1,4 @@
-"""Pins of the complex Hermitian oracle (CPOTRF, A = L L^H, lower and upper)
+"""Pins of the complex Hermitian oracle (CPOTRF and ZPOTRF, A = L L^H, lower and upper)
 against what the mathematics fixes (CPU only): the 2 x 2 closed form,
 Gaussian-integer factors recovered bit for bit, leading minors for n <= 3,
 exact info, the real oracle (pinned on its own) on real inputs, the
@@ -137,6 +137,35 @@ def test_batched_matches_single():
 
 
 # --------------------------------------------------------------------------
+# Double-precision complex input (ZPOTRF)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n", [2, 9, 40])
+def test_z_gaussian_integer_factor_beyond_single(n):
+    # entries up to 2^13: A's entries pass 2^24 (not complex64-exact) but every
+    # intermediate stays an exact double integer
+    g = np.random.default_rng(60 + n)
+    L = np.tril(g.integers(-2 ** 13, 2 ** 13, (n, n)) + 1j * g.integers(-2 ** 13, 2 ** 13, (n, n)),
+                -1)
+    L[np.diag_indices(n)] = g.integers(1, 2 ** 13, n)
+    A = L @ L.conj().T
+    assert np.abs(A).max() > 2 ** 24
+    for uplo, want in (("L", L), ("U", L.conj().T)):
+        F, info = oracle.zpotrf_one(A, uplo)
+        assert info == 0 and np.array_equal(F, want)
+
+
+def test_z_matches_c_on_complex64_inputs():
+    A = hermitian_spd(30, 7).astype(np.complex64)
+    for uplo in ("L", "U"):
+        assert np.array_equal(oracle.zpotrf_one(A.astype(np.complex128), uplo)[0],
+                              oracle.cpotrf_one(A, uplo)[0])
+    buf = np.concatenate([np.asfortranarray(A).ravel(order="F")] * 3)
+    F, info, _ = oracle.cpotrf_batched(buf.astype(np.complex128), 30, 30, 900, 3)
+    assert not info.any() and np.array_equal(F[2], oracle.cpotrf_one(A)[0])
+
+
+# --------------------------------------------------------------------------
 # Planted mistakes
 # --------------------------------------------------------------------------
 
@@ -148,9 +177,12 @@ MUTANTS = {
                                   "d -= creal(ljk * ljk);"),
     "upper without conjugate": ("s -= conj(U[k + (int64_t)j * ldu]) * U[k + (int64_t)i * ldu];",
                                 "s -= U[k + (int64_t)j * ldu] * U[k + (int64_t)i * ldu];"),
-    "upper reads the lower triangle": ("double complex s = ld_c(A, j + (int64_t)i * lda);",
-                                       "double complex s = ld_c(A, i + (int64_t)j * lda);"),
+    "upper reads the lower triangle": ("double complex s = ld_c(A, dbl, j + (int64_t)i * lda);",
+                                       "double complex s = ld_c(A, dbl, i + (int64_t)j * lda);"),
     "info zero-based": ("return j + 1;", "return j;"),
+    "double input rounded to float": (
+        "return ((const double *)A)[2 * idx] + ((const double *)A)[2 * idx + 1] * I;",
+        "return (float)((const double *)A)[2 * idx] + (float)((const double *)A)[2 * idx + 1] * I;"),
 }
 
 
@@ -179,6 +211,17 @@ def _battery(lib) -> list[str]:
     d = np.diag(np.array([1, 4, 0, 9], dtype=np.complex64))
     if run(lib.oracle_cpotrf_one, d)[1] != 3:
         failed.append("info")
+    lib.oracle_zpotrf_one.restype = ctypes.c_int
+    lib.oracle_zpotrf_one.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_void_p, ctypes.c_int]
+    g = np.random.default_rng(5)
+    Lz = np.tril(g.integers(-2 ** 13, 2 ** 13, (8, 8)) + 1j * g.integers(-2 ** 13, 2 ** 13, (8, 8)), -1)
+    Lz[np.diag_indices(8)] = g.integers(1, 2 ** 13, 8)
+    az = np.asfortranarray(Lz @ Lz.conj().T)
+    Fz = np.zeros((8, 8), dtype=np.complex128, order="F")
+    if lib.oracle_zpotrf_one(az.ctypes.data, 8, 8, Fz.ctypes.data, 8) != 0 or \
+            not np.array_equal(np.ascontiguousarray(Fz), Lz):
+        failed.append("integer double complex")
     return failed
 
 
