@@ -260,6 +260,17 @@ int bl_cpotrf_batched_uplo(char uplo, float *A, int n, int lda, int64_t strideA,
                            int *info, cudaStream_t stream);
 
 /*
+ * bl_zpotrf_batched / bl_zpotrf_batched_uplo - the same for a
+ * double-precision complex batch (ZPOTRF): A points at interleaved complex
+ * doubles (std::complex<double> / cuDoubleComplex), 16-byte aligned (else -1,
+ * or -2 for the uplo form); everything else as bl_cpotrf_batched.
+ */
+int bl_zpotrf_batched(double *A, int n, int lda, int64_t strideA, int batch, int *info,
+                      cudaStream_t stream);
+int bl_zpotrf_batched_uplo(char uplo, double *A, int n, int lda, int64_t strideA, int batch,
+                           int *info, cudaStream_t stream);
+
+/*
  * bl_fma_probe - the FMA throughput this device reaches (TFLOP/s, 2 flops an
  * FMA) with eight independent FMA chains a thread, 256 threads a block and
  * eight blocks an SM: the compute peak the factorizations are read against

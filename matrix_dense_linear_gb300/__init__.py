@@ -40,6 +40,8 @@ SYMBOLS = {
     "bl_fma_probe": (_I, [_I, _VP, _VP, _VP]),
     "bl_cpotrf_batched": (_I, [_VP, _I, _I, _I64, _I, _VP, _VP]),
     "bl_cpotrf_batched_uplo": (_I, [_C, _VP, _I, _I, _I64, _I, _VP, _VP]),
+    "bl_zpotrf_batched": (_I, [_VP, _I, _I, _I64, _I, _VP, _VP]),
+    "bl_zpotrf_batched_uplo": (_I, [_C, _VP, _I, _I, _I64, _I, _VP, _VP]),
     "bl_dpotrf_batched_uplo": (_I, [_C, _VP, _I, _I, _I64, _I, _VP, _VP]),
     "bl_spotrf_batched_uplo_ex": (_I, [_C, _VP, _I, _I, _I64, _I, _VP, _VP, _I]),
     "bl_spotrs_batched_uplo": (_I, [_C, _VP, _I, _I, _I64, _VP, _I, _I, _I64, _I, _VP]),
@@ -145,18 +147,23 @@ def dpotrf_batched(A, n: int, lda: int, strideA: int, batch: int, info, stream=N
 
 
 def cpotrf_batched(A, n: int, lda: int, strideA: int, batch: int, info, stream=None,
-                   uplo="L") -> int:
-    """bl_cpotrf_batched(_uplo): A is a complex64 device tensor (or pointer)."""
+                   uplo="L", double: Optional[bool] = None) -> int:
+    """bl_cpotrf_batched(_uplo), or bl_zpotrf_batched(_uplo) for a complex128
+    tensor (or with double=True for a raw pointer): A is a complex device
+    tensor (or pointer)."""
+    if double is None:
+        double = str(getattr(A, "dtype", "")) == "torch.complex128"
+    lib = library()
     if uplo in ("L", b"L"):
-        return library().bl_cpotrf_batched(_ptr(A), n, lda, strideA, batch, _ptr(info),
-                                           _stream(stream))
-    return library().bl_cpotrf_batched_uplo(_uplo(uplo), _ptr(A), n, lda, strideA, batch,
-                                            _ptr(info), _stream(stream))
+        fn = lib.bl_zpotrf_batched if double else lib.bl_cpotrf_batched
+        return fn(_ptr(A), n, lda, strideA, batch, _ptr(info), _stream(stream))
+    fn = lib.bl_zpotrf_batched_uplo if double else lib.bl_cpotrf_batched_uplo
+    return fn(_uplo(uplo), _ptr(A), n, lda, strideA, batch, _ptr(info), _stream(stream))
 
 
 def factor_complex(A, n: int, lda: int, strideA: int, batch: int, info, stream=None,
                    uplo="L") -> None:
-    """cpotrf_batched, raising BLError on a nonzero status."""
+    """cpotrf_batched (complex64 or complex128), raising BLError on a nonzero status."""
     code = cpotrf_batched(A, n, lda, strideA, batch, info, stream, uplo)
     if code:
         raise BLError(code, "cpotrf")

@@ -296,6 +296,29 @@ int bl_cpotrf_batched(float *A, int n, int lda, int64_t strideA, int batch, int 
     return e < 0 ? e + 1 : e;
 }
 
+int bl_zpotrf_batched_uplo(char uplo, double *A, int n, int lda, int64_t strideA, int batch,
+                           int *info, cudaStream_t stream)
+{
+    const int u = parse_uplo(uplo);
+    if (u < 0) return -1;
+    const int e = check_args(A, n, lda, strideA, batch, info);
+    if (e) return shift_arg(e);
+    if (batch > 0 && n > 0 && (reinterpret_cast<uintptr_t>(A) & 15) != 0) return -2;
+    if (batch == 0) return 0;
+    if (n == 0) return (int)cudaMemsetAsync(info, 0, sizeof(int) * (size_t)batch, stream);
+    if (trace_enabled())
+        std::fprintf(stderr, "bl_zpotrf: uplo=%c n=%d lda=%d strideA=%lld batch=%d\n",
+                     u ? 'U' : 'L', n, lda, (long long)strideA, batch);
+    return bl::launch_zpotrf(A, n, lda, strideA, batch, info, stream, u == 1);
+}
+
+int bl_zpotrf_batched(double *A, int n, int lda, int64_t strideA, int batch, int *info,
+                      cudaStream_t stream)
+{
+    const int e = bl_zpotrf_batched_uplo('L', A, n, lda, strideA, batch, info, stream);
+    return e < 0 ? e + 1 : e;
+}
+
 int bl_dpotrf_batched(double *A, int n, int lda, int64_t strideA, int batch, int *info,
                       cudaStream_t stream)
 {

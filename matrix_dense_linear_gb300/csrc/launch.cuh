@@ -41,6 +41,9 @@ int launch_dpotrf(double *A, int n, int lda, int64_t strideA, int batch, int *in
 // A: interleaved complex float (re, im); lda and strideA in complex elements
 int launch_cpotrf(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                   cudaStream_t stream, bool upper);
+// A: interleaved complex double; lda and strideA in complex elements
+int launch_zpotrf(double *A, int n, int lda, int64_t strideA, int batch, int *info,
+                  cudaStream_t stream, bool upper);
 int launch_potrs(const float *L, int n, int lda, int64_t strideA, float *B, int nrhs, int ldb,
                  int64_t strideB, int batch, const int *info, cudaStream_t stream, bool upper);
 int attrs_potrs(cudaFuncAttributes *fa, int *threads, int *dyn_smem);

@@ -1,5 +1,5 @@
-// DPOTRF and CPOTRF: batched Cholesky of double-precision real and
-// single-precision complex (Hermitian) batches, the operation of the
+// DPOTRF, CPOTRF and ZPOTRF: batched Cholesky of double-precision real and
+// single- and double-precision complex (Hermitian) batches, the operation of the
 // single-precision path (A = L L^T, or L L^H for complex; the upper storage
 // A = U^H U; info = first pivot with !(d > 0)). "BatchLAS perf_blackwell"
 // lists double and the complex types among the types of its batched potrf
@@ -9,7 +9,8 @@
 // library's FMA probe: 1.05 against 74.7 TFLOP/s), so a double factorization
 // is bound by its FMA count; the complex one is the same algorithm with
 // complex FMAs (four real ones each) on the FP32 pipes. The kernels are the
-// plain forms, one element type T (double or float2 = complex float) through
+// plain forms, one element type T (double, float2 or double2: complex float
+// or double) through
 // the small set of operations in Ar<T>, each doing only the FMAs of the lower
 // triangle, with IEEE square root and division:
 //   simple_potrf_kernel n <= 128 (and the 128 x 128 diagonal blocks of larger
@@ -17,8 +18,8 @@
 //                       right-looking column by column, the trailing
 //                       triangle spread evenly over the threads;
 //   simple_trsm_kernel  the panel solve of the blocked path, one thread per
-//                       row, L11 in shared memory, 32-column blocks (16 for
-//                       complex);
+//                       row, L11 packed in shared memory, 32-column blocks
+//                       (16 for complex);
 //   simple_syrk_kernel  its trailing update on 64 x 64 tiles on or below the
 //                       diagonal, k staged through shared memory.
 #include <mutex>
@@ -74,6 +75,28 @@ struct Ar<float2> {
     }
     __device__ static float2 sub(float2 c, float2 a) { return make_float2(c.x - a.x, c.y - a.y); }
     __device__ static R root(R d) { return sqrtf(d); }
+};
+
+template <>
+struct Ar<double2> {
+    using R = double;
+    __device__ static R re(double2 x) { return x.x; }
+    __device__ static double2 of_real(R r) { return make_double2(r, 0.0); }
+    __device__ static double2 zero() { return make_double2(0.0, 0.0); }
+    __device__ static double2 cj(double2 x) { return make_double2(x.x, -x.y); }
+    __device__ static double2 load(const double2 *p, bool up) { return up ? cj(*p) : *p; }
+    __device__ static void store(double2 *p, double2 v, bool up) { *p = up ? cj(v) : v; }
+    __device__ static double2 scale(double2 x, R s) { return make_double2(x.x * s, x.y * s); }
+    __device__ static double2 sub_mul_conj(double2 c, double2 a, double2 b)
+    {
+        return make_double2(fma(-a.x, b.x, fma(-a.y, b.y, c.x)), fma(-a.y, b.x, fma(a.x, b.y, c.y)));
+    }
+    __device__ static double2 add_mul_conj(double2 c, double2 a, double2 b)
+    {
+        return make_double2(fma(a.x, b.x, fma(a.y, b.y, c.x)), fma(a.y, b.x, fma(-a.x, b.y, c.y)));
+    }
+    __device__ static double2 sub(double2 c, double2 a) { return make_double2(c.x - a.x, c.y - a.y); }
+    __device__ static R root(R d) { return sqrt(d); }
 };
 
 constexpr int kDNb = 128;    // panel width of the blocked path
@@ -178,7 +201,7 @@ simple_trsm_kernel(T *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     using X = Ar<T>;
     using R = typename X::R;
     extern __shared__ __align__(16) uint8_t sraw[];
-    T *Ld = reinterpret_cast<T *>(sraw);  // Ld[i + k * 128] = L11(i, k), i >= k
+    T *Ld = reinterpret_cast<T *>(sraw);  // Ld[pk(i, k, 128)] = L11(i, k), i >= k (packed)
     __shared__ R rdiag[kDNb];             // 1 / L11(j, j)
     const int64_t mat = blockIdx.x;
     if (info[mat] != 0) return;
@@ -186,15 +209,15 @@ simple_trsm_kernel(T *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     const int tid = threadIdx.x;
     for (int k = 0; k < kDNb; ++k)
         for (int i = k + tid; i < kDNb; i += blockDim.x)
-            Ld[i + k * kDNb] = X::load(Ab + lidx<UP>(c0 + i, c0 + k, lda), UP);
+            Ld[pk(i, k, kDNb)] = X::load(Ab + lidx<UP>(c0 + i, c0 + k, lda), UP);
     __syncthreads();
-    for (int j = tid; j < kDNb; j += blockDim.x) rdiag[j] = R(1) / X::re(Ld[j + j * kDNb]);
+    for (int j = tid; j < kDNb; j += blockDim.x) rdiag[j] = R(1) / X::re(Ld[pk(j, j, kDNb)]);
     __syncthreads();
     const int row = c0 + kDNb + blockIdx.y * blockDim.x + tid;
     if (row >= n) return;
     // x L11^H = a, row by row: x_c = (a_c - sum_{k<c} x_k conj(l_ck)) / l_cc,
     // W columns at a time (16 for complex T, which keeps x in registers)
-    constexpr int W = std::is_same<T, float2>::value ? 16 : 32;
+    constexpr int W = std::is_same<T, double>::value ? 32 : 16;  // complex: 16
     T *Xr = Ab + lidx<UP>(row, c0, lda);  // Xr[k * xs] = element (row, c0 + k)
     const int64_t xs = UP ? 1 : lda;
 #pragma unroll 1
@@ -205,7 +228,7 @@ simple_trsm_kernel(T *__restrict__ A, int n, int lda, int64_t strideA, int c0,
 #pragma unroll 1
         for (int kk = 0; kk < W * jb; ++kk) {
             const T xk = X::load(Xr + (int64_t)kk * xs, UP);  // solved
-            const T *Lrow = Ld + W * jb + kk * kDNb;          // L11(W jb + c, kk)
+            const T *Lrow = Ld + pk(W * jb, kk, kDNb);        // Lrow[c] = L11(W jb + c, kk)
 #pragma unroll
             for (int c = 0; c < W; ++c) x[c] = X::sub_mul_conj(x[c], xk, Lrow[c]);
         }
@@ -215,7 +238,7 @@ simple_trsm_kernel(T *__restrict__ A, int n, int lda, int64_t strideA, int c0,
             x[c] = X::scale(x[c], rdiag[j]);
 #pragma unroll
             for (int t = c + 1; t < W; ++t)
-                x[t] = X::sub_mul_conj(x[t], x[c], Ld[W * jb + t + j * kDNb]);
+                x[t] = X::sub_mul_conj(x[t], x[c], Ld[pk(W * jb + t, j, kDNb)]);
         }
 #pragma unroll
         for (int c = 0; c < W; ++c) X::store(Xr + (int64_t)(W * jb + c) * xs, x[c], UP);
@@ -318,7 +341,7 @@ int launch_blocked_s(T *A, int n, int lda, int64_t strideA, int batch, int *info
     std::call_once(once, [] {
         attr = cudaFuncSetAttribute(simple_trsm_kernel<T, UP>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)(kDNb * kDNb * sizeof(T)));
+                                    (int)(kDNb * (kDNb + 1) / 2 * sizeof(T)));
     });
     if (attr != cudaSuccess) return (int)attr;
     for (int c0 = 0; c0 < n; c0 += kDNb) {
@@ -329,8 +352,8 @@ int launch_blocked_s(T *A, int n, int lda, int64_t strideA, int batch, int *info
         const int m = n - c0 - nb;
         if (m <= 0) break;
         dim3 gt((unsigned)batch, (unsigned)((m + 127) / 128));
-        simple_trsm_kernel<T, UP><<<gt, 128, kDNb * kDNb * sizeof(T), st>>>(A, n, lda, strideA,
-                                                                          c0, info);
+        simple_trsm_kernel<T, UP><<<gt, 128, kDNb * (kDNb + 1) / 2 * sizeof(T), st>>>(
+            A, n, lda, strideA, c0, info);
         if ((e = (int)cudaGetLastError())) return e;
         const int Tn = (m + kDTile - 1) / kDTile;
         dim3 gs((unsigned)batch, (unsigned)(Tn * (Tn + 1) / 2));
@@ -364,6 +387,13 @@ int launch_cpotrf(float *A, int n, int lda, int64_t strideA, int batch, int *inf
 {
     return launch_simple<float2>(reinterpret_cast<float2 *>(A), n, lda, strideA, batch, info,
                                  stream, upper);
+}
+
+int launch_zpotrf(double *A, int n, int lda, int64_t strideA, int batch, int *info,
+                  cudaStream_t stream, bool upper)
+{
+    return launch_simple<double2>(reinterpret_cast<double2 *>(A), n, lda, strideA, batch, info,
+                                  stream, upper);
 }
 
 }  // namespace bl

@@ -170,11 +170,15 @@ def test_cpotrf_argument_codes(bl):
     cases = [((8, -1, 1, 1, 1, 8), -2), ((8, 4, 4, 16, -1, 8), -5), ((8, 4, 3, 16, 2, 8), -3),
              ((8, 4, 4, 15, 2, 8), -4), ((None, 4, 4, 16, 2, 8), -1),
              ((8, 4, 4, 16, 2, None), -6), ((8, 4097, 4097, 4097 * 4097, 2, 8), -7),
-             ((12, 4, 4, 16, 2, 8), -1)]  # not 8-byte aligned
+             ((12, 4, 4, 16, 2, 8), -1)]  # not 8-byte aligned (the last case)
     for args, code in cases:
         assert lib.bl_cpotrf_batched(*args, None) == code
         assert lib.bl_cpotrf_batched_uplo(b"L", *args, None) == code - 1
     assert lib.bl_cpotrf_batched_uplo(b"?", 8, 4, 4, 16, 1, 8, None) == -1
+    for args, code in cases[:-1]:
+        assert lib.bl_zpotrf_batched(*args, None) == code
+        assert lib.bl_zpotrf_batched_uplo(b"U", *args, None) == code - 1
+    assert lib.bl_zpotrf_batched(8, 4, 4, 16, 2, 8, None) == -1  # not 16-byte aligned
 
 
 def test_forced_route_that_cannot_run(bl):

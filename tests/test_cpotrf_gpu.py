@@ -1,12 +1,14 @@
-"""Parity of the complex Hermitian factorization (CPOTRF) with the complex
-oracle, through the C-ABI (GPU).
+"""Parity of the complex Hermitian factorizations (CPOTRF, ZPOTRF) with the
+complex oracle, through the C-ABI (GPU).
 
-The single-precision bars of the real path, in complex arithmetic: info
-bit-exact; max|L - L_oracle| / max|L_oracle| <= 1e-5 n; the reconstruction
-||L L^H - A||_F / ||A||_F <= 2.38e-6 n over the full Hermitian matrix the
-stored triangle defines (diagonal: its real part); everything outside the
-factored triangle (NaN-poisoned) bitwise unchanged; the diagonal's imaginary
-part is not read.
+CPOTRF takes the single-precision bars of the real path in complex
+arithmetic: info bit-exact; max|L - L_oracle| / max|L_oracle| <= 1e-5 n; the
+reconstruction ||L L^H - A||_F / ||A||_F <= 2.38e-6 n over the full Hermitian
+matrix the stored triangle defines (diagonal: its real part). ZPOTRF takes
+them rescaled from u32 = 2^-24 to u64 = 2^-53, the reconstruction evaluated
+in extended precision. Everything outside the factored triangle
+(NaN-poisoned) comes back bitwise unchanged; the diagonal's imaginary part
+is not read.
 """
 from __future__ import annotations
 
@@ -17,6 +19,11 @@ import oracle
 from tests import checks
 
 pytestmark = pytest.mark.gpu
+
+U64, U32 = 2.0 ** -53, 2.0 ** -24
+BARS = {"c64": (checks.MAXREL_PER_N, checks.RECON_PER_N),
+        "c128": (checks.MAXREL_PER_N * U64 / U32, 20 * U64)}
+DT = {"c64": np.complex64, "c128": np.complex128}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -32,12 +39,12 @@ def _herm(n, seed):
     return 0.5 * (A + A.conj().T)
 
 
-def _pack(mats, n, lda, strideA, uplo, diag_imag=0.0):
+def _pack(mats, n, lda, strideA, uplo, diag_imag=0.0, dt="c64"):
     batch = len(mats)
     buf = np.full(max((batch - 1) * strideA + lda * n, 1), np.nan + 1j * np.nan,
-                  dtype=np.complex64)
+                  dtype=DT[dt])
     for b, M in enumerate(mats):
-        M = np.array(M, dtype=np.complex64)
+        M = np.array(M, dtype=DT[dt])
         M[np.diag_indices(n)] = M[np.diag_indices(n)].real + 1j * diag_imag
         for j in range(n):
             s0 = b * strideA + j * lda
@@ -77,8 +84,13 @@ def _slot(buf, n, lda, strideA, b):
 
 
 def _check(buf, out, info, n, lda, strideA, batch, uplo, what):
+    dt = "c128" if buf.dtype == np.complex128 else "c64"
+    maxrel, recon = BARS[dt]
     pat = _pattern(n, lda, strideA, batch, buf.size, uplo)
-    assert np.array_equal(out.view(np.uint64)[~pat], buf.view(np.uint64)[~pat]), what
+    ov, bv = out.view(np.uint64), buf.view(np.uint64)
+    if dt == "c128":  # two 64-bit words an element
+        pat = np.repeat(pat, 2)
+    assert np.array_equal(ov[~pat], bv[~pat]), what
     F, iref, _ = oracle.cpotrf_batched(buf, n, lda, strideA, batch, uplo=uplo)
     assert np.array_equal(info, iref), (what, info, iref)
     for b in range(batch):
@@ -89,30 +101,37 @@ def _check(buf, out, info, n, lda, strideA, batch, uplo, what):
         if k == 0:
             continue
         e = np.abs(L[:k, :k] - R[:k, :k]).max() / np.abs(R[:k, :k]).max()
-        assert e <= checks.MAXREL_PER_N * k, (what, b, e)
+        assert e <= maxrel * k, (what, b, e)
         if iref[b]:
             continue
         Ain = _slot(buf, n, lda, strideA, b).astype(np.complex128)
         low = np.tril(Ain) if uplo == "L" else np.triu(Ain).conj().T
         Ah = np.tril(low, -1) + np.tril(low, -1).conj().T + np.diag(low.diagonal().real)
         assert np.abs(np.diag(L).imag).max() == 0.0, (what, b, "complex diagonal")
-        r = np.linalg.norm(L @ L.conj().T - Ah) / np.linalg.norm(Ah)
-        assert r <= checks.RECON_PER_N * n, (what, b, r)
+        if dt == "c64":
+            r = np.linalg.norm(L @ L.conj().T - Ah) / np.linalg.norm(Ah)
+        else:
+            Lq, Aq = L.astype(np.clongdouble), Ah.astype(np.clongdouble)
+            Rq = Lq @ Lq.conj().T - Aq
+            r = float(np.sqrt((np.abs(Rq) ** 2).sum() / (np.abs(Aq) ** 2).sum()))
+        assert r <= recon * n, (what, b, r)
 
 
 @pytest.mark.parametrize("n", [1, 2, 5, 16, 31, 32, 33, 64, 100, 128, 129, 200, 256, 300])
 @pytest.mark.parametrize("uplo", ["L", "U"])
-def test_cpotrf_parity(n, uplo):
+@pytest.mark.parametrize("dt", ["c64", "c128"])
+def test_cpotrf_parity(n, uplo, dt):
     batch = 6 if n <= 128 else 3
     mats = [_herm(n, 2000 + 10 * n + b) for b in range(batch)]
     for lda, strideA in ((n, n * n), (n + 3, (n + 3) * n + 5)):
-        buf = _pack(mats, n, lda, strideA, uplo, diag_imag=0.25)
+        buf = _pack(mats, n, lda, strideA, uplo, diag_imag=0.25, dt=dt)
         out, info = _run(buf, n, lda, strideA, batch, uplo)
         _check(buf, out, info, n, lda, strideA, batch, uplo, f"n={n} lda={lda} {uplo}")
 
 
 @pytest.mark.parametrize("n", [8, 64, 128, 200])
-def test_cpotrf_info(n):
+@pytest.mark.parametrize("dt", ["c64", "c128"])
+def test_cpotrf_info(n, dt):
     g = np.random.default_rng(n)
     ks = [0, n - 1, n // 2, int(g.integers(0, n))]
     mats = [_herm(n, 2500 + 10 * n + b) for b in range(6)]
@@ -121,10 +140,10 @@ def test_cpotrf_info(n):
         q = (A[:k, k].conj() @ np.linalg.solve(A[:k, :k], A[:k, k])).real if k else 0.0
         A[k, k] = q - 0.5
     for uplo in ("L", "U"):
-        buf = _pack(mats, n, n, n * n, uplo)
+        buf = _pack(mats, n, n, n * n, uplo, dt=dt)
         out, info = _run(buf, n, n, n * n, 6, uplo)
         assert list(info[:4]) == [k + 1 for k in ks] and info[4] == 0 and info[5] == 0
-        _check(buf, out, info, n, n, n * n, 6, uplo, f"info n={n} {uplo}")
+        _check(buf, out, info, n, n, n * n, 6, uplo, f"info n={n} {uplo} {dt}")
 
 
 def test_cpotrf_real_input_matches_spotrf():
@@ -164,3 +183,6 @@ def test_cpotrf_codes():
     # a 4-byte-aligned (not 8) address is refused before any launch
     assert bl.cpotrf_batched(A.data_ptr() + 4, 2, 2, 4, 1, info) == -1
     assert bl.cpotrf_batched(A.data_ptr() + 4, 2, 2, 4, 1, info, uplo="U") == -2
+    Z = torch.zeros(4, dtype=torch.complex128, device="cuda")
+    assert bl.cpotrf_batched(Z.data_ptr() + 8, 2, 2, 4, 1, info, double=True) == -1
+    assert bl.cpotrf_batched(Z, 2, 1, 4, 1, info) == -3
