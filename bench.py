@@ -622,19 +622,20 @@ FP64_PEAK_TFLOPS = 1.25
 
 
 def run_shapes_f64(args) -> list:
-    """--shapes with --dtype f64 or c64: the double-precision (DPOTRF) or the
-    complex Hermitian (CPOTRF) factorization of A = G G^H / n + I (G iid
-    normal, complex for c64; 64 distinct matrices repeated), the same timing
-    as run_shapes; f64 against the measured FP64 rate, c64 (4 n^3 / 3 real
-    flops a matrix) against the FP32 roofline."""
+    """--shapes with --dtype f64, c64 or c128: the double-precision (DPOTRF)
+    or the complex Hermitian (CPOTRF, ZPOTRF) factorization of
+    A = G G^H / n + I (G iid normal, complex for c64 / c128; 64 distinct
+    matrices repeated), the same timing as run_shapes; f64 and c128 against
+    the measured FP64 rate, c64 against the FP32 roofline (complex: 4 n^3 / 3
+    real flops a matrix)."""
     import torch
 
     import matrix_dense_linear_gb300 as bl
     import synth
     bl.library()
     dev = torch.device("cuda", 0)
-    cplx = args.dtype == "c64"
-    if cplx:
+    cplx = args.dtype in ("c64", "c128")
+    if args.dtype == "c64":
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         peak = sms * 128 * 2 * peaks()["sm_max_mhz"] * 1e6 / 1e12
         peak_src = "FP32: SMs x 128 FMA x 2 x max clock"
@@ -654,14 +655,15 @@ def run_shapes_f64(args) -> list:
             for b in range(distinct):
                 g = synth.rng(7, b)
                 G = g.standard_normal((n, n)) + 1j * g.standard_normal((n, n))
-                mats.append((G @ G.conj().T / n + np.eye(n)).astype(np.complex64))
+                mats.append((G @ G.conj().T / n + np.eye(n)).astype(
+                    np.complex64 if args.dtype == "c64" else np.complex128))
         else:
             mats = [synth.gram(n, synth.rng(6, b), "normal", float(n), 1.0)
                     for b in range(distinct)]
         one = np.concatenate([np.asfortranarray(m).ravel(order="F") for m in mats])
         buf = np.tile(one, -(-batch // distinct))[: batch * n * n]
         src = torch.from_numpy(np.ascontiguousarray(buf)).to(dev)
-        nbytes = src.numel() * 8
+        nbytes = src.numel() * src.element_size()
         nrep = int(max(1, min(max(args.steps, -(-2 * l2 // nbytes)),
                               REPLICA_CAP_BYTES // max(nbytes, 1))))
         reps = torch.empty((nrep, src.numel()), dtype=src.dtype, device=dev)
@@ -846,8 +848,9 @@ def main():
     ap.add_argument("--shapes", default=None, metavar="NxB,...",
                     help="time these (n, batch) shapes (one JSON line each); 'pages' = "
                          "the shapes the pages quote timings for")
-    ap.add_argument("--dtype", choices=["f32", "f64", "c64"], default="f32",
-                    help="f64 / c64: time the double / complex factorization for --shapes")
+    ap.add_argument("--dtype", choices=["f32", "f64", "c64", "c128"], default="f32",
+                    help="f64 / c64 / c128: time the double / complex / double complex "
+                         "factorization for --shapes")
     ap.add_argument("--uplo", choices=["L", "U"], default="L",
                     help="storage of the factor for --shapes (U: upper triangle)")
     args = ap.parse_args()
@@ -863,7 +866,7 @@ def main():
     if args.shapes:
         if args.shapes == "pages":
             args.shapes = PAGES_SHAPES
-        if args.dtype in ("f64", "c64"):
+        if args.dtype in ("f64", "c64", "c128"):
             run_shapes_f64(args)
         else:
             run_shapes(args)

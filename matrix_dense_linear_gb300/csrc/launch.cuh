@@ -39,6 +39,9 @@ int launch_trsm_tc(float *A, int n, int lda, int64_t strideA, int batch, int *in
 int launch_dpotrf(double *A, int n, int lda, int64_t strideA, int batch, int *info,
                   cudaStream_t stream, bool upper);
 // A: interleaved complex float (re, im); lda and strideA in complex elements
+// CPOTRF for n <= 32: one group of n-rounded-up lanes per matrix, in registers
+int launch_cpotrf_warp(float *A, int n, int lda, int64_t strideA, int batch, int *info,
+                       cudaStream_t stream, bool upper);
 int launch_cpotrf(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                   cudaStream_t stream, bool upper);
 // A: interleaved complex double; lda and strideA in complex elements

@@ -129,7 +129,21 @@ def test_cpotrf_parity(n, uplo, dt):
         _check(buf, out, info, n, lda, strideA, batch, uplo, f"n={n} lda={lda} {uplo}")
 
 
-@pytest.mark.parametrize("n", [8, 64, 128, 200])
+@pytest.mark.parametrize("n", [3, 8, 9, 16, 20, 32])
+@pytest.mark.parametrize("uplo", ["L", "U"])
+def test_cpotrf_small_orders_ragged_batch(n, uplo):
+    """Orders of the register kernel (several matrices a warp below 17) over a
+    batch that leaves the last warp partly empty, with a padded lda and gaps."""
+    batch = 301
+    mats = [_herm(n, 3100 + 7 * n + b) for b in range(batch)]
+    lda = n + 1
+    strideA = lda * n + 3
+    buf = _pack(mats, n, lda, strideA, uplo, diag_imag=-1.5)
+    out, info = _run(buf, n, lda, strideA, batch, uplo)
+    _check(buf, out, info, n, lda, strideA, batch, uplo, f"ragged n={n} {uplo}")
+
+
+@pytest.mark.parametrize("n", [8, 20, 32, 64, 128, 200])
 @pytest.mark.parametrize("dt", ["c64", "c128"])
 def test_cpotrf_info(n, dt):
     g = np.random.default_rng(n)
