@@ -39,7 +39,8 @@ int launch_trsm_tc(float *A, int n, int lda, int64_t strideA, int batch, int *in
 int launch_dpotrf(double *A, int n, int lda, int64_t strideA, int batch, int *info,
                   cudaStream_t stream, bool upper);
 // A: interleaved complex float (re, im); lda and strideA in complex elements
-// CPOTRF for n <= 32: one group of n-rounded-up lanes per matrix, in registers
+// CPOTRF for n <= 64 in registers: a lane per row (n <= 32: 1, 2 or 4 matrices a warp;
+// above: two warps a matrix)
 int launch_cpotrf_warp(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                        cudaStream_t stream, bool upper);
 int launch_cpotrf(float *A, int n, int lda, int64_t strideA, int batch, int *info,
