@@ -43,10 +43,10 @@ REPLICA_CAP_BYTES = 96 << 30
 TRAFFIC = {
     # workload: (source files, sha256 prefix over them, bytes per launch, summary file)
     "n32": (("matrix_dense_linear_gb300/csrc/potrf_warp.cu",
-             "matrix_dense_linear_gb300/csrc/bl_common.cuh"), "cfa6b0f5864f3acd", 4219904,
+             "matrix_dense_linear_gb300/csrc/bl_common.cuh"), "e7bebddfc929997e", 4219904,
             "profiles/potrf_warp_n32_b1024.md"),
     "n64": (("matrix_dense_linear_gb300/csrc/potrf_warp.cu",
-             "matrix_dense_linear_gb300/csrc/bl_common.cuh"), "cfa6b0f5864f3acd", 12660224,
+             "matrix_dense_linear_gb300/csrc/bl_common.cuh"), "e7bebddfc929997e", 12660480,
             "profiles/potrf_warp64_n64_b1024.md"),
 }
 
