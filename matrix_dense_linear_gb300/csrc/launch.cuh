@@ -43,6 +43,12 @@ int launch_dpotrf(double *A, int n, int lda, int64_t strideA, int batch, int *in
 // above: two warps a matrix)
 int launch_cpotrf_warp(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                        cudaStream_t stream, bool upper);
+// CPOTRF for 64 < n <= 128: a warp per 32 x 32 tile of the lower triangle
+int launch_cpotrf_tiles(float *A, int n, int lda, int64_t strideA, int batch, int *info,
+                        cudaStream_t stream, bool upper);
+// the same schedule on real input (64 < n <= 128), a measured alternative to K2
+int launch_spotrf_tiles(float *A, int n, int lda, int64_t strideA, int batch, int *info,
+                        cudaStream_t stream, bool upper);
 int launch_cpotrf(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                   cudaStream_t stream, bool upper);
 // A: interleaved complex double; lda and strideA in complex elements

@@ -386,6 +386,7 @@ int launch_cpotrf(float *A, int n, int lda, int64_t strideA, int batch, int *inf
                   cudaStream_t stream, bool upper)
 {
     if (n <= 64) return launch_cpotrf_warp(A, n, lda, strideA, batch, info, stream, upper);
+    if (n <= 128) return launch_cpotrf_tiles(A, n, lda, strideA, batch, info, stream, upper);
     return launch_simple<float2>(reinterpret_cast<float2 *>(A), n, lda, strideA, batch, info,
                                  stream, upper);
 }

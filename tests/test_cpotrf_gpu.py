@@ -129,12 +129,12 @@ def test_cpotrf_parity(n, uplo, dt):
         _check(buf, out, info, n, lda, strideA, batch, uplo, f"n={n} lda={lda} {uplo}")
 
 
-@pytest.mark.parametrize("n", [3, 8, 9, 16, 20, 32, 33, 48, 64])
+@pytest.mark.parametrize("n", [3, 8, 9, 16, 20, 32, 33, 48, 64, 65, 96, 97, 128])
 @pytest.mark.parametrize("uplo", ["L", "U"])
 def test_cpotrf_small_orders_ragged_batch(n, uplo):
     """Orders of the register kernels (several matrices a warp below 17, two
-    warps a matrix above 32) over a batch that leaves the last warp partly
-    empty, with a padded lda and gaps."""
+    warps a matrix above 32, a warp per 32 x 32 tile above 64) over a batch
+    that leaves the last warp partly empty, with a padded lda and gaps."""
     batch = 301
     mats = [_herm(n, 3100 + 7 * n + b) for b in range(batch)]
     lda = n + 1
