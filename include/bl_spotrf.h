@@ -46,7 +46,9 @@ extern "C" {
 /* Route numbers of bl_spotrf_batched_ex and bl_spotrf_route. */
 #define BL_ROUTE_AUTO 0
 #define BL_ROUTE_WARP 1     /* K1: one warp (or a 16/8-lane group) per matrix, n <= 64 */
-#define BL_ROUTE_CTA 2      /* K2: one thread block per matrix, shared-memory resident, n <= 128 */
+#define BL_ROUTE_CTA 2      /* one thread block per matrix, n <= 128: K2 (shared-memory
+                               resident, bulk copies) for n <= 64 and the aligned orders
+                               96 and 128, else a warp per 32 x 32 tile in registers */
 #define BL_ROUTE_BLOCKED 3  /* K3: right-looking blocked, 128-wide panels: diagonal factor,
                                panel triangular solve, lower-only trailing update, any n */
 #define BL_ROUTE_TMEM 4     /* K2t: one thread block per matrix, the matrix resident in tensor
@@ -107,7 +109,9 @@ int bl_spotrf_route(int n, int batch);
 
 /*
  * bl_spotrf_kernel_info - static resources of the kernel that `route` uses at
- * order n, as the CUDA runtime reports them (registers per thread, local
+ * order n on a 16-byte-aligned batch (route 2 at 64 < n <= 128: the
+ * warp-per-tile kernel except at n = 96 and 128, where the shared-memory
+ * block kernel runs), as the CUDA runtime reports them (registers per thread, local
  * memory bytes per thread, static shared bytes, dynamic shared bytes the
  * launch asks for, threads per block). Any output pointer may be NULL.
  * Needs a CUDA device. Returns 0, -8 for a route that cannot run n, or a

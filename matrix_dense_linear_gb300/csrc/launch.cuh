@@ -49,6 +49,7 @@ int launch_cpotrf_tiles(float *A, int n, int lda, int64_t strideA, int batch, in
 // the same schedule on real input (64 < n <= 128), a measured alternative to K2
 int launch_spotrf_tiles(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                         cudaStream_t stream, bool upper);
+int attrs_tiles(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem);
 int launch_cpotrf(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                   cudaStream_t stream, bool upper);
 // A: interleaved complex double; lda and strideA in complex elements

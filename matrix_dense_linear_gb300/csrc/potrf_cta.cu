@@ -369,8 +369,10 @@ int launch_cta(float *A, int n, int lda, int64_t strideA, int batch, int *info,
     return launch_nb<4, 128>(A, n, lda, strideA, batch, info, stream, o, upper, nb);
 }
 
+// the kernel route 2 runs for this n on an aligned batch
 int attrs_cta(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem)
 {
+    if (n > 64 && n != 96 && n != 128) return attrs_tiles(n, fa, threads, dyn_smem);
     if (n <= 32) return attrs_nb<1, 32>(fa, threads, dyn_smem);
     if (n <= 64) return attrs_nb<2, 64>(fa, threads, dyn_smem);
     if (n <= 96) return attrs_nb<3, 128>(fa, threads, dyn_smem);

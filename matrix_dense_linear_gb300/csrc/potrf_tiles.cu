@@ -242,4 +242,16 @@ int launch_spotrf_tiles(float *A, int n, int lda, int64_t strideA, int batch, in
     return launch_tiles(A, n, lda, strideA, batch, info, stream, upper);
 }
 
+int attrs_tiles(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem)
+{
+    if (n <= 96) {
+        *threads = TileGeom<float, 3>::kThreads;
+        *dyn_smem = (int)TileGeom<float, 3>::kBytes;
+        return (int)cudaFuncGetAttributes(fa, potrf_tiles_kernel<float, 3, false>);
+    }
+    *threads = TileGeom<float, 4>::kThreads;
+    *dyn_smem = (int)TileGeom<float, 4>::kBytes;
+    return (int)cudaFuncGetAttributes(fa, potrf_tiles_kernel<float, 4, false>);
+}
+
 }  // namespace bl

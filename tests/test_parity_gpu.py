@@ -328,7 +328,8 @@ def test_concurrent_calls_from_host_threads():
 
 
 @pytest.mark.parametrize("route,n", [(1, 8), (1, 16), (1, 32), (1, 64), (2, 32), (2, 64),
-                                     (2, 96), (2, 128), (3, 256), (4, 100), (4, 128)])
+                                     (2, 80), (2, 96), (2, 100), (2, 128), (3, 256), (4, 100),
+                                     (4, 128)])
 def test_kernels_use_no_local_memory(route, n):
     import matrix_dense_linear_gb300 as bl
     ki = bl.kernel_info(route, n)
