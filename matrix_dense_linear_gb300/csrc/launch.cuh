@@ -5,7 +5,31 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace bl {
+
+// One-time setup per device (a kernel's function attributes belong to the
+// context of the device they were set on): run(f) calls f once for the
+// current device and returns its result there on every call.
+class DeviceOnce {
+public:
+    template <typename F>
+    int run(F &&f)
+    {
+        int dev = 0;
+        const cudaError_t g = cudaGetDevice(&dev);
+        if (g != cudaSuccess) return (int)g;
+        if (dev < 0 || dev >= kMaxDevices) return (int)cudaErrorInvalidDevice;
+        std::call_once(flag_[dev], [&] { err_[dev] = f(); });
+        return (int)err_[dev];
+    }
+
+private:
+    static constexpr int kMaxDevices = 64;
+    std::once_flag flag_[kMaxDevices];
+    cudaError_t err_[kMaxDevices] = {};
+};
 
 // info handling of one launch over a strided batch.
 //   info_off < 0 : the launch factors whole matrices and writes info[b]

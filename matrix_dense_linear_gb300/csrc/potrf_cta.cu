@@ -310,13 +310,12 @@ int launch_v(float *A, int n, int lda, int64_t strideA, int batch, int *info, cu
              int info_off)
 {
     constexpr int bytes = CtaGeom<NB>::bytes;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(potrf_cta_kernel<NB, NT, FULL, UP>,
+    static DeviceOnce attrs;
+    if (const int e = attrs.run([] {
+            return cudaFuncSetAttribute(potrf_cta_kernel<NB, NT, FULL, UP>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    });
-    if (attr_err != cudaSuccess) return (int)attr_err;
+        }))
+        return e;
     return launch_pdl(potrf_cta_kernel<NB, NT, FULL, UP>, dim3((unsigned)batch), dim3(NT),
                       (size_t)bytes, st, A, n, lda, strideA, batch, info, info_off);
 }

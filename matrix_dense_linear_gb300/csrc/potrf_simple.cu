@@ -316,14 +316,13 @@ template <typename T, bool UP>
 int launch_cta_s(T *A, int n, int lda, int64_t strideA, int batch, int *info, cudaStream_t st,
                  int info_off)
 {
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(simple_potrf_kernel<T, UP>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)(kDNb * (kDNb + 1) / 2 * sizeof(T)));
-    });
-    if (attr != cudaSuccess) return (int)attr;
+    static DeviceOnce attrs;
+    if (const int e = attrs.run([] {
+            return cudaFuncSetAttribute(simple_potrf_kernel<T, UP>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)(kDNb * (kDNb + 1) / 2 * sizeof(T)));
+        }))
+        return e;
     const size_t smem = (size_t)n * (n + 1) / 2 * sizeof(T);
     // four threads a row pair: 2n threads (a multiple of 32, at most 256)
     const int threads = 2 * n < 32 ? 32 : ((2 * n + 31) / 32) * 32;
@@ -336,14 +335,13 @@ template <typename T, bool UP>
 int launch_blocked_s(T *A, int n, int lda, int64_t strideA, int batch, int *info,
                      cudaStream_t st)
 {
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(simple_trsm_kernel<T, UP>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)(kDNb * (kDNb + 1) / 2 * sizeof(T)));
-    });
-    if (attr != cudaSuccess) return (int)attr;
+    static DeviceOnce attrs;
+    if (const int e = attrs.run([] {
+            return cudaFuncSetAttribute(simple_trsm_kernel<T, UP>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)(kDNb * (kDNb + 1) / 2 * sizeof(T)));
+        }))
+        return e;
     for (int c0 = 0; c0 < n; c0 += kDNb) {
         const int nb = n - c0 < kDNb ? n - c0 : kDNb;
         int e = launch_cta_s<T, UP>(A + c0 + (int64_t)c0 * lda, nb, lda, strideA, batch, info,

@@ -204,13 +204,13 @@ template <typename T, int NT, bool UP>
 int launch_t(T *A, int n, int lda, int64_t strideA, int batch, int *info, cudaStream_t st)
 {
     using Gm = TileGeom<T, NT>;
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(potrf_tiles_kernel<T, NT, UP>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Gm::kBytes);
-    });
-    if (attr != cudaSuccess) return (int)attr;
+    static DeviceOnce attrs;
+    if (const int e = attrs.run([] {
+            return cudaFuncSetAttribute(potrf_tiles_kernel<T, NT, UP>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)Gm::kBytes);
+        }))
+        return e;
     return launch_pdl(potrf_tiles_kernel<T, NT, UP>, dim3((unsigned)batch), dim3(Gm::kThreads),
                       Gm::kBytes, st, A, n, lda, strideA, batch, info);
 }

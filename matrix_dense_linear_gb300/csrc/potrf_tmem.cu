@@ -296,19 +296,18 @@ potrf_tmem_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int ba
     }
 }
 
-std::once_flag g_once;
-cudaError_t g_attr = cudaSuccess;
+DeviceOnce g_attrs;
 
 }  // namespace
 
 int launch_tmem(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                 cudaStream_t stream, InfoMode mode)
 {
-    std::call_once(g_once, [] {
-        g_attr = cudaFuncSetAttribute(potrf_tmem_kernel,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    });
-    if (g_attr != cudaSuccess) return (int)g_attr;
+    if (const int e = g_attrs.run([] {
+            return cudaFuncSetAttribute(potrf_tmem_kernel,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        }))
+        return e;
     potrf_tmem_kernel<<<(unsigned)batch, 128, kSmemBytes, stream>>>(A, n, lda, strideA, batch,
                                                                     info, mode.off);
     return (int)cudaGetLastError();

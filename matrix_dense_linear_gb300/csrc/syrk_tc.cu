@@ -274,13 +274,12 @@ template <bool UP>
 int launch_u(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
              cudaStream_t stream)
 {
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(syrk_tc_kernel<UP>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    });
-    if (attr != cudaSuccess) return (int)attr;
+    static DeviceOnce attrs;
+    if (const int e = attrs.run([] {
+            return cudaFuncSetAttribute(syrk_tc_kernel<UP>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        }))
+        return e;
     const int m = n - c0 - kNbTc;
     const int T = (m + 127) / 128;
     dim3 grid((unsigned)batch, (unsigned)(T * (T + 1) / 2));

@@ -346,13 +346,12 @@ int launch_k(float *A, int n, int lda, int64_t strideA, int batch, int *info, in
              cudaStream_t stream)
 {
     constexpr int smem = FUSED ? kSmemFused : kSmemBytes;
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(trsm_tc_kernel<UP, FUSED>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    });
-    if (attr != cudaSuccess) return (int)attr;
+    static DeviceOnce attrs;
+    if (const int e = attrs.run([] {
+            return cudaFuncSetAttribute(trsm_tc_kernel<UP, FUSED>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        }))
+        return e;
     const int m = n - c0 - 128;
     dim3 grid((unsigned)batch, (unsigned)((m + 127) / 128));
     trsm_tc_kernel<UP, FUSED><<<grid, 128, smem, stream>>>(A, n, lda, strideA, c0, info);
