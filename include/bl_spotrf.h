@@ -238,7 +238,11 @@ int bl_sposv_batched_uplo(char uplo, float *A, int n, int lda, int64_t strideA, 
  * returns, argument indices and their order, stream ordering, ownership) as
  * bl_spotrf_batched and bl_spotrf_batched_uplo. IEEE double arithmetic with
  * FMA contraction, IEEE square root and division. On GB300 the FP64 rate is
- * about 1/66 of the FP32 rate, so these calls are bound by their n^3/3 flops.
+ * about 1/70 of the FP32 rate (1.05 against 74.7 TFLOP/s by bl_fma_probe),
+ * so these calls are bound by their n^3/3 flops. "BatchLAS perf_blackwell"
+ * lists double, complex float and complex double among the element types of
+ * its batched potrf (the type columns of its potrf rows); these calls and the
+ * two below are those types.
  */
 int bl_dpotrf_batched(double *A, int n, int lda, int64_t strideA, int batch, int *info,
                       cudaStream_t stream);
