@@ -20,7 +20,9 @@
  * else untouched.
  *
  * info[b] = 0 when every pivot d_j was > 0, else the 1-based index j+1 of the
- * first pivot with !(d_j > 0) (a NaN pivot fails; +Inf passes). After a
+ * first pivot with !(d_j > 0) (a NaN pivot fails; +Inf passes; a positive
+ * pivot below FLT_MIN, a subnormal, is read as zero the way flush-to-zero
+ * single precision reads it, and fails). After a
  * failure at k = info[b] only the leading (k-1) x (k-1) block of L_b is
  * defined; the rest of that matrix's lower triangle is unspecified.
  * info[b] = -1 reports an internal error: a bounded wait inside a
@@ -289,6 +291,25 @@ int bl_zpotrf_batched_uplo(char uplo, double *A, int n, int lda, int64_t strideA
  * cudaError_t.
  */
 int bl_fma_probe(int precision, void *out, double *tflops, cudaStream_t stream);
+
+/*
+ * bl_debug_fail_first_wait - failure injection, for testing the internal-error
+ * path (info[b] = -1) only. While `every` > 0 for a kernel class, every block
+ * of that class on the current device whose matrix index b is a multiple of
+ * `every` reports its first bounded wait as timed out without waiting and
+ * takes the path a real timeout takes: it sets info[b] = -1, lets the copies
+ * and tensor-core operations it has already issued finish (bounded), releases
+ * its tensor memory and exits; later launches of the same call skip matrix b.
+ * Other matrices are factored as usual. every = 0 (the state at load) turns
+ * the injection off. Classes: 1 the shared-memory block
+ * kernel's bulk-copy load (route 2 at n = 96 and 128 on 16-byte-aligned
+ * batches, and the diagonal blocks of route 3), 2 the tensor-core panel solve
+ * and 3 the tensor-core trailing update (route 3 on 16-byte-aligned batches),
+ * 4 the tensor-memory kernel (route 4). Synchronous with the host; call it
+ * while no other work of the library runs. Returns 0, -1 (unknown class), -2
+ * (every < 0) or a cudaError_t.
+ */
+int bl_debug_fail_first_wait(int kernel_class, int every);
 
 /* Version string of the library ("bl_spotrf <major>.<minor> sm_103a"). */
 const char *bl_spotrf_version(void);

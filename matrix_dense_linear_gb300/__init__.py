@@ -46,6 +46,7 @@ SYMBOLS = {
     "bl_spotrf_batched_uplo_ex": (_I, [_C, _VP, _I, _I, _I64, _I, _VP, _VP, _I]),
     "bl_spotrs_batched_uplo": (_I, [_C, _VP, _I, _I, _I64, _VP, _I, _I, _I64, _I, _VP]),
     "bl_sposv_batched_uplo": (_I, [_C, _VP, _I, _I, _I64, _VP, _I, _I, _I64, _I, _VP, _VP]),
+    "bl_debug_fail_first_wait": (_I, [_I, _I]),
 }
 
 

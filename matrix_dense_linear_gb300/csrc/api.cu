@@ -377,6 +377,18 @@ int bl_spotrf_kernel_info(int route, int n, int *regs, int *local_bytes, int *st
     return 0;
 }
 
-const char *bl_spotrf_version(void) { return "bl_spotrf 0.1 sm_103a"; }
+int bl_debug_fail_first_wait(int kernel_class, int every)
+{
+    if (every < 0) return -2;
+    switch (kernel_class) {
+    case 1: return bl::set_fail_first_wait_cta(every);
+    case 2: return bl::set_fail_first_wait_trsm_tc(every);
+    case 3: return bl::set_fail_first_wait_syrk_tc(every);
+    case 4: return bl::set_fail_first_wait_tmem(every);
+    default: return -1;
+    }
+}
+
+const char *bl_spotrf_version(void) { return "bl_spotrf 0.2 sm_103a"; }
 
 }  // extern "C"

@@ -9,15 +9,41 @@ namespace bl {
 
 // Pivot test of batched SPOTRF: a pivot passes only when it is > 0, so zero,
 // negative and NaN pivots all fail (the first failure's 1-based index is info).
-__device__ __forceinline__ bool pivot_ok(float d) { return d > 0.0f; }
+// A positive pivot below FLT_MIN (a subnormal) fails too: the reciprocal root
+// below flushes it to zero, so it is a zero pivot in single precision, and a
+// matrix that reports info = 0 never carries the infinite root it would give.
+// One IEEE comparison: d >= FLT_MIN is false for subnormals, zero, negatives
+// and NaN, true for normal positive numbers and +Inf.
+__device__ __forceinline__ bool pivot_ok(float d) { return d >= 1.17549435e-38f; }
+
+// Whether the block's matrix has already failed (info[mat] != 0), read once
+// by thread 0 and shared through the block, so that every thread takes the
+// same branch even while a sibling block of the same matrix writes info[mat]
+// (a tile or row block that gave up sets it to -1). Every thread of the block
+// must call it (it contains a block barrier).
+__device__ __forceinline__ bool block_skip(const int *info, int64_t mat)
+{
+    __shared__ int flag;
+    if (threadIdx.x == 0) flag = *(volatile const int *)(info + mat);
+    __syncthreads();
+    return flag != 0;
+}
+
+// Failure injection for the test of the give-up path: a kernel file with
+// bounded waits keeps a device flag `every` (0 in normal runs); when it is
+// positive, the blocks of matrices whose index is a multiple of it report their
+// first bounded wait as timed out.
+__device__ __forceinline__ bool injected_failure(int every, int64_t mat)
+{
+    return every > 0 && mat % every == 0;
+}
 
 // 1/sqrt(d) with the hardware approximation (about 2 ulp), the one operation on
 // the per-column chain; the pages' measurements put IEEE sqrt + divide there
 // at ~25 instructions ("kernelbot-cholesky-930185", chol_diag kernel comment).
 // The flush-to-zero form is one instruction on the chain (measured: the
-// 128 x 128 block factor 8 % faster); a positive pivot below FLT_MIN then
-// counts as 0 here (rsqrt = +Inf, a non-finite column) while the pivot test,
-// taken on d itself, still passes it.
+// 128 x 128 block factor 8 % faster); a positive pivot below FLT_MIN counts as
+// 0 here (rsqrt = +Inf), which pivot_ok matches by failing that pivot.
 __device__ __forceinline__ float rsqrt_approx(float d) {
     float r;
     asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(d));

@@ -53,12 +53,28 @@ int launch_tmem(float *A, int n, int lda, int64_t strideA, int batch, int *info,
 int launch_blocked(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                    cudaStream_t stream, bool upper);
 
+// A22 -= L21 L21^T with k columns c0 .. c0+nk-1 (nk = 128: one panel, 256: two
+// panels at once) over the trailing matrix from c0 + nk: every lower tile, or
+// with `narrow` only its first tile column. Returns 1 when the panels are not
+// 16-byte aligned (the caller's FP32 path), -1 on a bad nk.
 int launch_syrk_tc(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
-                   cudaStream_t stream, bool upper);
+                   int nk, bool narrow, cudaStream_t stream, bool upper);
 int attrs_syrk_tc(cudaFuncAttributes *fa);
 // fused: also A22 -= L21 L21^T (only when the trailing matrix is one tile, m <= 128)
 int launch_trsm_tc(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
                    cudaStream_t stream, bool upper, bool fused);
+
+// Failure injection for the test of the give-up path. Each kernel file with
+// bounded waits keeps its own device flag (every file is a device module of
+// its own) on the current device; while it is positive, every block of that
+// file's kernels whose matrix index is a multiple of it reports its first
+// bounded wait as timed out without waiting, and so takes the path a real
+// timeout takes: info = -1, the copies and MMAs it has in flight drained
+// (bounded), tensor memory released. Zero in normal runs.
+int set_fail_first_wait_cta(int every);      // K2's bulk-copy load
+int set_fail_first_wait_trsm_tc(int every);  // tensor-core panel solve
+int set_fail_first_wait_syrk_tc(int every);  // tensor-core trailing update
+int set_fail_first_wait_tmem(int every);     // K2t
 
 int launch_dpotrf(double *A, int n, int lda, int64_t strideA, int batch, int *info,
                   cudaStream_t stream, bool upper);

@@ -36,6 +36,9 @@ namespace {
 
 using namespace cta;
 
+// failure injection for the give-up test (see set_fail_first_wait in launch.cuh)
+__device__ int g_fail_first_wait;
+
 // Step 3: one 4 x 4 tile (I, K), I >= K, of the trailing lower triangle that
 // starts at c1 = c0 + 32; L21 is panel p's rows c1.. .
 template <int NB>
@@ -204,7 +207,9 @@ potrf_cta_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int bat
     __syncthreads();
     if constexpr (FULL) {
         bulk_load_full<NB>(S, Ab, lda, tid, mbar);
-        if (tid == 0 && !tc::mbar_wait(&mbar[0], 0, kWaitCycles)) sh_err = 1;
+        if (tid == 0 && (injected_failure(g_fail_first_wait, mat) ||
+                         !tc::mbar_wait(&mbar[0], 0, kWaitCycles)))
+            sh_err = 1;
     } else if constexpr (UP) {
         load_upper<NB, NT>(S, Ab, n, lda, 0, 32, warp, lane);
         cp_async_commit();
@@ -342,6 +347,11 @@ int attrs_nb(cudaFuncAttributes *fa, int *threads, int *dyn)
 }
 
 }  // namespace
+
+int set_fail_first_wait_cta(int every)
+{
+    return (int)cudaMemcpyToSymbol(g_fail_first_wait, &every, sizeof every);
+}
 
 int launch_cta(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                cudaStream_t stream, InfoMode mode, bool upper, bool no_bulk)

@@ -50,6 +50,7 @@ struct Ar<double> {
     __device__ static double add_mul_conj(double c, double a, double b) { return fma(a, b, c); }
     __device__ static double sub(double c, double a) { return c - a; }
     __device__ static R root(R d) { return sqrt(d); }
+    __device__ static bool pivot_pass(R d) { return d > 0.0; }
 };
 
 template <>
@@ -75,6 +76,8 @@ struct Ar<float2> {
     }
     __device__ static float2 sub(float2 c, float2 a) { return make_float2(c.x - a.x, c.y - a.y); }
     __device__ static R root(R d) { return sqrtf(d); }
+    // single precision: a subnormal pivot fails, as in every float kernel
+    __device__ static bool pivot_pass(R d) { return pivot_ok(d); }
 };
 
 template <>
@@ -97,6 +100,7 @@ struct Ar<double2> {
     }
     __device__ static double2 sub(double2 c, double2 a) { return make_double2(c.x - a.x, c.y - a.y); }
     __device__ static R root(R d) { return sqrt(d); }
+    __device__ static bool pivot_pass(R d) { return d > 0.0; }
 };
 
 constexpr int kDNb = 128;    // panel width of the blocked path
@@ -138,7 +142,7 @@ simple_potrf_kernel(T *__restrict__ A, int n, int lda, int64_t strideA, int batc
         // and division are long sequences on this GPU's slow FP64 pipe)
         if (tid == 0) {
             const R d = X::re(Sd[pk(j, j, n)]);  // a complex diagonal's imaginary part is not read
-            if (!(d > R(0))) {
+            if (!X::pivot_pass(d)) {
                 sh_fail = j + 1;
             } else {
                 const R ljj = X::root(d);
@@ -204,7 +208,7 @@ simple_trsm_kernel(T *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     T *Ld = reinterpret_cast<T *>(sraw);  // Ld[pk(i, k, 128)] = L11(i, k), i >= k (packed)
     __shared__ R rdiag[kDNb];             // 1 / L11(j, j)
     const int64_t mat = blockIdx.x;
-    if (info[mat] != 0) return;
+    if (block_skip(info, mat)) return;
     T *__restrict__ Ab = A + mat * strideA;
     const int tid = threadIdx.x;
     for (int k = 0; k < kDNb; ++k)
@@ -256,7 +260,7 @@ simple_syrk_kernel(T *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     using X = Ar<T>;
     __shared__ T As[kDKc][kDTile + 1], Bs[kDKc][kDTile + 1];
     const int64_t mat = blockIdx.x;
-    if (info[mat] != 0) return;
+    if (block_skip(info, mat)) return;
     int I, K;
     {
         const int t = blockIdx.y;

@@ -31,6 +31,9 @@
 namespace bl {
 namespace {
 
+// failure injection for the give-up test (see set_fail_first_wait in launch.cuh)
+__device__ int g_fail_first_wait;
+
 constexpr uint32_t kLbo = 128;               // K-adjacent core matrices
 constexpr uint32_t kSbo = 8 * 128 + 16;      // K = 32 per row group, +16 B (banks)
 constexpr uint32_t kTileBytes = 16 * kSbo;   // 128 rows
@@ -152,7 +155,9 @@ potrf_tmem_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int ba
     for (int p = 0; p < NB; ++p) {
         const int c0 = 32 * p;
         if (p > 0) {
-            if (tid == 0 && !tc::mbar_wait(&mbar[0], (n0 - 1) & 1, kWaitCycles)) sh_err = 1;
+            if (tid == 0 && ((p == 1 && injected_failure(g_fail_first_wait, mat)) ||
+                             !tc::mbar_wait(&mbar[0], (n0 - 1) & 1, kWaitCycles)))
+                sh_err = 1;
             tc::fence_before_sync();
             __syncthreads();
             if (sh_err) break;
@@ -299,6 +304,11 @@ potrf_tmem_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int ba
 DeviceOnce g_attrs;
 
 }  // namespace
+
+int set_fail_first_wait_tmem(int every)
+{
+    return (int)cudaMemcpyToSymbol(g_fail_first_wait, &every, sizeof every);
+}
 
 int launch_tmem(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                 cudaStream_t stream, InfoMode mode)

@@ -45,6 +45,9 @@ constexpr uint32_t kOffLd = kOffLt + kLtBytes;
 constexpr uint32_t kOffRinv = kOffLd + 4 * 32 * 32 * 4;
 constexpr int kSmemBytes = (int)(kOffRinv + 128 * 4);
 
+// failure injection for the give-up test (see set_fail_first_wait in launch.cuh)
+__device__ int g_fail_first_wait;
+
 __device__ __forceinline__ uint32_t core_off(int r, int q)
 {
     return (uint32_t)(r >> 3) * kSbo + (uint32_t)q * kLbo + (uint32_t)(r & 7) * 16;
@@ -117,7 +120,11 @@ trsm_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     __shared__ int sh_err;
 
     const int64_t mat = blockIdx.x;
-    if (info[mat] != 0) return;
+    // launched as a programmatic dependent: wait for the previous kernel's
+    // writes, then let the next kernel of the stream start launching
+    pdl_wait();
+    pdl_trigger();
+    if (block_skip(info, mat)) return;
     float *__restrict__ Ab = A + mat * strideA;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int R = c0 + 128 + (int)blockIdx.y * 128 + tid;  // this thread's row
@@ -194,10 +201,18 @@ trsm_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     __syncthreads();
 
     const uint32_t sbase = tc::smem_u32(smem);
+    // the MMA group committed last and not yet seen complete (thread 0; -1: none):
+    // a block that gives up waits for it before releasing tensor memory
+    int pend = -1;
 #pragma unroll 1
     for (int j = 0; j < 4; ++j) {
         if (j > 0) {
-            if (tid == 0 && !tc::mbar_wait(&mbar, (j - 1) & 1, kWaitCycles)) sh_err = 1;
+            if (tid == 0) {
+                if (!(j == 1 && injected_failure(g_fail_first_wait, mat)) &&
+                    tc::mbar_wait(&mbar, (j - 1) & 1, kWaitCycles))
+                    pend = -1;
+                else sh_err = 1;
+            }
             tc::fence_before_sync();
             __syncthreads();
             if (sh_err) break;
@@ -293,7 +308,10 @@ trsm_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
                 }
             }
         }
-        if (tid == 0) tc::mma_commit(&mbar);
+        if (tid == 0) {
+            tc::mma_commit(&mbar);
+            pend = j;
+        }
     }
 
     if constexpr (FUSED) {
@@ -302,7 +320,10 @@ trsm_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
         // D's row r; lower storage: it updates the entries (r, c), c <= r,
         // coalesced over r; upper storage: the entries (c, r), c >= r, whose
         // memory (c1 + r) + (c1 + c) lda is coalesced over r too
-        if (tid == 0 && !sh_err && !tc::mbar_wait(&mbar, 1, kWaitCycles)) sh_err = 1;
+        if (tid == 0 && !sh_err) {
+            if (tc::mbar_wait(&mbar, 1, kWaitCycles)) pend = -1;
+            else sh_err = 1;
+        }
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
@@ -329,6 +350,9 @@ trsm_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
         }
     }
 
+    // a block that gave up lets its last MMA group drain (bounded) first: no
+    // MMA may still write the tensor memory it releases
+    if (tid == 0 && sh_err && pend >= 0) tc::mbar_wait(&mbar, pend & 1, kWaitCycles);
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, kCols);
@@ -354,11 +378,16 @@ int launch_k(float *A, int n, int lda, int64_t strideA, int batch, int *info, in
         return e;
     const int m = n - c0 - 128;
     dim3 grid((unsigned)batch, (unsigned)((m + 127) / 128));
-    trsm_tc_kernel<UP, FUSED><<<grid, 128, smem, stream>>>(A, n, lda, strideA, c0, info);
-    return (int)cudaGetLastError();
+    return launch_pdl(trsm_tc_kernel<UP, FUSED>, grid, dim3(128), (size_t)smem, stream, A, n, lda,
+                      strideA, c0, info);
 }
 
 }  // namespace
+
+int set_fail_first_wait_trsm_tc(int every)
+{
+    return (int)cudaMemcpyToSymbol(g_fail_first_wait, &every, sizeof every);
+}
 
 // Returns 0 after launching, 1 when the caller must use the FP32 kernel
 // (unaligned panels), or a cudaError_t.
