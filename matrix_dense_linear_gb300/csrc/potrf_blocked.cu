@@ -7,6 +7,12 @@
 //          32-column blocks, L11 packed in shared memory);
 //   syrk   A22 <- A22 - L21 L21^T on the trailing LOWER triangle only, in
 //          128 x 128 tiles (only tiles on or below the diagonal are launched).
+// On the tensor-core path the update is delayed by one panel where the
+// trailing matrix spans more than one tile: panel p updates only panel p+1's
+// columns, and panel p+1 then applies both panels' updates to the rest at once
+// (k = 256), which halves the passes over the trailing matrix, the largest
+// memory traffic of the schedule (n = 1024: 50 tile passes instead of 84), on
+// large batches (delay_pays).
 // This is the blocked right-looking schedule of "BatchLAS perf_blackwell"
 // (potrf Blocked nb/W rows: nb = 128 won above n = 512) and of the blocked
 // driver on "kernelbot-cholesky-930185", whose measured defect (a full-square
@@ -53,7 +59,7 @@ trsm_panel_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0
     __shared__ __align__(16) float Ls[kL11Floats];
     __shared__ float rinv[kNb];
     const int64_t mat = blockIdx.x;
-    if (info[mat] != 0) return;
+    if (block_skip(info, mat)) return;
     float *__restrict__ Ab = A + mat * strideA;
     const float *L11 = Ab + c0 + (int64_t)c0 * lda;  // element (c0, c0), either storage
     const int tid = threadIdx.x;
@@ -194,7 +200,7 @@ syrk_tile_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     __shared__ __align__(16) float As[2][kKc][kTile + 4];
     __shared__ __align__(16) float Bs[2][kKc][kTile + 4];
     const int64_t mat = blockIdx.x;
-    if (info[mat] != 0) return;
+    if (block_skip(info, mat)) return;
     int I, K;
     {
         const int t = blockIdx.y;
@@ -316,9 +322,29 @@ syrk_tile_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
 
 }  // namespace
 
+// Whether delaying a panel's trailing update pays: it halves the passes over
+// the trailing matrix but puts a k = 256 update on the critical path, so it is
+// taken only when the update launch covers at least eight waves of tiles (two
+// per SM): measured on GB300, 4096 x 8, 2048 x 64 and 1024 x 512 gain 3-7 %,
+// while one matrix of order 1024 loses 19 % and 60 of them 2 %.
+static bool delay_pays(int m, int batch, int sms)
+{
+    const int64_t T = (m + kTile - 1) / kTile;
+    return (int64_t)batch * (T * (T + 1) / 2) >= 8 * 2 * (int64_t)sms;
+}
+
 int launch_blocked(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                    cudaStream_t stream, bool upper)
 {
+    // pending: the previous panel updated only this panel's columns (a narrow
+    // update); its update of everything right of them is applied together with
+    // this panel's, with k = 256 (both panels' columns), so that each trailing
+    // tile is read and written once per two panels
+    bool pending = false;
+    int sms = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return (int)cudaGetLastError();
     for (int c0 = 0; c0 < n; c0 += kNb) {
         const int nb = n - c0 < kNb ? n - c0 : kNb;
         int e = launch_cta(A + c0 + (int64_t)c0 * lda, nb, lda, strideA, batch, info, stream,
@@ -332,8 +358,9 @@ int launch_blocked(float *A, int n, int lda, int64_t strideA, int batch, int *in
         // 256: 1.02 against 1.10 ms), a ragged tile (order 200: 0.77 against
         // 0.80 ms) and smaller batches (64 of order 256: 63 against 67 us), but
         // not a full tile of a large batch (4096 of order 256: 0.80 either way,
-        // 1 % slower fused)
-        const bool fuse = m <= kTile && (upper || m < kTile || batch <= 2048);
+        // 1 % slower fused); never while an update is pending (it takes the
+        // two panels' columns)
+        const bool fuse = !pending && m <= kTile && (upper || m < kTile || batch <= 2048);
         e = launch_trsm_tc(A, n, lda, strideA, batch, info, c0, stream, upper, fuse);
         if (e == 0 && fuse) continue;
         if (e == 1) {
@@ -348,15 +375,35 @@ int launch_blocked(float *A, int n, int lda, int64_t strideA, int batch, int *in
         }
         if (e) return e;
         // tensor cores (3xTF32) when the panels are 16-byte aligned, else FP32
-        e = launch_syrk_tc(A, n, lda, strideA, batch, info, c0, stream, upper);
-        if (e == 1) {
-            const int T = (m + kTile - 1) / kTile;
-            dim3 gs((unsigned)batch, (unsigned)(T * (T + 1) / 2));
-            if (upper)
-                syrk_tile_kernel<true><<<gs, 256, 0, stream>>>(A, n, lda, strideA, c0, info);
-            else
-                syrk_tile_kernel<false><<<gs, 256, 0, stream>>>(A, n, lda, strideA, c0, info);
-            e = (int)cudaGetLastError();
+        if (pending) {
+            // the previous panel's delayed update and this panel's, k = 256
+            e = launch_syrk_tc(A, n, lda, strideA, batch, info, c0 - kNb, 2 * kNb, false, stream,
+                               upper);
+            pending = false;
+        } else if (m > kTile && delay_pays(m, batch, sms)) {
+            // delay: only the next panel's columns now (one tile column)
+            e = launch_syrk_tc(A, n, lda, strideA, batch, info, c0, kNb, true, stream, upper);
+            pending = e == 0;
+            if (e == 1) {  // unaligned: the FP32 kernel updates everything now
+                const int T = (m + kTile - 1) / kTile;
+                dim3 gs((unsigned)batch, (unsigned)(T * (T + 1) / 2));
+                if (upper)
+                    syrk_tile_kernel<true><<<gs, 256, 0, stream>>>(A, n, lda, strideA, c0, info);
+                else
+                    syrk_tile_kernel<false><<<gs, 256, 0, stream>>>(A, n, lda, strideA, c0, info);
+                e = (int)cudaGetLastError();
+            }
+        } else {
+            e = launch_syrk_tc(A, n, lda, strideA, batch, info, c0, kNb, false, stream, upper);
+            if (e == 1) {
+                const int T = (m + kTile - 1) / kTile;
+                dim3 gs((unsigned)batch, (unsigned)(T * (T + 1) / 2));
+                if (upper)
+                    syrk_tile_kernel<true><<<gs, 256, 0, stream>>>(A, n, lda, strideA, c0, info);
+                else
+                    syrk_tile_kernel<false><<<gs, 256, 0, stream>>>(A, n, lda, strideA, c0, info);
+                e = (int)cudaGetLastError();
+            }
         }
         if (e) return e;
     }

@@ -1,5 +1,6 @@
 // Trailing update of the blocked path on the tensor cores:
-//     A22 <- A22 - L21 L21^T     (lower triangle, 128 x 128 output tiles, K = 128)
+//     A22 <- A22 - L21 L21^T     (lower triangle, 128 x 128 output tiles, K = 128
+//                                 or 256: one panel or two panels at once)
 // with an error-compensated "3xTF32" split of the FP32 operands: each operand
 // x = hi + lo with hi exact in TF32 and lo the FP32 remainder, and
 //     L_I L_K^T ~= hi_I hi_K^T + hi_I lo_K^T + lo_I hi_K^T
@@ -20,6 +21,13 @@
 // accumulator back from tensor memory (warp w: rows 32(w%4).., columns
 // 64(w/4)..) and subtracts it from A22 in place, lower triangle only.
 //
+// Two panels at once (K = 256): the blocked driver may delay a panel's update
+// of everything right of the next panel's columns and apply it together with
+// the next panel's update, so that each trailing tile is read and written
+// once for two panels. The next panel's own columns are updated alone first
+// (`narrow`: the first tile column of the trailing matrix only), since its
+// diagonal factor and panel solve need them.
+//
 // Every wait is bounded (about a second); a block that gives up marks the
 // matrix with info = -1 and still releases its tensor memory. The upper
 // storage (uplo = 'U') changes only the addresses: a row of L is contiguous
@@ -33,15 +41,17 @@
 namespace bl {
 namespace {
 
-constexpr int kNbTc = 128;                 // panel width = GEMM k
+constexpr int kNbTc = 128;                 // panel width
 constexpr int kKs = 16;                    // k columns per shared-memory slice
-constexpr int kSlices = kNbTc / kKs;       // 8
 constexpr uint32_t kLbo = 128;             // K-adjacent core matrices
 constexpr uint32_t kSbo = (kKs / 4) * 128 + 16;  // row-group stride, +16 B: no bank conflicts
 constexpr uint32_t kTileBytes = 16 * kSbo;  // 128 rows
 constexpr uint32_t kStageBytes = 4 * kTileBytes;  // A hi, A lo, B hi, B lo
 constexpr int kSmemBytes = 2 * kStageBytes;
 constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at 2 GHz
+
+// failure injection for the give-up test (see set_fail_first_wait in launch.cuh)
+__device__ int g_fail_first_wait;
 
 __device__ __forceinline__ uint32_t core_off(int r, int kq)
 {
@@ -51,18 +61,27 @@ __device__ __forceinline__ uint32_t core_off(int r, int kq)
 
 template <bool UP>
 __global__ void __launch_bounds__(256, 2)
-syrk_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
-               int *__restrict__ info)
+syrk_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0, int nk,
+               int narrow, int *__restrict__ info)
 {
+    // k columns c0 .. c0+nk-1 (nk = 128 or 256); the trailing matrix starts at
+    // c1 = c0 + nk; narrow: tile column 0 only (I = blockIdx.y, K = 0)
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ uint32_t tmem_base;
     __shared__ __align__(8) uint64_t mbar[2];
     __shared__ int sh_err;
 
     const int64_t mat = blockIdx.x;
-    if (info[mat] != 0) return;
+    // launched as a programmatic dependent: wait for the previous kernel's
+    // writes, then let the next kernel of the stream start launching
+    pdl_wait();
+    pdl_trigger();
+    if (block_skip(info, mat)) return;
     int I, K;
-    {
+    if (narrow) {
+        I = (int)blockIdx.y;
+        K = 0;
+    } else {
         const int t = blockIdx.y;
         int i = (int)((sqrtf(8.0f * (float)t + 1.0f) - 1.0f) * 0.5f);
         while ((i + 1) * (i + 2) / 2 <= t) ++i;
@@ -71,8 +90,9 @@ syrk_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
         K = t - i * (i + 1) / 2;
     }
     float *__restrict__ Ab = A + mat * strideA;
-    const int c1 = c0 + kNbTc;
+    const int c1 = c0 + nk;
     const int m = n - c1;
+    const int nslices = nk / kKs;
     const int ri = I * 128, rk = K * 128;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // The MMA computes D[r][c] = sum_k L(tm + r, k) L(tn + c, k). Lower storage:
@@ -86,6 +106,9 @@ syrk_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     // warp's lanes take 32 row quads (16-byte loads down a column), upper: 8
     // row quads x 4 k quads (16-byte loads along the rows, 64 bytes a row)
     const int op = tid >> 7;                            // 0: rows tm.. (A), 1: rows tn.. (B)
+    // a diagonal tile's two operands are the same rows: staged once (op 0),
+    // and the MMAs read that copy as B too
+    const bool stager = !(op == 1 && tm == tn);
     const int rq = UP ? (tid >> 2) & 31 : tid & 31;     // row quad: rows 4rq .. 4rq+3
     const int kq = UP ? tid & 3 : (tid >> 5) & 3;       // k quad within the slice
     const int rbase = op ? tn : tm;
@@ -114,6 +137,7 @@ syrk_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
 
     float4 cur[4], nxt[4], nxt2[4];  // lower: [k][4 rows]; upper: [row][4 k]
     auto load_slice = [&](int s, float4 (&v)[4]) {
+        if (!stager) return;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             if constexpr (UP) {
@@ -136,13 +160,16 @@ syrk_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     load_slice(0, cur);
     load_slice(1, nxt);
 
+    const bool fail_first = injected_failure(g_fail_first_wait, mat);
     bool ok = true;
     int issued = 0;  // slices whose MMAs thread 0 has issued (same in every thread)
 #pragma unroll 1
-    for (int s = 0; s < kSlices; ++s) {
+    for (int s = 0; s < nslices; ++s) {
         const int b = s & 1;
-        if (s + 2 < kSlices) load_slice(s + 2, nxt2);  // two slices in flight
-        if (s >= 2 && !tc::mbar_wait(&mbar[b], ((s - 2) >> 1) & 1, kWaitCycles)) ok = false;
+        if (s + 2 < nslices) load_slice(s + 2, nxt2);  // two slices in flight
+        if (s >= 2 && ((s == 2 && fail_first) ||
+                       !tc::mbar_wait(&mbar[b], ((s - 2) >> 1) & 1, kWaitCycles)))
+            ok = false;
         // transpose the 4 x 4 block to K-major rows, split into hi and lo
         uint8_t *st = smem + b * kStageBytes + (op ? 2 : 0) * kTileBytes;
         const float cv[4][4] = {{cur[0].x, cur[0].y, cur[0].z, cur[0].w},
@@ -150,7 +177,7 @@ syrk_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
                                 {cur[2].x, cur[2].y, cur[2].z, cur[2].w},
                                 {cur[3].x, cur[3].y, cur[3].z, cur[3].w}};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 4 && stager; ++i) {
             float h[4], l[4];
 #pragma unroll
             for (int c = 0; c < 4; ++c) tc::split_tf32(UP ? cv[i][c] : cv[c][i], h[c], l[c]);
@@ -166,7 +193,8 @@ syrk_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
         if (sh_err) { ok = false; break; }
         if (tid == 0) {
             const uint32_t a_hi = sbase + b * kStageBytes, a_lo = a_hi + kTileBytes;
-            const uint32_t b_hi = a_hi + 2 * kTileBytes, b_lo = a_hi + 3 * kTileBytes;
+            const uint32_t b_hi = tm == tn ? a_hi : a_hi + 2 * kTileBytes;
+            const uint32_t b_lo = b_hi + kTileBytes;
 #pragma unroll
             for (int ks = 0; ks < kKs / 8; ++ks) {
                 const uint32_t ko = ks * 2 * kLbo;
@@ -271,8 +299,8 @@ syrk_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
 }
 
 template <bool UP>
-int launch_u(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
-             cudaStream_t stream)
+int launch_u(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0, int nk,
+             bool narrow, cudaStream_t stream)
 {
     static DeviceOnce attrs;
     if (const int e = attrs.run([] {
@@ -280,23 +308,29 @@ int launch_u(float *A, int n, int lda, int64_t strideA, int batch, int *info, in
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         }))
         return e;
-    const int m = n - c0 - kNbTc;
+    const int m = n - c0 - nk;
     const int T = (m + 127) / 128;
-    dim3 grid((unsigned)batch, (unsigned)(T * (T + 1) / 2));
-    syrk_tc_kernel<UP><<<grid, 256, kSmemBytes, stream>>>(A, n, lda, strideA, c0, info);
-    return (int)cudaGetLastError();
+    dim3 grid((unsigned)batch, (unsigned)(narrow ? T : T * (T + 1) / 2));
+    return launch_pdl(syrk_tc_kernel<UP>, grid, dim3(256), (size_t)kSmemBytes, stream, A, n, lda,
+                      strideA, c0, nk, narrow ? 1 : 0, info);
 }
 
 }  // namespace
 
+int set_fail_first_wait_syrk_tc(int every)
+{
+    return (int)cudaMemcpyToSymbol(g_fail_first_wait, &every, sizeof every);
+}
+
 // Returns 0 and launches when the tensor-core path applies (16-byte aligned
 // panels), 1 when the caller must use the FP32 path, or a cudaError_t.
 int launch_syrk_tc(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
-                   cudaStream_t stream, bool upper)
+                   int nk, bool narrow, cudaStream_t stream, bool upper)
 {
     if (((reinterpret_cast<uintptr_t>(A) & 15) != 0) || (lda & 3) || (strideA & 3)) return 1;
-    return upper ? launch_u<true>(A, n, lda, strideA, batch, info, c0, stream)
-                 : launch_u<false>(A, n, lda, strideA, batch, info, c0, stream);
+    if ((nk != kNbTc && nk != 2 * kNbTc) || n - c0 - nk <= 0) return -1;
+    return upper ? launch_u<true>(A, n, lda, strideA, batch, info, c0, nk, narrow, stream)
+                 : launch_u<false>(A, n, lda, strideA, batch, info, c0, nk, narrow, stream);
 }
 
 int attrs_syrk_tc(cudaFuncAttributes *fa)
