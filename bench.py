@@ -38,16 +38,14 @@ L2_FLUSH_BYTES = 512 << 20
 REPLICA_CAP_BYTES = 96 << 30
 
 # DRAM bytes (read + write) per launch of the dominant kernel from one ncu
-# capture, with the sha256 of the kernel's source file at capture time; a
-# changed source reports null. Filled from the summaries under profiles/.
+# capture (dram__bytes_read.sum + dram__bytes_write.sum), with the sha256 of the
+# kernel's source files at capture time: a changed source reports null.
 TRAFFIC = {
-    # workload: (source files, sha256 prefix over them, bytes per launch, summary file)
+    # workload: (source files, sha256 prefix over them, bytes per launch)
     "n32": (("matrix_dense_linear_gb300/csrc/potrf_warp.cu",
-             "matrix_dense_linear_gb300/csrc/bl_common.cuh"), "e7bebddfc929997e", 4219904,
-            "profiles/potrf_warp_n32_b1024.md"),
+             "matrix_dense_linear_gb300/csrc/bl_common.cuh"), "e7bebddfc929997e", 4219904),
     "n64": (("matrix_dense_linear_gb300/csrc/potrf_warp.cu",
-             "matrix_dense_linear_gb300/csrc/bl_common.cuh"), "e7bebddfc929997e", 12660480,
-            "profiles/potrf_warp64_n64_b1024.md"),
+             "matrix_dense_linear_gb300/csrc/bl_common.cuh"), "e7bebddfc929997e", 12660480),
 }
 
 
@@ -102,7 +100,7 @@ def traffic_for(name: str, n: int):
     ent = TRAFFIC.get(name)
     if not ent:
         return None
-    srcs, sha, nbytes, _ = ent
+    srcs, sha, nbytes = ent
     h = hashlib.sha256()
     for src in srcs:
         with open(os.path.join(ROOT, src), "rb") as f:

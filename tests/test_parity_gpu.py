@@ -342,7 +342,11 @@ def test_kernels_use_no_local_memory(route, n):
 # times (the automatic route); poisoned outside the lower triangles.
 # ---------------------------------------------------------------------------
 
-SAMPLE = {"n32": None, "n64": None, "n128": None, "n256": 384, "n1024": 40}
+# matrices compared with the oracle per workload: None = all of them; k = the
+# first, the last and k more drawn without replacement by a generator seeded
+# with the workload's id (n1024: 130 of 512, about 3 s of oracle time on 16
+# host cores; every other workload in full)
+SAMPLE = {"n32": None, "n64": None, "n128": None, "n256": None, "n1024": 128}
 
 
 @pytest.mark.parametrize("name", ["n32", "n64", "n128", "n256", "n1024"])
