@@ -206,11 +206,23 @@ class DeviceWorkload:
         self.flush.fill_(1.0)
 
     uplo = "L"
+    work = None  # a device workspace: the call is bl_spotrf_batched_ws
+
+    def use_workspace(self) -> None:
+        import torch
+
+        import matrix_dense_linear_gb300 as bl
+        nbytes = bl.workspace_bytes(self.bt.n, self.bt.batch)
+        self.work = torch.empty(max(nbytes // 4, 4), dtype=torch.float32, device=self.dev)
 
     def call(self, i: int, stream) -> None:
         import matrix_dense_linear_gb300 as bl
         bt = self.bt
-        if self.uplo == "L":
+        if self.work is not None:
+            code = bl.spotrf_batched_ws(self.rep[i].data_ptr(), bt.n, bt.lda, bt.strideA,
+                                        bt.batch, self.info, self.work, stream=stream,
+                                        uplo=self.uplo)
+        elif self.uplo == "L":
             code = bl.spotrf_batched(self.rep[i].data_ptr(), bt.n, bt.lda, bt.strideA, bt.batch,
                                      self.info, stream)
         else:
@@ -493,6 +505,24 @@ def run_ours(args, rank: int, world: int, barrier) -> dict | None:
                    "gflops": b2.batch * flops_per_matrix(b2.n) / (pc / 1e3) / 1e9,
                    "roofline": {k: r2[k] for k in ("bound", "frac", "roof_ms")},
                    "launches_per_call": launches_per_call(b2.n)}
+            if b2.n > 128:
+                # the same workload through bl_spotrf_batched_ws (a caller-owned
+                # workspace, allocated once outside the timed region)
+                w2.use_workspace()
+                for i in range(min(args.warmup, w2.nrep)):
+                    w2.refresh(i)
+                    w2.call(i, torch.cuda.current_stream().cuda_stream)
+                torch.cuda.synchronize()
+                ms3 = time_steps(w2, args.steps, lambda: None)
+                assert not w2.info.cpu().numpy().any()
+                pc3 = ms3 / args.steps
+                r3 = roofline_entry(name, b2.n, b2.batch, pc3, pk, sms)
+                row["workspace_call"] = {
+                    "call": "bl_spotrf_batched_ws", "ms_per_call": pc3,
+                    "matrices_per_s": b2.batch / (pc3 / 1e3),
+                    "gflops": b2.batch * flops_per_matrix(b2.n) / (pc3 / 1e3) / 1e9,
+                    "roofline": {k: r3[k] for k in ("bound", "frac", "roof_ms")},
+                    "workspace_bytes": int(w2.work.numel() * 4)}
             if args.cpu_baseline:
                 ob = oracle_rate(b2, 1.0, oracle_sample_size(b2.n))
                 row["oracle_matrices_per_s"] = ob["value"]
@@ -595,6 +625,8 @@ def run_shapes(args) -> list:
         bt = type(base)(buf=buf, n=n, lda=n, strideA=n * n, batch=batch, fill=base.fill)
         w = DeviceWorkload(bt, args.steps, dev)
         w.uplo = args.uplo
+        if args.ws:
+            w.use_workspace()
         for i in range(min(args.warmup, w.nrep)):
             w.call(i, torch.cuda.current_stream().cuda_stream)
         torch.cuda.synchronize()
@@ -602,7 +634,8 @@ def run_shapes(args) -> list:
         ms = statistics.median(time_steps(w, k, lambda: None) / k for _ in range(3))
         assert not w.info.cpu().numpy().any()
         rf = roofline_entry("shape", n, batch, ms, pk, sms)
-        row = {"shape": spec, "uplo": args.uplo, "n": n, "batch": batch, "ms_per_call": ms,
+        row = {"shape": spec, "uplo": args.uplo, "workspace": bool(args.ws), "n": n,
+               "batch": batch, "ms_per_call": ms,
                "us_per_call": ms * 1e3, "matrices_per_s": batch / (ms / 1e3),
                "tflops": flops_per_matrix(n) * batch / (ms / 1e3) / 1e12,
                "roofline": {k2: rf[k2] for k2 in ("bound", "frac", "roof_ms")},
@@ -849,6 +882,8 @@ def main():
     ap.add_argument("--dtype", choices=["f32", "f64", "c64", "c128"], default="f32",
                     help="f64 / c64 / c128: time the double / complex / double complex "
                          "factorization for --shapes")
+    ap.add_argument("--ws", action="store_true",
+                    help="--shapes through bl_spotrf_batched_ws (a caller workspace)")
     ap.add_argument("--uplo", choices=["L", "U"], default="L",
                     help="storage of the factor for --shapes (U: upper triangle)")
     args = ap.parse_args()

@@ -35,6 +35,7 @@
 #ifndef BL_SPOTRF_H
 #define BL_SPOTRF_H
 
+#include <stddef.h>
 #include <stdint.h>
 #include <cuda_runtime_api.h>
 
@@ -293,6 +294,37 @@ int bl_zpotrf_batched_uplo(char uplo, double *A, int n, int lda, int64_t strideA
 int bl_fma_probe(int precision, void *out, double *tflops, cudaStream_t stream);
 
 /*
+ * bl_spotrf_workspace_bytes - the workspace bl_spotrf_batched_ws can use for
+ * (n, batch): 64 KB (one 128 x 128 float block) per matrix when n > 128, 0
+ * otherwise (and for n <= 0, batch <= 0 or n above BL_SPOTRF_MAX_N). Host
+ * only.
+ *
+ * bl_spotrf_batched_ws / bl_spotrf_batched_uplo_ws - bl_spotrf_batched (and
+ * its uplo form) with a caller-owned device workspace `work` of `work_bytes`
+ * bytes. On the blocked route (n > 128) the panels with at least 256 rows below
+ * their 128 x 128 diagonal block are then solved by the inverse of that block
+ * (the inverse-based panel solve of "kernelbot-cholesky-930185", changelog
+ * section "THE MECHANISM, FOR THE NEXT BUILD": the inverse, computed once per
+ * matrix and panel into the workspace, and one tensor-core product per 128 rows
+ * instead of a forward substitution); every other step is the same as in
+ * bl_spotrf_batched. The workspace holds nothing between calls and may be
+ * reused by any later call on the same stream; calls in flight at once on
+ * different streams need their own. work = NULL: exactly bl_spotrf_batched.
+ * The results agree with bl_spotrf_batched within the same tolerances but not
+ * bit for bit (a product by the inverse rounds differently from the
+ * substitution), and the explicit inverse makes the panel's accuracy depend on
+ * the conditioning of its diagonal block. Returns as bl_spotrf_batched, plus
+ * -8 (work not 16-byte aligned) and -9 (work_bytes below
+ * bl_spotrf_workspace_bytes(n, batch)); the uplo form moves every negative code
+ * down by one (uplo is argument 1).
+ */
+size_t bl_spotrf_workspace_bytes(int n, int batch);
+int bl_spotrf_batched_ws(float *A, int n, int lda, int64_t strideA, int batch, int *info,
+                         void *work, size_t work_bytes, cudaStream_t stream);
+int bl_spotrf_batched_uplo_ws(char uplo, float *A, int n, int lda, int64_t strideA, int batch,
+                              int *info, void *work, size_t work_bytes, cudaStream_t stream);
+
+/*
  * bl_debug_fail_first_wait - failure injection, for testing the internal-error
  * path (info[b] = -1) only. While `every` > 0 for a kernel class, every block
  * of that class on the current device whose matrix index b is a multiple of
@@ -305,7 +337,8 @@ int bl_fma_probe(int precision, void *out, double *tflops, cudaStream_t stream);
  * kernel's bulk-copy load (route 2 at n = 96 and 128 on 16-byte-aligned
  * batches, and the diagonal blocks of route 3), 2 the tensor-core panel solve
  * and 3 the tensor-core trailing update (route 3 on 16-byte-aligned batches),
- * 4 the tensor-memory kernel (route 4). Synchronous with the host; call it
+ * 4 the tensor-memory kernel (route 4), 5 the tensor-core product of the
+ * inverse-based panel solve (bl_spotrf_batched_ws). Synchronous with the host; call it
  * while no other work of the library runs. Returns 0, -1 (unknown class), -2
  * (every < 0) or a cudaError_t.
  */

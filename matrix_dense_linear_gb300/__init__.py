@@ -16,6 +16,7 @@ __all__ = ["ROUTE_AUTO", "ROUTE_WARP", "ROUTE_CTA", "ROUTE_BLOCKED", "ROUTE_TMEM
            "BLError",
            "library", "library_path", "spotrf_batched", "spotrf_batched_ex", "route",
            "kernel_info", "version", "factor", "factor_host", "spotrs_batched",
+           "workspace_bytes", "spotrf_batched_ws",
            "sposv_batched", "solve", "factor_solve"]
 
 ROUTE_AUTO, ROUTE_WARP, ROUTE_CTA, ROUTE_BLOCKED, ROUTE_TMEM = 0, 1, 2, 3, 4
@@ -47,6 +48,10 @@ SYMBOLS = {
     "bl_spotrs_batched_uplo": (_I, [_C, _VP, _I, _I, _I64, _VP, _I, _I, _I64, _I, _VP]),
     "bl_sposv_batched_uplo": (_I, [_C, _VP, _I, _I, _I64, _VP, _I, _I, _I64, _I, _VP, _VP]),
     "bl_debug_fail_first_wait": (_I, [_I, _I]),
+    "bl_spotrf_workspace_bytes": (ctypes.c_size_t, [_I, _I]),
+    "bl_spotrf_batched_ws": (_I, [_VP, _I, _I, _I64, _I, _VP, _VP, ctypes.c_size_t, _VP]),
+    "bl_spotrf_batched_uplo_ws": (_I, [_C, _VP, _I, _I, _I64, _I, _VP, _VP, ctypes.c_size_t,
+                                       _VP]),
 }
 
 
@@ -247,9 +252,36 @@ def version() -> str:
     return library().bl_spotrf_version().decode()
 
 
+def workspace_bytes(n: int, batch: int) -> int:
+    """bl_spotrf_workspace_bytes: device bytes the workspace call can use."""
+    return int(library().bl_spotrf_workspace_bytes(n, batch))
+
+
+def spotrf_batched_ws(A, n: int, lda: int, strideA: int, batch: int, info, work,
+                      work_bytes: Optional[int] = None, stream=None, uplo="L") -> int:
+    """bl_spotrf_batched_ws / bl_spotrf_batched_uplo_ws: `work` is a device
+    tensor (or pointer, or None); work_bytes defaults to the tensor's size."""
+    if work_bytes is None:
+        work_bytes = 0 if work is None or isinstance(work, int) else \
+            int(work.numel() * work.element_size())
+    if uplo in ("L", b"L"):
+        return library().bl_spotrf_batched_ws(_ptr(A), n, lda, strideA, batch, _ptr(info),
+                                              _ptr(work), work_bytes, _stream(stream))
+    return library().bl_spotrf_batched_uplo_ws(_uplo(uplo), _ptr(A), n, lda, strideA, batch,
+                                               _ptr(info), _ptr(work), work_bytes,
+                                               _stream(stream))
+
+
 def factor(A, n: int, lda: int, strideA: int, batch: int, info, stream=None,
-           route_: int = ROUTE_AUTO, uplo="L") -> None:
-    """Factor in place on the device; raises BLError on a nonzero status."""
+           route_: int = ROUTE_AUTO, uplo="L", work=None) -> None:
+    """Factor in place on the device; raises BLError on a nonzero status. With
+    `work` (a device workspace of workspace_bytes(n, batch) bytes) the call is
+    bl_spotrf_batched_ws (automatic route only)."""
+    if work is not None:
+        code = spotrf_batched_ws(A, n, lda, strideA, batch, info, work, stream=stream, uplo=uplo)
+        if code:
+            raise BLError(code)
+        return
     if uplo in ("L", b"L"):
         code = spotrf_batched_ex(A, n, lda, strideA, batch, info, stream, route_)
     else:

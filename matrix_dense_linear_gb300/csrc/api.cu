@@ -63,7 +63,7 @@ bool route_can_run(int route, int n, bool upper)
 }
 
 int run(float *A, int n, int lda, int64_t strideA, int batch, int *info, cudaStream_t stream,
-        int route, bool upper = false, bool host_mapped = false)
+        int route, bool upper = false, bool host_mapped = false, float *W = nullptr)
 {
     int e = check_args(A, n, lda, strideA, batch, info);
     if (e) return e;
@@ -81,8 +81,31 @@ int run(float *A, int n, int lda, int64_t strideA, int batch, int *info, cudaStr
                               host_mapped);
     case BL_ROUTE_TMEM:
         return bl::launch_tmem(A, n, lda, strideA, batch, info, stream, bl::InfoMode{-1});
-    default: return bl::launch_blocked(A, n, lda, strideA, batch, info, stream, upper);
+    default: return bl::launch_blocked(A, n, lda, strideA, batch, info, stream, upper, W);
     }
+}
+
+// Workspace of the inverse-based panel solve: one 128 x 128 block per matrix
+// on the blocked route (n > 128), none below.
+size_t workspace_bytes(int n, int batch)
+{
+    if (n <= kCtaMaxN || n > BL_SPOTRF_MAX_N || batch <= 0) return 0;
+    return bl::kInvBytes * (size_t)batch;
+}
+
+// the calls with a workspace: the argument checks of run(), then work (-8: not
+// 16-byte aligned; -9: work_bytes too small), then run()
+int run_ws(float *A, int n, int lda, int64_t strideA, int batch, int *info, void *work,
+           size_t work_bytes, cudaStream_t stream, bool upper)
+{
+    int e = check_args(A, n, lda, strideA, batch, info);
+    if (e) return e;
+    if (work != nullptr) {
+        if ((reinterpret_cast<uintptr_t>(work) & 15) != 0) return -8;
+        if (work_bytes < workspace_bytes(n, batch)) return -9;
+    }
+    return run(A, n, lda, strideA, batch, info, stream, BL_ROUTE_AUTO, upper, false,
+               static_cast<float *>(work));
 }
 
 // The device address of a page-locked host allocation the device maps (with
@@ -377,6 +400,22 @@ int bl_spotrf_kernel_info(int route, int n, int *regs, int *local_bytes, int *st
     return 0;
 }
 
+size_t bl_spotrf_workspace_bytes(int n, int batch) { return workspace_bytes(n, batch); }
+
+int bl_spotrf_batched_ws(float *A, int n, int lda, int64_t strideA, int batch, int *info,
+                         void *work, size_t work_bytes, cudaStream_t stream)
+{
+    return run_ws(A, n, lda, strideA, batch, info, work, work_bytes, stream, false);
+}
+
+int bl_spotrf_batched_uplo_ws(char uplo, float *A, int n, int lda, int64_t strideA, int batch,
+                              int *info, void *work, size_t work_bytes, cudaStream_t stream)
+{
+    const int u = parse_uplo(uplo);
+    if (u < 0) return -1;
+    return shift_arg(run_ws(A, n, lda, strideA, batch, info, work, work_bytes, stream, u == 1));
+}
+
 int bl_debug_fail_first_wait(int kernel_class, int every)
 {
     if (every < 0) return -2;
@@ -385,6 +424,7 @@ int bl_debug_fail_first_wait(int kernel_class, int every)
     case 2: return bl::set_fail_first_wait_trsm_tc(every);
     case 3: return bl::set_fail_first_wait_syrk_tc(every);
     case 4: return bl::set_fail_first_wait_tmem(every);
+    case 5: return bl::set_fail_first_wait_trsm_inv(every);
     default: return -1;
     }
 }

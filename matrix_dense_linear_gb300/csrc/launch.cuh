@@ -50,8 +50,16 @@ int launch_cta(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                cudaStream_t stream, InfoMode mode, bool upper, bool no_bulk = false);
 int launch_tmem(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                 cudaStream_t stream, InfoMode mode);
+// W: the caller's workspace for the inverse-based panel solve (kInvBytes per
+// matrix, 16-byte aligned), or nullptr (substitution only)
 int launch_blocked(float *A, int n, int lda, int64_t strideA, int batch, int *info,
-                   cudaStream_t stream, bool upper);
+                   cudaStream_t stream, bool upper, float *W = nullptr);
+constexpr size_t kInvBytes = 128 * 128 * sizeof(float);
+// The panel solve by the inverse of the diagonal block (trsm_inv.cu): W[b] =
+// L11^{-1} of matrix b, then L21 = A21 W^T on the tensor cores. Returns 1 when
+// A or W is not 16-byte aligned (the caller's substitution path).
+int launch_trsm_inv(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
+                    float *W, cudaStream_t stream, bool upper);
 
 // A22 -= L21 L21^T with k columns c0 .. c0+nk-1 (nk = 128: one panel, 256: two
 // panels at once) over the trailing matrix from c0 + nk: every lower tile, or
@@ -75,6 +83,7 @@ int set_fail_first_wait_cta(int every);      // K2's bulk-copy load
 int set_fail_first_wait_trsm_tc(int every);  // tensor-core panel solve
 int set_fail_first_wait_syrk_tc(int every);  // tensor-core trailing update
 int set_fail_first_wait_tmem(int every);     // K2t
+int set_fail_first_wait_trsm_inv(int every); // the inverse-based panel solve's GEMM
 
 int launch_dpotrf(double *A, int n, int lda, int64_t strideA, int batch, int *info,
                   cudaStream_t stream, bool upper);

@@ -32,6 +32,7 @@ constexpr int kNb = 128;          // panel width
 constexpr int kTrsmRows = 128;    // rows per TRSM block (one per thread)
 constexpr int kTile = 128;        // SYRK output tile
 constexpr int kKc = 16;           // SYRK k-slice staged in shared memory
+constexpr int kInvMinRows = 256;  // inverse-based panel solve from two row blocks on
 
 // L11 in shared memory, packed by 32-column blocks: block b keeps rows
 // 32b .. 127 of its 32 columns, column-major with leading dimension 128 - 32b.
@@ -334,7 +335,7 @@ static bool delay_pays(int m, int batch, int sms)
 }
 
 int launch_blocked(float *A, int n, int lda, int64_t strideA, int batch, int *info,
-                   cudaStream_t stream, bool upper)
+                   cudaStream_t stream, bool upper, float *W)
 {
     // pending: the previous panel updated only this panel's columns (a narrow
     // update); its update of everything right of them is applied together with
@@ -361,7 +362,13 @@ int launch_blocked(float *A, int n, int lda, int64_t strideA, int batch, int *in
         // 1 % slower fused); never while an update is pending (it takes the
         // two panels' columns)
         const bool fuse = !pending && m <= kTile && (upper || m < kTile || batch <= 2048);
-        e = launch_trsm_tc(A, n, lda, strideA, batch, info, c0, stream, upper, fuse);
+        // with a workspace, panels with at least kInvMinRows rows below the
+        // diagonal block are solved by its inverse (computed once, shared by
+        // the panel's row blocks)
+        e = 1;
+        if (W != nullptr && !fuse && m >= kInvMinRows)
+            e = launch_trsm_inv(A, n, lda, strideA, batch, info, c0, W, stream, upper);
+        if (e == 1) e = launch_trsm_tc(A, n, lda, strideA, batch, info, c0, stream, upper, fuse);
         if (e == 0 && fuse) continue;
         if (e == 1) {
             dim3 gt((unsigned)batch, (unsigned)((m + kTrsmRows - 1) / kTrsmRows));

@@ -219,3 +219,33 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(bl, "_lib", None)
     with pytest.raises(ImportError):
         bl.library()
+
+
+def test_workspace_bytes(bl):
+    """One 128 x 128 float block per matrix on the blocked route, none below it
+    or for empty and out-of-range calls (host only)."""
+    assert bl.workspace_bytes(128, 1000) == 0
+    assert bl.workspace_bytes(129, 3) == 3 * 128 * 128 * 4
+    assert bl.workspace_bytes(1024, 512) == 512 * 65536
+    assert bl.workspace_bytes(4096, 1) == 65536
+    assert bl.workspace_bytes(4097, 1) == 0
+    assert bl.workspace_bytes(0, 5) == 0 and bl.workspace_bytes(512, 0) == 0
+    assert bl.workspace_bytes(-3, 5) == 0 and bl.workspace_bytes(512, -1) == 0
+
+
+def test_workspace_argument_codes(bl):
+    """Checked on the host before anything is launched: the usual argument codes
+    first, then -8 (work not 16-byte aligned) and -9 (too small); the uplo form
+    counts uplo as argument 1."""
+    lib = bl.library()
+    need = bl.workspace_bytes(512, 2)
+    assert lib.bl_spotrf_batched_ws(16, 512, 512, 512 * 512, 2, 16, 4100, need, None) == -8
+    assert lib.bl_spotrf_batched_ws(16, 512, 512, 512 * 512, 2, 16, 4096, need - 4, None) == -9
+    assert lib.bl_spotrf_batched_ws(16, 512, 511, 512 * 512, 2, 16, 4100, need, None) == -3
+    assert lib.bl_spotrf_batched_ws(16, 512, 512, 512 * 512, 2, None, 4100, need, None) == -6
+    assert lib.bl_spotrf_batched_uplo_ws(b"L", 16, 512, 512, 512 * 512, 2, 16, 4100, need,
+                                         None) == -9
+    assert lib.bl_spotrf_batched_uplo_ws(b"U", 16, 512, 512, 512 * 512, 2, 16, 4096, 0,
+                                         None) == -10
+    assert lib.bl_spotrf_batched_uplo_ws(b"Q", 16, 512, 512, 512 * 512, 2, 16, 4096, need,
+                                         None) == -1
