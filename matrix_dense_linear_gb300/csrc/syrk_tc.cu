@@ -62,16 +62,22 @@ __device__ __forceinline__ uint32_t core_off(int r, int kq)
 template <bool UP>
 __global__ void __launch_bounds__(256, 2)
 syrk_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0, int nk,
-               int narrow, int *__restrict__ info)
+               int narrow, int ntiles_col, int *__restrict__ info)
 {
     // k columns c0 .. c0+nk-1 (nk = 128 or 256); the trailing matrix starts at
-    // c1 = c0 + nk; narrow: tile column 0 only (I = blockIdx.y, K = 0)
+    // c1 = c0 + nk; narrow: tile column 0 only (K = 0). The grid is one
+    // dimension, the tile index fastest: a matrix's tiles run together, so its
+    // panel is read from memory once and from L2 by the other tiles (with the
+    // matrix fastest, a round of tiles over a large batch streams more than L2
+    // holds between two tiles of one matrix).
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ uint32_t tmem_base;
     __shared__ __align__(8) uint64_t mbar[2];
     __shared__ int sh_err;
 
-    const int64_t mat = blockIdx.x;
+    const int nt = narrow ? ntiles_col : ntiles_col * (ntiles_col + 1) / 2;  // tiles a matrix
+    const int64_t mat = blockIdx.x / nt;
+    const int tile = (int)(blockIdx.x % nt);
     // launched as a programmatic dependent: wait for the previous kernel's
     // writes, then let the next kernel of the stream start launching
     pdl_wait();
@@ -79,10 +85,10 @@ syrk_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0, i
     if (block_skip(info, mat)) return;
     int I, K;
     if (narrow) {
-        I = (int)blockIdx.y;
+        I = tile;
         K = 0;
     } else {
-        const int t = blockIdx.y;
+        const int t = tile;
         int i = (int)((sqrtf(8.0f * (float)t + 1.0f) - 1.0f) * 0.5f);
         while ((i + 1) * (i + 2) / 2 <= t) ++i;
         while (i * (i + 1) / 2 > t) --i;
@@ -310,9 +316,10 @@ int launch_u(float *A, int n, int lda, int64_t strideA, int batch, int *info, in
         return e;
     const int m = n - c0 - nk;
     const int T = (m + 127) / 128;
-    dim3 grid((unsigned)batch, (unsigned)(narrow ? T : T * (T + 1) / 2));
-    return launch_pdl(syrk_tc_kernel<UP>, grid, dim3(256), (size_t)kSmemBytes, stream, A, n, lda,
-                      strideA, c0, nk, narrow ? 1 : 0, info);
+    const int64_t blocks = (int64_t)batch * (narrow ? T : T * (T + 1) / 2);
+    if (blocks > 0x7fffffffLL) return (int)cudaErrorInvalidConfiguration;
+    return launch_pdl(syrk_tc_kernel<UP>, dim3((unsigned)blocks), dim3(256), (size_t)kSmemBytes,
+                      stream, A, n, lda, strideA, c0, nk, narrow ? 1 : 0, T, info);
 }
 
 }  // namespace

@@ -111,7 +111,7 @@ struct LtPieces {
 // read back).
 template <bool UP, bool FUSED>
 __global__ void __launch_bounds__(128, FUSED ? 2 : 3)
-trsm_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
+trsm_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0, int nrb,
                int *__restrict__ info)
 {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -119,7 +119,10 @@ trsm_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     __shared__ __align__(8) uint64_t mbar;
     __shared__ int sh_err;
 
-    const int64_t mat = blockIdx.x;
+    // one-dimensional grid, the row block fastest: a matrix's row blocks run
+    // together and share its L11 through L2
+    const int64_t mat = blockIdx.x / nrb;
+    const int rb = (int)(blockIdx.x % nrb);
     // launched as a programmatic dependent: wait for the previous kernel's
     // writes, then let the next kernel of the stream start launching
     pdl_wait();
@@ -127,7 +130,7 @@ trsm_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     if (block_skip(info, mat)) return;
     float *__restrict__ Ab = A + mat * strideA;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int R = c0 + 128 + (int)blockIdx.y * 128 + tid;  // this thread's row
+    const int R = c0 + 128 + rb * 128 + tid;  // this thread's row
     const bool live = R < n;
     const int64_t xs = UP ? 1 : lda;  // step between the columns of one row
     const float *L11 = Ab + c0 + (int64_t)c0 * lda;         // L11(i, k) = L11[lidx(i, k)]
@@ -377,9 +380,11 @@ int launch_k(float *A, int n, int lda, int64_t strideA, int batch, int *info, in
         }))
         return e;
     const int m = n - c0 - 128;
-    dim3 grid((unsigned)batch, (unsigned)((m + 127) / 128));
-    return launch_pdl(trsm_tc_kernel<UP, FUSED>, grid, dim3(128), (size_t)smem, stream, A, n, lda,
-                      strideA, c0, info);
+    const int nrb = (m + 127) / 128;
+    const int64_t blocks = (int64_t)batch * nrb;
+    if (blocks > 0x7fffffffLL) return (int)cudaErrorInvalidConfiguration;
+    return launch_pdl(trsm_tc_kernel<UP, FUSED>, dim3((unsigned)blocks), dim3(128), (size_t)smem,
+                      stream, A, n, lda, strideA, c0, nrb, info);
 }
 
 }  // namespace
