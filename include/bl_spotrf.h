@@ -324,6 +324,37 @@ int bl_spotrf_batched_ws(float *A, int n, int lda, int64_t strideA, int batch, i
 int bl_spotrf_batched_uplo_ws(char uplo, float *A, int n, int lda, int64_t strideA, int batch,
                               int *info, void *work, size_t work_bytes, cudaStream_t stream);
 
+/* Device memory the library reserves on every GPU that loads it, for
+ * bl_spotrf_batched_static (held until the process exits). */
+#define BL_SPOTRF_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/*
+ * bl_spotrf_batched_static - bl_spotrf_batched_ws for callers that cannot
+ * allocate device memory where they factor: a library running inside a
+ * framework that owns all device memory through an allocator the library
+ * cannot reach, a latency-bounded loop that cannot take the device-wide
+ * synchronization cudaMalloc and cudaFree may cause, or a process that already
+ * holds all the memory it was given. The call allocates nothing: the scratch of
+ * the inverse-based panel solve comes from a fixed device array of
+ * BL_SPOTRF_STATIC_SCRATCH_BYTES inside the library, so a call whose scratch
+ * would exceed it (n > 128 and batch > 256) is rejected with -10 before any
+ * work. The caller still owns A and info; arguments, results, info and every
+ * other return code are those of bl_spotrf_batched_ws with a workspace.
+ *
+ * The first call made on a device looks the array's device address up (once
+ * per device, on the host, with that device current); make that first call
+ * before capturing a stream into a CUDA graph. All calls share the one array,
+ * which keeps the last call's contents: every block a call reads it has
+ * written first, so nothing needs clearing, but calls that run at the same
+ * time on the GPU (on different streams, or from different host threads) race
+ * on it and must be ordered by the caller.
+ *
+ * The pages have no counterpart to this entry point: it exists for the callers
+ * above.
+ */
+int bl_spotrf_batched_static(float *A, int n, int lda, int64_t strideA, int batch, int *info,
+                             cudaStream_t stream);
+
 /*
  * bl_debug_fail_first_wait - failure injection, for testing the internal-error
  * path (info[b] = -1) only. While `every` > 0 for a kernel class, every block

@@ -52,6 +52,7 @@ SYMBOLS = {
     "bl_spotrf_batched_ws": (_I, [_VP, _I, _I, _I64, _I, _VP, _VP, ctypes.c_size_t, _VP]),
     "bl_spotrf_batched_uplo_ws": (_I, [_C, _VP, _I, _I, _I64, _I, _VP, _VP, ctypes.c_size_t,
                                        _VP]),
+    "bl_spotrf_batched_static": (_I, [_VP, _I, _I, _I64, _I, _VP, _VP]),
 }
 
 

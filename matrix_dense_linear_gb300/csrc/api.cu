@@ -153,6 +153,13 @@ int check_trs_args(const float *L, int n, int lda, int64_t strideA, const float 
 
 }  // namespace
 
+// the argument checks of bl_spotrf_batched, for entry points in other files
+int bl::check_potrf_args(const void *A, int n, int lda, int64_t strideA, int batch,
+                         const int *info)
+{
+    return check_args(A, n, lda, strideA, batch, info);
+}
+
 extern "C" {
 
 int bl_spotrf_batched_host(float *A_host, int n, int lda, int64_t strideA, int batch,

@@ -55,6 +55,8 @@ int launch_tmem(float *A, int n, int lda, int64_t strideA, int batch, int *info,
 int launch_blocked(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                    cudaStream_t stream, bool upper, float *W = nullptr);
 constexpr size_t kInvBytes = 128 * 128 * sizeof(float);
+// the argument checks of bl_spotrf_batched (0 or a negative argument index)
+int check_potrf_args(const void *A, int n, int lda, int64_t strideA, int batch, const int *info);
 // The panel solve by the inverse of the diagonal block (trsm_inv.cu): W[b] =
 // L11^{-1} of matrix b, then L21 = A21 W^T on the tensor cores. Returns 1 when
 // A or W is not 16-byte aligned (the caller's substitution path).
