@@ -579,6 +579,7 @@ def run_sweep(args) -> list:
                             strideA=base.strideA, batch=batch, fill=base.fill)
             w = DeviceWorkload(bt, args.steps, dev)
             for i in range(min(args.warmup, w.nrep)):
+                w.refresh(i)
                 w.call(i, torch.cuda.current_stream().cuda_stream)
             torch.cuda.synchronize()
             k = min(args.steps, w.nrep)
@@ -628,6 +629,7 @@ def run_shapes(args) -> list:
         if args.ws:
             w.use_workspace()
         for i in range(min(args.warmup, w.nrep)):
+            w.refresh(i)
             w.call(i, torch.cuda.current_stream().cuda_stream)
         torch.cuda.synchronize()
         k = min(args.steps, w.nrep)
