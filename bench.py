@@ -487,7 +487,7 @@ def run_ours(args, rank: int, world: int, barrier) -> dict | None:
                              "ms_per_call": per_call, "matrices_per_s": batch / (per_call / 1e3),
                              "gflops": batch * flops_per_matrix(n) / (per_call / 1e3) / 1e9,
                              "roofline": {k: rf[k] for k in ("bound", "frac", "roof_ms")},
-                             "launches_per_call": nl,
+                             "launches_per_call": nl, "e2e": out["e2e"],
                              "oracle_matrices_per_s": out.get("cpu_baseline", {}).get("value")})
                 continue
             b2 = make_host_batch(name)
@@ -505,6 +505,12 @@ def run_ours(args, rank: int, world: int, barrier) -> dict | None:
                    "gflops": b2.batch * flops_per_matrix(b2.n) / (pc / 1e3) / 1e9,
                    "roofline": {k: r2[k] for k in ("bound", "frac", "roof_ms")},
                    "launches_per_call": launches_per_call(b2.n)}
+            # the same workload end to end through the host-buffer call
+            e2 = e2e_steps(w2, min(args.steps, 5), 2, lambda: None)
+            row["e2e"] = {"value": b2.batch * min(args.steps, 5) / (e2["ms"] / 1e3),
+                          "unit": UNIT, "ms_per_step": e2["ms"] / min(args.steps, 5),
+                          "h2d_bytes_per_step": e2["h2d"], "d2h_bytes_per_step": e2["d2h"],
+                          "mode": e2["mode"]}
             if b2.n > 128:
                 # the same workload through bl_spotrf_batched_ws (a caller-owned
                 # workspace, allocated once outside the timed region)

@@ -96,10 +96,10 @@ int launch_cpotrf_warp(float *A, int n, int lda, int64_t strideA, int batch, int
                        cudaStream_t stream, bool upper);
 // CPOTRF for 64 < n <= 128: a warp per 32 x 32 tile of the lower triangle
 int launch_cpotrf_tiles(float *A, int n, int lda, int64_t strideA, int batch, int *info,
-                        cudaStream_t stream, bool upper);
+                        cudaStream_t stream, bool upper, int info_off = -1);
 // the same schedule on real input (64 < n <= 128), a measured alternative to K2
 int launch_spotrf_tiles(float *A, int n, int lda, int64_t strideA, int batch, int *info,
-                        cudaStream_t stream, bool upper);
+                        cudaStream_t stream, bool upper, int info_off = -1);
 int attrs_tiles(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem);
 int launch_cpotrf(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                   cudaStream_t stream, bool upper);

@@ -358,19 +358,20 @@ int launch_cta(float *A, int n, int lda, int64_t strideA, int batch, int *info,
 {
     const int o = mode.off;
     const bool nb = no_bulk;
-    // 64 < n <= 128 on one call's own batch: a warp per 32 x 32 tile
-    // (potrf_tiles.cu) wherever the bulk-copy form below cannot run; 1024
+    // 64 < n <= 128, a whole matrix or a diagonal block of the blocked route
+    // (info_off >= 0: its ragged last block, or unaligned batches): a warp per
+    // 32 x 32 tile (potrf_tiles.cu) wherever the bulk-copy form below cannot run; 1024
     // matrices: n = 65 34.6 against 45.5 us, 112 70.8 against 86.1, 127 74.8
     // against 83.4; the bulk-copy form keeps n = 96 (36.7 against 42.0) and
     // 128 (58.7 against 74.6). The choice ignores no_bulk and uplo (the tile
     // kernel makes plain loads, fine on host-mapped memory, and reads either
     // storage), so a host batch gets the same kernel as on the device and the
     // upper storage the same arithmetic as the lower: the same bits.
-    if (n > 64 && o < 0) {
+    if (n > 64) {
         const bool vec = ((reinterpret_cast<uintptr_t>(A) & 15) == 0) && ((lda & 3) == 0) &&
                          ((strideA & 3) == 0);
         if (!(vec && (n == 96 || n == 128)))
-            return launch_spotrf_tiles(A, n, lda, strideA, batch, info, stream, upper);
+            return launch_spotrf_tiles(A, n, lda, strideA, batch, info, stream, upper, o);
     }
     if (n <= 32) return launch_nb<1, 32>(A, n, lda, strideA, batch, info, stream, o, upper, nb);
     if (n <= 64) return launch_nb<2, 64>(A, n, lda, strideA, batch, info, stream, o, upper, nb);

@@ -348,8 +348,21 @@ int launch_blocked_s(T *A, int n, int lda, int64_t strideA, int batch, int *info
         return e;
     for (int c0 = 0; c0 < n; c0 += kDNb) {
         const int nb = n - c0 < kDNb ? n - c0 : kDNb;
-        int e = launch_cta_s<T, UP>(A + c0 + (int64_t)c0 * lda, nb, lda, strideA, batch, info,
-                                    st, c0 == 0 ? -1 : c0);
+        // single-precision complex diagonal blocks above 64 on the warp-per-tile
+        // register kernel (potrf_tiles.cu, complex arithmetic), the others on
+        // the plain shared-memory kernel
+        int e;
+        if constexpr (std::is_same<T, float2>::value) {
+            if (nb > 64)
+                e = launch_cpotrf_tiles(reinterpret_cast<float *>(A + c0 + (int64_t)c0 * lda), nb,
+                                        lda, strideA, batch, info, st, UP, c0 == 0 ? -1 : c0);
+            else
+                e = launch_cta_s<T, UP>(A + c0 + (int64_t)c0 * lda, nb, lda, strideA, batch,
+                                        info, st, c0 == 0 ? -1 : c0);
+        } else {
+            e = launch_cta_s<T, UP>(A + c0 + (int64_t)c0 * lda, nb, lda, strideA, batch, info, st,
+                                    c0 == 0 ? -1 : c0);
+        }
         if (e) return e;
         const int m = n - c0 - nb;
         if (m <= 0) break;

@@ -101,7 +101,7 @@ __device__ __forceinline__ void tile_of(int w, int &R, int &C)
 template <typename T, int NT, bool UP>
 __global__ void __launch_bounds__(TileGeom<T, NT>::kThreads, sizeof(T) == 4 ? 3 : 2)
 potrf_tiles_kernel(T *__restrict__ A, int n, int lda, int64_t strideA, int batch,
-                   int *__restrict__ info)
+                   int *__restrict__ info, int info_off)
 {
     using X = TileOps<T>;
     using Gm = TileGeom<T, NT>;
@@ -121,6 +121,9 @@ potrf_tiles_kernel(T *__restrict__ A, int n, int lda, int64_t strideA, int batch
     const bool diag = R == Cw;
     pdl_wait();
     pdl_trigger();
+    // a diagonal block of a larger matrix (info_off >= 0): skip a matrix that
+    // failed in an earlier block (one block per matrix: the read is uniform)
+    if (info_off >= 0 && info[mat] != 0) return;
 
     T t[32];
 #pragma unroll
@@ -196,12 +199,14 @@ potrf_tiles_kernel(T *__restrict__ A, int n, int lda, int64_t strideA, int batch
         int f = 0;
         for (int C = 0; C < NT && !f; ++C)
             if (bad_rows[C]) f = 32 * C + __ffs(bad_rows[C]);
-        info[mat] = f;
+        if (info_off < 0) info[mat] = f;
+        else if (f) info[mat] = info_off + f;
     }
 }
 
 template <typename T, int NT, bool UP>
-int launch_t(T *A, int n, int lda, int64_t strideA, int batch, int *info, cudaStream_t st)
+int launch_t(T *A, int n, int lda, int64_t strideA, int batch, int *info, cudaStream_t st,
+             int info_off)
 {
     using Gm = TileGeom<T, NT>;
     static DeviceOnce attrs;
@@ -212,34 +217,34 @@ int launch_t(T *A, int n, int lda, int64_t strideA, int batch, int *info, cudaSt
         }))
         return e;
     return launch_pdl(potrf_tiles_kernel<T, NT, UP>, dim3((unsigned)batch), dim3(Gm::kThreads),
-                      Gm::kBytes, st, A, n, lda, strideA, batch, info);
+                      Gm::kBytes, st, A, n, lda, strideA, batch, info, info_off);
 }
 
 template <typename T>
 int launch_tiles(T *A, int n, int lda, int64_t strideA, int batch, int *info, cudaStream_t st,
-                 bool upper)
+                 bool upper, int info_off)
 {
     if (n <= 64 || n > 128) return -1;
     if (n <= 96)
-        return upper ? launch_t<T, 3, true>(A, n, lda, strideA, batch, info, st)
-                     : launch_t<T, 3, false>(A, n, lda, strideA, batch, info, st);
-    return upper ? launch_t<T, 4, true>(A, n, lda, strideA, batch, info, st)
-                 : launch_t<T, 4, false>(A, n, lda, strideA, batch, info, st);
+        return upper ? launch_t<T, 3, true>(A, n, lda, strideA, batch, info, st, info_off)
+                     : launch_t<T, 3, false>(A, n, lda, strideA, batch, info, st, info_off);
+    return upper ? launch_t<T, 4, true>(A, n, lda, strideA, batch, info, st, info_off)
+                 : launch_t<T, 4, false>(A, n, lda, strideA, batch, info, st, info_off);
 }
 
 }  // namespace
 
 int launch_cpotrf_tiles(float *A, int n, int lda, int64_t strideA, int batch, int *info,
-                        cudaStream_t stream, bool upper)
+                        cudaStream_t stream, bool upper, int info_off)
 {
     return launch_tiles(reinterpret_cast<float2 *>(A), n, lda, strideA, batch, info, stream,
-                        upper);
+                        upper, info_off);
 }
 
 int launch_spotrf_tiles(float *A, int n, int lda, int64_t strideA, int batch, int *info,
-                        cudaStream_t stream, bool upper)
+                        cudaStream_t stream, bool upper, int info_off)
 {
-    return launch_tiles(A, n, lda, strideA, batch, info, stream, upper);
+    return launch_tiles(A, n, lda, strideA, batch, info, stream, upper, info_off);
 }
 
 int attrs_tiles(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem)
