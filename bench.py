@@ -37,15 +37,18 @@ UNIT = "matrices/s"
 L2_FLUSH_BYTES = 512 << 20
 REPLICA_CAP_BYTES = 96 << 30
 
-# DRAM bytes (read + write) per launch of the dominant kernel from one ncu
-# capture (dram__bytes_read.sum + dram__bytes_write.sum), with the sha256 of the
-# kernel's source files at capture time: a changed source reports null.
+# DRAM bytes (read + write) from one ncu pass over the workload's bench command
+# (dram__bytes_read.sum + dram__bytes_write.sum, one-pass metrics), with the
+# sha256 of the sources at capture time: a changed source reports null. Scope:
+# one launch of the workload's one kernel (n <= 128), or one whole call, all
+# its launches summed (the blocked route, whose `achieved` is per call too).
 TRAFFIC = {
-    # workload: (source files, sha256 prefix over them, bytes per launch)
-    "n32": (("matrix_dense_linear_gb300/csrc/potrf_warp.cu",
-             "matrix_dense_linear_gb300/csrc/bl_common.cuh"), "e7bebddfc929997e", 4219904),
-    "n64": (("matrix_dense_linear_gb300/csrc/potrf_warp.cu",
-             "matrix_dense_linear_gb300/csrc/bl_common.cuh"), "e7bebddfc929997e", 12660480),
+    # workload: (source files, sha256 prefix over them, bytes, scope)
+    "n32": (('matrix_dense_linear_gb300/csrc/potrf_warp.cu', 'matrix_dense_linear_gb300/csrc/bl_common.cuh'), "3256ed3948addbed", 4219904, "per launch"),
+    "n64": (('matrix_dense_linear_gb300/csrc/potrf_warp.cu', 'matrix_dense_linear_gb300/csrc/bl_common.cuh'), "3256ed3948addbed", 12660224, "per launch"),
+    "n128": (('matrix_dense_linear_gb300/csrc/potrf_cta.cu', 'matrix_dense_linear_gb300/csrc/cta_common.cuh', 'matrix_dense_linear_gb300/csrc/bl_common.cuh', 'matrix_dense_linear_gb300/csrc/tc_sm100.cuh'), "5ddde5688af11cca", 42150000, "per launch"),
+    "n256": (('matrix_dense_linear_gb300/csrc/potrf_blocked.cu', 'matrix_dense_linear_gb300/csrc/potrf_cta.cu', 'matrix_dense_linear_gb300/csrc/cta_common.cuh', 'matrix_dense_linear_gb300/csrc/trsm_tc.cu', 'matrix_dense_linear_gb300/csrc/syrk_tc.cu', 'matrix_dense_linear_gb300/csrc/tc_sm100.cuh', 'matrix_dense_linear_gb300/csrc/bl_common.cuh'), "a2c68e3b1c53561d", 1707000000, "per call (4 launches)"),
+    "n1024": (('matrix_dense_linear_gb300/csrc/potrf_blocked.cu', 'matrix_dense_linear_gb300/csrc/potrf_cta.cu', 'matrix_dense_linear_gb300/csrc/cta_common.cuh', 'matrix_dense_linear_gb300/csrc/trsm_tc.cu', 'matrix_dense_linear_gb300/csrc/syrk_tc.cu', 'matrix_dense_linear_gb300/csrc/tc_sm100.cuh', 'matrix_dense_linear_gb300/csrc/bl_common.cuh'), "a2c68e3b1c53561d", 5737000000, "per call (21 launches)"),
 }
 
 
@@ -70,11 +73,34 @@ def alg_bytes_per_matrix(n: int) -> float:
     return 4.0 * n * (n + 1)
 
 
-def launches_per_call(n: int) -> int:
+def launches_per_call(n: int, batch: int = 0) -> int:
+    """Kernels one lower-storage call on a 16-byte-aligned batch launches: one
+    for n <= 128; above, per 128-wide panel the diagonal factor, the panel
+    solve and the trailing update, except that the last panel has only its
+    factor and a one-tile trailing matrix is updated inside the panel solve
+    when the call holds at most 2048 matrices and no delayed update is pending
+    (the blocked driver's schedule)."""
     if n <= 128:
         return 1
     panels = (n + 127) // 128
-    return panels + 2 * (panels - 1)
+    count, pending = 0, False
+    sms = 152
+    for p in range(panels):
+        count += 1  # diagonal factor
+        m = n - 128 * (p + 1)
+        if m <= 0:
+            break
+        fuse = not pending and m <= 128 and (m < 128 or batch <= 2048)
+        count += 1  # panel solve
+        if fuse:
+            continue
+        t = (m + 127) // 128
+        if pending:
+            pending = False
+        elif m > 128 and batch * (t * (t + 1) // 2) >= 16 * sms:
+            pending = True
+        count += 1  # trailing update
+    return count
 
 
 def dominant_kernel(n: int) -> str:
@@ -100,7 +126,7 @@ def traffic_for(name: str, n: int):
     ent = TRAFFIC.get(name)
     if not ent:
         return None
-    srcs, sha, nbytes = ent
+    srcs, sha, nbytes, _ = ent
     h = hashlib.sha256()
     for src in srcs:
         with open(os.path.join(ROOT, src), "rb") as f:
@@ -438,9 +464,10 @@ def run_ours(args, rank: int, world: int, barrier) -> dict | None:
     per_call = ms / args.steps
     value = job_rate(world, batch, args.steps, ms)
     rf = roofline_entry(args.workload, n, batch, per_call, pk, sms)
-    nl = launches_per_call(n)
+    nl = launches_per_call(n, batch)
     roof = {"bound": rf["bound"], "achieved": rf["achieved"], "peak": rf["peak"],
             "unit": rf["unit"], "frac": rf["frac"], "traffic": traffic_for(args.workload, n),
+            "traffic_scope": TRAFFIC[args.workload][3] if args.workload in TRAFFIC else None,
             "kernel": dominant_kernel(n), "peak_source": pk["source"],
             "peak_note": ("HBM: measured copy bandwidth" if rf["bound"] == "hbm" else
                           f"FP32: {sms} SMs x 128 FMA x 2 x {pk['sm_max_mhz']:.0f} MHz")}
@@ -504,7 +531,9 @@ def run_ours(args, rank: int, world: int, barrier) -> dict | None:
                    "matrices_per_s": b2.batch / (pc / 1e3),
                    "gflops": b2.batch * flops_per_matrix(b2.n) / (pc / 1e3) / 1e9,
                    "roofline": {k: r2[k] for k in ("bound", "frac", "roof_ms")},
-                   "launches_per_call": launches_per_call(b2.n)}
+                   "launches_per_call": launches_per_call(b2.n, b2.batch)}
+            row["roofline"]["traffic"] = traffic_for(name, b2.n)
+            row["roofline"]["traffic_scope"] = TRAFFIC[name][3] if name in TRAFFIC else None
             # the same workload end to end through the host-buffer call
             e2 = e2e_steps(w2, min(args.steps, 5), 2, lambda: None)
             row["e2e"] = {"value": b2.batch * min(args.steps, 5) / (e2["ms"] / 1e3),
