@@ -11,12 +11,13 @@
 // compensated split, the accumulator in tensor memory.
 //
 // One block (256 threads) per output tile (I, K), I >= K. The k dimension goes
-// through shared memory 16 columns at a time, double-buffered: every thread
+// through shared memory 16 columns at a time in a ring of three buffers: every thread
 // loads a 4 x 4 block of one operand (4 columns x 4 rows, 16-byte loads along
 // the contiguous rows), splits it and writes it K-major (row r: k..k+3) into
 // the hi and lo tiles; thread 0 then issues 2 k-steps x 3 products of
-// tcgen05.mma (M = N = 128, K = 8) and commits them to the buffer's mbarrier,
-// which the stagers wait on before reusing the buffer. The next slice's global
+// tcgen05.mma (M = N = 128, K = 8) and commits them to the buffer's mbarrier;
+// thread 0 alone waits on it, one slice ahead of the buffer's reuse, and the
+// block barrier each slice has anyway passes that on. The next slice's global
 // loads are in flight while the current one is written. The epilogue reads the
 // accumulator back from tensor memory (warp w: rows 32(w%4).., columns
 // 64(w/4)..) and subtracts it from A22 in place, lower triangle only.
@@ -47,7 +48,8 @@ constexpr uint32_t kLbo = 128;             // K-adjacent core matrices
 constexpr uint32_t kSbo = (kKs / 4) * 128 + 16;  // row-group stride, +16 B: no bank conflicts
 constexpr uint32_t kTileBytes = 16 * kSbo;  // 128 rows
 constexpr uint32_t kStageBytes = 4 * kTileBytes;  // A hi, A lo, B hi, B lo
-constexpr int kSmemBytes = 2 * kStageBytes;
+constexpr int kStages = 3;                 // operand buffers in the ring
+constexpr int kSmemBytes = kStages * kStageBytes;
 constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at 2 GHz
 
 // failure injection for the give-up test (see set_fail_first_wait in launch.cuh)
@@ -72,7 +74,7 @@ syrk_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0, i
     // holds between two tiles of one matrix).
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ uint32_t tmem_base;
-    __shared__ __align__(8) uint64_t mbar[2];
+    __shared__ __align__(8) uint64_t mbar[kStages];
     __shared__ int sh_err;
 
     const int nt = narrow ? ntiles_col : ntiles_col * (ntiles_col + 1) / 2;  // tiles a matrix
@@ -126,8 +128,7 @@ syrk_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0, i
 
     if (tid == 0) {
         sh_err = 0;
-        tc::mbar_init(&mbar[0], 1);
-        tc::mbar_init(&mbar[1], 1);
+        for (int i = 0; i < kStages; ++i) tc::mbar_init(&mbar[i], 1);
         tc::fence_mbar_init();
     }
     if (warp == 0) {
@@ -171,11 +172,11 @@ syrk_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0, i
     int issued = 0;  // slices whose MMAs thread 0 has issued (same in every thread)
 #pragma unroll 1
     for (int s = 0; s < nslices; ++s) {
-        const int b = s & 1;
+        // a three-buffer ring: slice s goes to buffer s % 3, which the MMAs of
+        // slice s - 3 read; thread 0 saw those complete before the previous
+        // slice's barrier (below), so no thread waits here
+        const int b = s % kStages;
         if (s + 2 < nslices) load_slice(s + 2, nxt2);  // two slices in flight
-        if (s >= 2 && ((s == 2 && fail_first) ||
-                       !tc::mbar_wait(&mbar[b], ((s - 2) >> 1) & 1, kWaitCycles)))
-            ok = false;
         // transpose the 4 x 4 block to K-major rows, split into hi and lo
         uint8_t *st = smem + b * kStageBytes + (op ? 2 : 0) * kTileBytes;
         const float cv[4][4] = {{cur[0].x, cur[0].y, cur[0].z, cur[0].w},
@@ -192,7 +193,12 @@ syrk_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0, i
             *reinterpret_cast<float4 *>(st + kTileBytes + off) = make_float4(l[0], l[1], l[2], l[3]);
         }
         tc::fence_async_smem();
-        if (!ok) sh_err = 1;
+        // the buffer the next slice overwrites is read by the MMAs of slice
+        // s - 2: thread 0 alone waits for them, and the barrier tells the rest
+        if (tid == 0 && s >= 2 &&
+            ((s == 2 && fail_first) ||
+             !tc::mbar_wait(&mbar[(s - 2) % kStages], ((s - 2) / kStages) & 1, kWaitCycles)))
+            sh_err = 1;
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
@@ -249,8 +255,8 @@ syrk_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0, i
     // all MMAs issued before the last commit are complete once it arrives; the
     // outcome is made block-uniform (tcgen05.ld is a warp-collective)
     const int last = issued - 1;
-    if (ok && !tc::mbar_wait(&mbar[last & 1], (last >> 1) & 1, kWaitCycles)) ok = false;
-    if (!ok) sh_err = 1;
+    if (tid == 0 && ok && !tc::mbar_wait(&mbar[last % kStages], (last / kStages) & 1, kWaitCycles))
+        sh_err = 1;
     __syncthreads();
     ok = sh_err == 0;
     tc::fence_after_sync();
@@ -297,7 +303,7 @@ syrk_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0, i
     } else if (tid == 0) {
         info[mat] = -1;
         // let anything still in flight drain (bounded) before releasing TMEM
-        if (last >= 0) tc::mbar_wait(&mbar[last & 1], (last >> 1) & 1, kWaitCycles);
+        if (last >= 0) tc::mbar_wait(&mbar[last % kStages], (last / kStages) & 1, kWaitCycles);
     }
     tc::fence_before_sync();
     __syncthreads();

@@ -129,7 +129,7 @@ trinv_kernel(const float *__restrict__ A, int n, int lda, int64_t strideA, int c
 // L21 = A21 W^T: one block (256 threads) per 128 rows below the diagonal
 // block. Operand P = those rows of A21 (k = the panel's 128 columns), operand
 // Q = W (row c of W = row c of the inverse); the k dimension goes through
-// shared memory 16 columns at a time, double-buffered, each operand split into
+// shared memory 16 columns at a time (a ring of three buffers), each operand split into
 // a TF32-exact high part and the FP32 remainder and written K-major (threads
 // 0..127 stage P, 128..255 stage Q; 16-byte loads down the columns of P in
 // the lower storage, along the rows otherwise), and thread 0 issues three
@@ -145,7 +145,8 @@ constexpr uint32_t kLbo = 128;             // K-adjacent core matrices
 constexpr uint32_t kSbo = (kKs / 4) * 128 + 16;  // row-group stride, +16 B: no bank conflicts
 constexpr uint32_t kTileBytes = 16 * kSbo;  // 128 rows
 constexpr uint32_t kStageBytes = 4 * kTileBytes;  // P hi, P lo, Q hi, Q lo
-constexpr int kGemmSmem = 2 * kStageBytes;
+constexpr int kStages = 3;                 // operand buffers in the ring
+constexpr int kGemmSmem = kStages * kStageBytes;
 
 // failure injection for the give-up test (see set_fail_first_wait in launch.cuh)
 __device__ int g_fail_first_wait;
@@ -163,7 +164,7 @@ trsm_gemm_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
 {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ uint32_t tmem_base;
-    __shared__ __align__(8) uint64_t mbar[2];
+    __shared__ __align__(8) uint64_t mbar[kStages];
     __shared__ int sh_err;
 
     // one-dimensional grid, the row block fastest: a matrix's row blocks run
@@ -192,8 +193,7 @@ trsm_gemm_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
 
     if (tid == 0) {
         sh_err = 0;
-        tc::mbar_init(&mbar[0], 1);
-        tc::mbar_init(&mbar[1], 1);
+        for (int i = 0; i < kStages; ++i) tc::mbar_init(&mbar[i], 1);
         tc::fence_mbar_init();
     }
     if (warp == 0) {
@@ -237,11 +237,10 @@ trsm_gemm_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     int issued = 0;  // slices whose MMAs thread 0 has issued (same in every thread)
 #pragma unroll 1
     for (int s = 0; s < kSlices; ++s) {
-        const int b = s & 1;
+        // a three-buffer ring: slice s goes to buffer s % 3, whose MMAs (slice
+        // s - 3) thread 0 saw complete before the previous slice's barrier
+        const int b = s % kStages;
         if (s + 2 < kSlices) load_slice(s + 2, nxt2);  // two slices in flight
-        if (s >= 2 && ((s == 2 && fail_first) ||
-                       !tc::mbar_wait(&mbar[b], ((s - 2) >> 1) & 1, kWaitCycles)))
-            ok = false;
         uint8_t *st = smem + b * kStageBytes + (op ? 2 : 0) * kTileBytes;
         const float cv[4][4] = {{cur[0].x, cur[0].y, cur[0].z, cur[0].w},
                                 {cur[1].x, cur[1].y, cur[1].z, cur[1].w},
@@ -257,7 +256,12 @@ trsm_gemm_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
             *reinterpret_cast<float4 *>(st + kTileBytes + off) = make_float4(l[0], l[1], l[2], l[3]);
         }
         tc::fence_async_smem();
-        if (!ok) sh_err = 1;
+        // thread 0 waits for the MMAs of slice s - 2 (the buffer the next slice
+        // overwrites); the block barrier passes it on
+        if (tid == 0 && s >= 2 &&
+            ((s == 2 && fail_first) ||
+             !tc::mbar_wait(&mbar[(s - 2) % kStages], ((s - 2) / kStages) & 1, kWaitCycles)))
+            sh_err = 1;
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
@@ -292,8 +296,8 @@ trsm_gemm_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     }
 
     const int last = issued - 1;
-    if (ok && !tc::mbar_wait(&mbar[last & 1], (last >> 1) & 1, kWaitCycles)) ok = false;
-    if (!ok) sh_err = 1;
+    if (tid == 0 && ok && !tc::mbar_wait(&mbar[last % kStages], (last / kStages) & 1, kWaitCycles))
+        sh_err = 1;
     __syncthreads();
     ok = sh_err == 0;
     tc::fence_after_sync();
@@ -327,7 +331,7 @@ trsm_gemm_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     } else if (tid == 0) {
         info[mat] = -1;
         // let anything still in flight drain (bounded) before releasing TMEM
-        if (last >= 0) tc::mbar_wait(&mbar[last & 1], (last >> 1) & 1, kWaitCycles);
+        if (last >= 0) tc::mbar_wait(&mbar[last % kStages], (last / kStages) & 1, kWaitCycles);
     }
     tc::fence_before_sync();
     __syncthreads();

@@ -157,9 +157,30 @@ trsm_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0, i
     }
     cp_async_commit();
 
-    // the off-diagonal rows of column block 0
+    // -A21 rows, this thread's row: column chunks of 32 (16-byte loads along the
+    // row in the upper storage, one column at a time in the lower)
+    const float *g = Ab + (live ? lidx<UP>(R, c0, lda) : 0);  // g[c * xs] = (R, c0 + c)
+    auto load_chunk = [&](int q, float (&v)[32]) {
+        if constexpr (UP) {
+#pragma unroll
+            for (int c = 0; c < 32; c += 4) {
+                const float4 a = live ? *reinterpret_cast<const float4 *>(g + 32 * q + c)
+                                      : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                v[c] = -a.x; v[c + 1] = -a.y; v[c + 2] = -a.z; v[c + 3] = -a.w;
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) v[c] = live ? -g[(int64_t)(32 * q + c) * xs] : 0.0f;
+        }
+    };
+    // the off-diagonal rows of L11's column block 0 and the first half of the
+    // row travel together (one memory round trip instead of two); the second
+    // half follows once the first is in tensor memory
     LtPieces<UP> pc;
     pc.load(L11, lda, 0, tid);
+    float v0[32], v1[32];
+    load_chunk(0, v0);
+    load_chunk(1, v1);
     pc.stage(Lt, 0, tid);
 
     tc::fence_before_sync();
@@ -167,34 +188,12 @@ trsm_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0, i
     tc::fence_after_sync();
     const uint32_t tmem = tmem_base;
     const uint32_t tlane = tmem + ((uint32_t)(32 * warp) << 16);
-
-    // -A21 rows into tensor memory (two 32-column chunks in flight)
-    {
-        const float *g = Ab + (live ? lidx<UP>(R, c0, lda) : 0);  // g[c * xs] = (R, c0 + c)
-        float v0[32], v1[32];
-#pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
-            if constexpr (UP) {  // the row is contiguous: 16-byte loads
-#pragma unroll
-                for (int c = 0; c < 32; c += 4) {
-                    const float4 a = live ? *reinterpret_cast<const float4 *>(g + 64 * h + c)
-                                          : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                    const float4 b = live ? *reinterpret_cast<const float4 *>(g + 64 * h + 32 + c)
-                                          : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                    v0[c] = -a.x; v0[c + 1] = -a.y; v0[c + 2] = -a.z; v0[c + 3] = -a.w;
-                    v1[c] = -b.x; v1[c + 1] = -b.y; v1[c + 2] = -b.z; v1[c + 3] = -b.w;
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    v0[c] = live ? -g[(int64_t)(64 * h + c) * xs] : 0.0f;
-                    v1[c] = live ? -g[(int64_t)(64 * h + 32 + c) * xs] : 0.0f;
-                }
-            }
-            tc::tmem_st32(tlane + 64 * h, v0);
-            tc::tmem_st32(tlane + 64 * h + 32, v1);
-        }
-    }
+    tc::tmem_st32(tlane, v0);
+    tc::tmem_st32(tlane + 32, v1);
+    load_chunk(2, v0);
+    load_chunk(3, v1);
+    tc::tmem_st32(tlane + 64, v0);
+    tc::tmem_st32(tlane + 96, v1);
     cp_async_wait<0>();
     tc::fence_async_smem();
     tc::fence_before_sync();
