@@ -86,6 +86,7 @@ int set_fail_first_wait_trsm_tc(int every);  // tensor-core panel solve
 int set_fail_first_wait_syrk_tc(int every);  // tensor-core trailing update
 int set_fail_first_wait_tmem(int every);     // K2t
 int set_fail_first_wait_trsm_inv(int every); // the inverse-based panel solve's GEMM
+int set_fail_first_wait_cherk_tc(int every); // the complex tensor-core trailing update
 
 int launch_dpotrf(double *A, int n, int lda, int64_t strideA, int batch, int *info,
                   cudaStream_t stream, bool upper);
@@ -101,6 +102,11 @@ int launch_cpotrf_tiles(float *A, int n, int lda, int64_t strideA, int batch, in
 int launch_spotrf_tiles(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                         cudaStream_t stream, bool upper, int info_off = -1);
 int attrs_tiles(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem);
+// A22 -= L21 L21^H of the complex blocked path (lower storage, interleaved
+// complex floats, lda and strideA in complex elements) on the tensor cores;
+// returns 1 when the panels are not 16-byte aligned (the caller's FP32 path)
+int launch_cherk_tc(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
+                    cudaStream_t stream);
 int launch_cpotrf(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                   cudaStream_t stream, bool upper);
 // A: interleaved complex double; lda and strideA in complex elements

@@ -370,6 +370,14 @@ int launch_blocked_s(T *A, int n, int lda, int64_t strideA, int batch, int *info
         simple_trsm_kernel<T, UP><<<gt, 128, kDNb * (kDNb + 1) / 2 * sizeof(T), st>>>(
             A, n, lda, strideA, c0, info);
         if ((e = (int)cudaGetLastError())) return e;
+        // single-precision complex, lower storage, 16-byte aligned: the trailing
+        // update on the tensor cores (cherk_tc.cu); else the FP32 tiles below
+        if constexpr (std::is_same<T, float2>::value && !UP) {
+            e = launch_cherk_tc(reinterpret_cast<float *>(A), n, lda, strideA, batch, info, c0,
+                                st);
+            if (e == 0) continue;
+            if (e != 1) return e;
+        }
         const int Tn = (m + kDTile - 1) / kDTile;
         dim3 gs((unsigned)batch, (unsigned)(Tn * (Tn + 1) / 2));
         simple_syrk_kernel<T, UP><<<gs, 256, 0, st>>>(A, n, lda, strideA, c0, info);

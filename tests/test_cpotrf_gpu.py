@@ -201,3 +201,42 @@ def test_cpotrf_codes():
     Z = torch.zeros(4, dtype=torch.complex128, device="cuda")
     assert bl.cpotrf_batched(Z.data_ptr() + 8, 2, 2, 4, 1, info, double=True) == -1
     assert bl.cpotrf_batched(Z, 2, 1, 4, 1, info) == -3
+
+
+@pytest.mark.parametrize("n", [256, 384, 520])
+def test_cpotrf_tensor_core_update(n):
+    """Single-precision complex, lower storage, 16-byte-aligned batches above
+    n = 128: the trailing update runs on the tensor cores (3xTF32 real and
+    imaginary products); several trailing tiles, one of them ragged at 520."""
+    batch = 5
+    mats = [_herm(n, 4000 + 10 * n + b) for b in range(batch)]
+    buf = _pack(mats, n, n, n * n, "L", diag_imag=0.75)
+    out, info = _run(buf, n, n, n * n, batch, "L")
+    _check(buf, out, info, n, n, n * n, batch, "L", f"tensor-core update n={n}")
+
+
+def test_cpotrf_tensor_core_update_give_up():
+    """Class 6 of the failure injection: the complex tensor-core update gives up
+    at its first bounded wait for every third matrix: those report -1, the
+    others match the oracle, nothing outside the triangles changes, and the next
+    call factors the whole batch."""
+    import matrix_dense_linear_gb300 as bl
+    lib = bl.library()
+    n, batch = 384, 6
+    mats = [_herm(n, 4500 + b) for b in range(batch)]
+    buf = _pack(mats, n, n, n * n, "L")
+    assert lib.bl_debug_fail_first_wait(6, 3) == 0
+    try:
+        out, info = _run(buf, n, n, n * n, batch, "L")
+    finally:
+        assert lib.bl_debug_fail_first_wait(6, 0) == 0
+    assert [int(x) for x in info] == [-1 if b % 3 == 0 else 0 for b in range(batch)], list(info)
+    pat = _pattern(n, n, n * n, batch, buf.size, "L")
+    assert np.array_equal(out.view(np.uint64)[~pat], buf.view(np.uint64)[~pat])
+    keep = [b for b in range(batch) if b % 3]
+    sub = _pack([mats[b] for b in keep], n, n, n * n, "L")
+    sub_out = np.concatenate([out[b * n * n:(b + 1) * n * n] for b in keep])
+    _check(sub, sub_out, np.zeros(len(keep), dtype=np.int32), n, n, n * n, len(keep), "L",
+           "give-up: untouched matrices")
+    out2, info2 = _run(buf, n, n, n * n, batch, "L")
+    _check(buf, out2, info2, n, n, n * n, batch, "L", "after the give-up")
