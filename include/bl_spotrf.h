@@ -371,7 +371,8 @@ int bl_spotrf_batched_static(float *A, int n, int lda, int64_t strideA, int batc
  * 4 the tensor-memory kernel (route 4), 5 the tensor-core product of the
  * inverse-based panel solve (bl_spotrf_batched_ws), 6 the tensor-core trailing
  * update of the single-precision complex call (bl_cpotrf_batched, n > 128,
- * lower storage, 16-byte-aligned batches). Synchronous with the host; call it
+ * lower storage, 16-byte-aligned batches), 7 the tensor-core panel solve of
+ * the same call. Synchronous with the host; call it
  * while no other work of the library runs. Returns 0, -1 (unknown class), -2
  * (every < 0) or a cudaError_t.
  */

@@ -433,6 +433,7 @@ int bl_debug_fail_first_wait(int kernel_class, int every)
     case 4: return bl::set_fail_first_wait_tmem(every);
     case 5: return bl::set_fail_first_wait_trsm_inv(every);
     case 6: return bl::set_fail_first_wait_cherk_tc(every);
+    case 7: return bl::set_fail_first_wait_ctrsm_tc(every);
     default: return -1;
     }
 }

@@ -87,6 +87,7 @@ int set_fail_first_wait_syrk_tc(int every);  // tensor-core trailing update
 int set_fail_first_wait_tmem(int every);     // K2t
 int set_fail_first_wait_trsm_inv(int every); // the inverse-based panel solve's GEMM
 int set_fail_first_wait_cherk_tc(int every); // the complex tensor-core trailing update
+int set_fail_first_wait_ctrsm_tc(int every); // the complex tensor-core panel solve
 
 int launch_dpotrf(double *A, int n, int lda, int64_t strideA, int batch, int *info,
                   cudaStream_t stream, bool upper);
@@ -106,6 +107,11 @@ int attrs_tiles(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem);
 // complex floats, lda and strideA in complex elements) on the tensor cores;
 // returns 1 when the panels are not 16-byte aligned (the caller's FP32 path)
 int launch_cherk_tc(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
+                    cudaStream_t stream);
+// L21 = A21 L11^{-H} of the complex blocked path (lower storage, the same
+// conventions) with the block updates on the tensor cores; returns 1 when the
+// panels are not 16-byte aligned (the caller's FP32 kernel)
+int launch_ctrsm_tc(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
                     cudaStream_t stream);
 int launch_cpotrf(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                   cudaStream_t stream, bool upper);

@@ -22,6 +22,10 @@
 //                       (16 for complex);
 //   simple_syrk_kernel  its trailing update on 64 x 64 tiles on or below the
 //                       diagonal, k staged through shared memory.
+// Single-precision complex batches in the lower storage with 16-byte-aligned
+// panels take the tensor-core forms of the panel solve and the trailing update
+// instead (ctrsm_tc.cu, cherk_tc.cu), and their diagonal blocks above order 64
+// the warp-per-tile register kernel (potrf_tiles.cu).
 #include <mutex>
 #include <type_traits>
 
@@ -366,10 +370,21 @@ int launch_blocked_s(T *A, int n, int lda, int64_t strideA, int batch, int *info
         if (e) return e;
         const int m = n - c0 - nb;
         if (m <= 0) break;
-        dim3 gt((unsigned)batch, (unsigned)((m + 127) / 128));
-        simple_trsm_kernel<T, UP><<<gt, 128, kDNb * (kDNb + 1) / 2 * sizeof(T), st>>>(
-            A, n, lda, strideA, c0, info);
-        if ((e = (int)cudaGetLastError())) return e;
+        // single-precision complex, lower storage, 16-byte aligned: the panel
+        // solve's block updates on the tensor cores (ctrsm_tc.cu); else the
+        // FP32 kernel
+        e = 1;
+        if constexpr (std::is_same<T, float2>::value && !UP) {
+            e = launch_ctrsm_tc(reinterpret_cast<float *>(A), n, lda, strideA, batch, info, c0,
+                                st);
+            if (e != 0 && e != 1) return e;
+        }
+        if (e == 1) {
+            dim3 gt((unsigned)batch, (unsigned)((m + 127) / 128));
+            simple_trsm_kernel<T, UP><<<gt, 128, kDNb * (kDNb + 1) / 2 * sizeof(T), st>>>(
+                A, n, lda, strideA, c0, info);
+            if ((e = (int)cudaGetLastError())) return e;
+        }
         // single-precision complex, lower storage, 16-byte aligned: the trailing
         // update on the tensor cores (cherk_tc.cu); else the FP32 tiles below
         if constexpr (std::is_same<T, float2>::value && !UP) {

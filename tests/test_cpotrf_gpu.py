@@ -203,11 +203,12 @@ def test_cpotrf_codes():
     assert bl.cpotrf_batched(Z, 2, 1, 4, 1, info) == -3
 
 
-@pytest.mark.parametrize("n", [256, 384, 520])
+@pytest.mark.parametrize("n", [130, 256, 384, 520])
 def test_cpotrf_tensor_core_update(n):
     """Single-precision complex, lower storage, 16-byte-aligned batches above
-    n = 128: the trailing update runs on the tensor cores (3xTF32 real and
-    imaginary products); several trailing tiles, one of them ragged at 520."""
+    n = 128: the panel solve's block updates and the trailing update run on the
+    tensor cores (3xTF32 real and imaginary products); several row blocks and
+    trailing tiles, ragged ones at 130 and 520."""
     batch = 5
     mats = [_herm(n, 4000 + 10 * n + b) for b in range(batch)]
     buf = _pack(mats, n, n, n * n, "L", diag_imag=0.75)
@@ -215,21 +216,23 @@ def test_cpotrf_tensor_core_update(n):
     _check(buf, out, info, n, n, n * n, batch, "L", f"tensor-core update n={n}")
 
 
-def test_cpotrf_tensor_core_update_give_up():
-    """Class 6 of the failure injection: the complex tensor-core update gives up
-    at its first bounded wait for every third matrix: those report -1, the
-    others match the oracle, nothing outside the triangles changes, and the next
-    call factors the whole batch."""
+@pytest.mark.parametrize("cls", [6, 7])
+def test_cpotrf_tensor_core_give_up(cls):
+    """Classes 6 and 7 of the failure injection: the complex tensor-core
+    trailing update (6) or panel solve (7) gives up at its first bounded wait
+    for every third matrix: those report -1, the others match the oracle,
+    nothing outside the triangles changes, and the next call factors the whole
+    batch."""
     import matrix_dense_linear_gb300 as bl
     lib = bl.library()
     n, batch = 384, 6
     mats = [_herm(n, 4500 + b) for b in range(batch)]
     buf = _pack(mats, n, n, n * n, "L")
-    assert lib.bl_debug_fail_first_wait(6, 3) == 0
+    assert lib.bl_debug_fail_first_wait(cls, 3) == 0
     try:
         out, info = _run(buf, n, n, n * n, batch, "L")
     finally:
-        assert lib.bl_debug_fail_first_wait(6, 0) == 0
+        assert lib.bl_debug_fail_first_wait(cls, 0) == 0
     assert [int(x) for x in info] == [-1 if b % 3 == 0 else 0 for b in range(batch)], list(info)
     pat = _pattern(n, n, n * n, batch, buf.size, "L")
     assert np.array_equal(out.view(np.uint64)[~pat], buf.view(np.uint64)[~pat])
@@ -240,3 +243,20 @@ def test_cpotrf_tensor_core_update_give_up():
            "give-up: untouched matrices")
     out2, info2 = _run(buf, n, n, n * n, batch, "L")
     _check(buf, out2, info2, n, n, n * n, batch, "L", "after the give-up")
+
+
+def test_cpotrf_tensor_core_info():
+    """Failed pivots in the later panels of the tensor-core complex path: the
+    panel solve and the update skip a failed matrix, info is the oracle's and the
+    leading block before the failure matches."""
+    n = 384
+    ks = [130, 300, 383, 5]
+    mats = [_herm(n, 4700 + b) for b in range(6)]
+    for t, k in enumerate(ks):
+        A = mats[t]
+        q = (A[:k, k].conj() @ np.linalg.solve(A[:k, :k], A[:k, k])).real
+        A[k, k] = q - 0.5
+    buf = _pack(mats, n, n, n * n, "L")
+    out, info = _run(buf, n, n, n * n, 6, "L")
+    assert list(info[:4]) == [k + 1 for k in ks] and info[4] == 0 and info[5] == 0, list(info)
+    _check(buf, out, info, n, n, n * n, 6, "L", "tensor-core info")

@@ -141,7 +141,7 @@ def test_injection_argument_checks():
     import matrix_dense_linear_gb300 as bl
     lib = bl.library()
     assert lib.bl_debug_fail_first_wait(0, 1) == -1
-    assert lib.bl_debug_fail_first_wait(7, 1) == -1
+    assert lib.bl_debug_fail_first_wait(8, 1) == -1
     assert lib.bl_debug_fail_first_wait(1, -1) == -2
-    for k in (1, 2, 3, 4, 5, 6):
+    for k in (1, 2, 3, 4, 5, 6, 7):
         assert lib.bl_debug_fail_first_wait(k, 0) == 0
