@@ -32,6 +32,7 @@ namespace bl {
 namespace {
 
 constexpr int kLd = 36;  // leading dimension of a 32 x 32 block in shared memory
+constexpr int kWaveMaxN = 1024;  // the wavefront form: a warp per row block, 32 warps at most
 
 template <int W>
 struct TrsShared {
@@ -286,6 +287,181 @@ potrs_kernel(const float *__restrict__ L, int n, int lda, int64_t strideA, float
     }
 }
 
+// ---------------------------------------------------------------------------
+// Wavefront form (one right-hand side, n <= 1024): one block of NB =
+// ceil(n / 32) warps per system, warp i owning row block i (lane = row). Both
+// solves run as a wavefront over the diagonal blocks with one block barrier a
+// step:
+//   forward step s:  warp s solves Y_s = L_ss^{-1} b_s and publishes it;
+//                    every warp i > s subtracts L_is Y_s from its b_i
+//   backward step s: warp s solves X_s = L_ss^{-T} y_s, publishes and stores
+//                    it; every warp i < s subtracts L_si^T X_s
+// so the block products of a step run on all warps at once and a system's
+// critical path is the chain of 2 NB diagonal solves, not the ~n^2 / 512 block
+// products of the left-looking form above. Inside a diagonal solve each solved
+// entry goes to the other lanes by a warp shuffle (one right-hand side: one
+// value a step). The L block a warp needs at the next step is loaded into
+// registers while the current step's solve runs; the warp's own diagonal block
+// stays in shared memory (row r at D[33 r]); Y never leaves the chip (the
+// backward pass starts from the warp's own y_i). Measured against the
+// left-looking form with several right-hand sides a block, the wavefront
+// loses (most of a system's warps wait at the barriers while one solves, and
+// fewer systems fit an SM), so it takes one right-hand side only.
+
+// lc[k] = element (r0 + lane, c0 + k) of L when ROWS (lane = row of L), else
+// element (r0 + k, c0 + lane); zero outside the matrix. The memory layout of
+// the storage decides which of the two is contiguous per lane (VEC: 16-byte
+// loads there when the whole block is inside).
+template <bool UP, bool VEC, bool ROWS>
+__device__ __forceinline__ void load_block(float (&lc)[32], const float *Lb, int lda, int n, int r0,
+                                           int c0, int lane)
+{
+    // per lane: the fixed index and the 32 running ones
+    const int fixed = (ROWS ? r0 : c0) + lane;
+    const int run0 = ROWS ? c0 : r0;
+    const bool fv = fixed < n;
+    // contiguous per lane: lower storage with the running index a row (the
+    // lane a column), upper storage with the running index a column
+    constexpr bool contig = UP ? ROWS : !ROWS;
+    if constexpr (contig) {
+        // element (run0 + k, fixed) [lower] or (fixed, run0 + k) [upper] at
+        // run0 + k + fixed * lda
+        const float *p = Lb + run0 + (int64_t)(fv ? fixed : 0) * lda;
+        if (VEC && fv && run0 + 32 <= n) {
+#pragma unroll
+            for (int k = 0; k < 32; k += 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(p + k);
+                lc[k] = v.x; lc[k + 1] = v.y; lc[k + 2] = v.z; lc[k + 3] = v.w;
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) lc[k] = fv && run0 + k < n ? p[k] : 0.0f;
+        }
+    } else {
+        // element (fixed, run0 + k) [lower] or (run0 + k, fixed) [upper] at
+        // fixed + (run0 + k) * lda: coalesced over the lanes
+        const float *p = Lb + (fv ? fixed : 0) + (int64_t)run0 * lda;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) lc[k] = fv && run0 + k < n ? p[(int64_t)k * lda] : 0.0f;
+    }
+}
+
+template <int MAXW, bool UP, bool VEC>
+__global__ void __launch_bounds__(32 * MAXW, 32 / MAXW)
+potrs_wave_kernel(const float *__restrict__ L, int n, int lda, int64_t strideA, float *__restrict__ B,
+                  int64_t strideB, const int *__restrict__ info)
+{
+    extern __shared__ __align__(16) float wsm[];
+    const int NB = (n + 31) >> 5;
+    const int64_t sys = blockIdx.x;
+    pdl_wait();
+    pdl_trigger();
+    if (info != nullptr && info[sys] != 0) return;
+    const float *Lb = L + sys * strideA;
+    float *Bb = B + sys * strideB;
+    const int tid = threadIdx.x, i = tid >> 5, lane = tid & 31;
+    const int row = 32 * i + lane;
+    const bool rv = row < n;
+    float *D = wsm + i * (32 * 33);  // D[33 r + k] = L(32i + r, 32i + k), k <= r (else 0)
+    float *Ys = wsm + NB * (32 * 33);  // [2][32]: the block published last
+
+    // the warp's diagonal block (rows past n: the identity) and its entries of b
+#pragma unroll 4
+    for (int k = 0; k < 32; ++k) {
+        const int col = 32 * i + k;
+        D[lane * 33 + k] = rv && k <= lane ? Lb[lidx<UP>(row, col, lda)]
+                                           : (k == lane ? 1.0f : 0.0f);
+    }
+    float acc = rv ? Bb[row] : 0.0f;
+    float lc[32];
+    if (i > 0) load_block<UP, VEC, true>(lc, Lb, lda, n, 32 * i, 0, lane);
+    __syncwarp();
+    const float rinv = 1.0f / D[lane * 33 + lane];
+
+    // ---------------- forward: L y = b ----------------
+#pragma unroll 1
+    for (int s = 0; s < NB; ++s) {
+        float *Y = Ys + (s & 1) * 32;
+        if (i == s) {
+            // y_k = acc_k / l_kk from lane k; lanes r > k subtract l_rk y_k
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                const float l = D[lane * 33 + k];
+                const float yk = __shfl_sync(0xffffffffu, acc * rinv, k);
+                acc = lane == k ? yk : (lane > k ? fmaf(-l, yk, acc) : acc);
+            }
+            Y[lane] = acc;
+        }
+        __syncthreads();
+        if (i > s) {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) acc = fmaf(-lc[k], Y[k], acc);
+            if (i > s + 1) load_block<UP, VEC, true>(lc, Lb, lda, n, 32 * i, 32 * (s + 1), lane);
+        }
+    }
+
+    // ---------------- backward: L^T x = y (acc holds y_i) ----------------
+    if (i < NB - 1) load_block<UP, VEC, false>(lc, Lb, lda, n, 32 * (NB - 1), 32 * i, lane);
+#pragma unroll 1
+    for (int s = NB - 1; s >= 0; --s) {
+        float *X = Ys + (s & 1) * 32;
+        if (i == s) {
+            // x_k = acc_k / l_kk from lane k (k from the bottom); lanes r < k subtract l_kr x_k
+#pragma unroll
+            for (int k = 31; k >= 0; --k) {
+                const float l = D[k * 33 + lane];
+                const float xk = __shfl_sync(0xffffffffu, acc * rinv, k);
+                acc = lane == k ? xk : (lane < k ? fmaf(-l, xk, acc) : acc);
+            }
+            X[lane] = acc;
+            if (rv) Bb[row] = acc;
+        }
+        __syncthreads();
+        if (i < s) {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) acc = fmaf(-lc[k], X[k], acc);
+            if (i < s - 1) load_block<UP, VEC, false>(lc, Lb, lda, n, 32 * (s - 1), 32 * i, lane);
+        }
+    }
+}
+
+size_t wave_smem(int n)
+{
+    const int NB = (n + 31) / 32;
+    return (size_t)NB * 32 * 33 * 4 + (size_t)2 * 32 * 4;
+}
+
+template <int MAXW, bool UP, bool VEC>
+int launch_wave_t(const float *L, int n, int lda, int64_t strideA, float *B, int64_t strideB,
+                  int batch, const int *info, cudaStream_t stream)
+{
+    static DeviceOnce attrs;
+    if (const int e = attrs.run([] {
+            return cudaFuncSetAttribute(potrs_wave_kernel<MAXW, UP, VEC>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)wave_smem(32 * MAXW));
+        }))
+        return e;
+    const int NB = (n + 31) / 32;
+    return launch_pdl(potrs_wave_kernel<MAXW, UP, VEC>, dim3((unsigned)batch), dim3(32 * NB),
+                      wave_smem(n), stream, L, n, lda, strideA, B, strideB, info);
+}
+
+template <int MAXW>
+int launch_wave(const float *L, int n, int lda, int64_t strideA, float *B, int64_t strideB,
+                int batch, const int *info, cudaStream_t stream, bool upper)
+{
+    const bool vec = ((reinterpret_cast<uintptr_t>(L) & 15) == 0) && (lda & 3) == 0 &&
+                     (strideA & 3) == 0;
+#define BL_WAVE_ARGS L, n, lda, strideA, B, strideB, batch, info, stream
+    if (upper)
+        return vec ? launch_wave_t<MAXW, true, true>(BL_WAVE_ARGS)
+                   : launch_wave_t<MAXW, true, false>(BL_WAVE_ARGS);
+    return vec ? launch_wave_t<MAXW, false, true>(BL_WAVE_ARGS)
+               : launch_wave_t<MAXW, false, false>(BL_WAVE_ARGS);
+#undef BL_WAVE_ARGS
+}
+
 template <int W, int C>
 int launch_wc(const float *L, int n, int lda, int64_t strideA, float *B, int nrhs, int ldb,
               int64_t strideB, int batch, const int *info, cudaStream_t stream, bool upper)
@@ -306,6 +482,15 @@ int launch_potrs(const float *L, int n, int lda, int64_t strideA, float *B, int 
                  int64_t strideB, int batch, const int *info, cudaStream_t stream, bool upper)
 {
 #define BL_POTRS_ARGS L, n, lda, strideA, B, nrhs, ldb, strideB, batch, info, stream, upper
+    // one right-hand side: the wavefront form (8, 16 or 32 warps at most, for
+    // 64 registers a thread); the left-looking form otherwise
+    if (nrhs == 1 && n <= kWaveMaxN) {
+        const int NB = (n + 31) / 32;
+        if (NB <= 8) return launch_wave<8>(L, n, lda, strideA, B, strideB, batch, info, stream, upper);
+        if (NB <= 16)
+            return launch_wave<16>(L, n, lda, strideA, B, strideB, batch, info, stream, upper);
+        return launch_wave<32>(L, n, lda, strideA, B, strideB, batch, info, stream, upper);
+    }
     if (nrhs <= 1) return launch_wc<1, 1>(BL_POTRS_ARGS);
     if (nrhs <= 2) return launch_wc<1, 2>(BL_POTRS_ARGS);
     if (nrhs <= 4) return launch_wc<1, 4>(BL_POTRS_ARGS);
