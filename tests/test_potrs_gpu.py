@@ -124,6 +124,32 @@ def test_potrs_parity(n, nrhs):
         _check_solution(Ls[b], Bs[b], X, X_ref[b], f"n={n} nrhs={nrhs} system {b}")
 
 
+@pytest.mark.parametrize("aligned", [True, False])
+@pytest.mark.parametrize("n", [32, 97, 256, 300, 520, 1000])
+def test_potrs_one_rhs_wavefront(n, aligned):
+    """One right-hand side runs the wavefront form (a warp per 32-row block;
+    8, 16 or 32 warps at most by n): every block size, the ragged last row
+    block, and both forms of the L loads (16-byte ones when lda and the
+    matrix stride are multiples of four floats, scalar ones otherwise)."""
+    batch = 3
+    if aligned:
+        lda = (n + 3) // 4 * 4 + 4
+        strideA, ldb, strideB = lda * n, n + 4, n + 8
+    else:
+        lda = n + 3
+        strideA, ldb, strideB = lda * n + 5, n + 1, n + 3
+    lbuf, Ls = _factors(n, batch, 1700 + n, lda, strideA)
+    bbuf, Bs = _rhs(n, 1, batch, 1750 + n, ldb, strideB)
+    l_after, b_after = _gpu_potrs(lbuf, n, lda, strideA, bbuf, 1, ldb, strideB, batch)
+    assert np.array_equal(l_after.view(np.uint32), lbuf.view(np.uint32))
+    pat = _solution_pattern(n, 1, ldb, strideB, batch, bbuf.size)
+    assert np.array_equal(b_after.view(np.uint32)[~pat], bbuf.view(np.uint32)[~pat])
+    X_ref, _ = oracle.potrs_batched(lbuf, n, lda, strideA, bbuf, 1, ldb, strideB, batch)
+    for b in range(batch):
+        _check_solution(Ls[b], Bs[b], _view(b_after, n, 1, ldb, strideB, b), X_ref[b],
+                        f"n={n} aligned={aligned} system {b}")
+
+
 def test_potrs_large_order():
     n, nrhs, batch = 1024, 32, 2
     lbuf, Ls = _factors(n, batch, 1100, n, n * n)

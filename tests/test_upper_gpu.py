@@ -257,6 +257,52 @@ def test_upper_solve_parity(n, nrhs):
     assert np.array_equal(out.view(np.uint32)[~pat], bbuf.view(np.uint32)[~pat])
 
 
+@pytest.mark.parametrize("aligned", [True, False])
+@pytest.mark.parametrize("n", [97, 300, 700])
+def test_upper_solve_one_rhs(n, aligned):
+    """One right-hand side with U (the wavefront form, 8, 16 and 32 warps at
+    most): U's rows are contiguous there, so the forward pass reads them with
+    16-byte loads when lda and the stride are multiples of four floats."""
+    import torch
+
+    import matrix_dense_linear_gb300 as bl
+    batch = 3
+    if aligned:
+        lda = (n + 3) // 4 * 4
+        strideA, ldb, strideB = lda * n + 4, n, n + 4
+    else:
+        lda = n + 1
+        strideA, ldb, strideB = lda * n + 3, n + 2, n + 5
+    Us = []
+    for A in _mats(n, batch, 1300 + n):
+        Uo, info = oracle.potrf_one(A, uplo="U")
+        assert info == 0
+        Us.append(np.triu(Uo).astype(np.float32))
+    ubuf = _pack_upper(Us, n, lda, strideA)
+    bbuf, Bs = _rhs(n, 1, batch, 1350 + n, ldb, strideB)
+    du = torch.from_numpy(ubuf.copy()).cuda()
+    db = torch.from_numpy(bbuf.copy()).cuda()
+    assert bl.spotrs_batched_uplo("U", du, n, lda, strideA, db, 1, ldb, strideB, batch) == 0
+    torch.cuda.synchronize()
+    assert np.array_equal(du.cpu().numpy().view(np.uint32), ubuf.view(np.uint32))
+    out = db.cpu().numpy()
+    X_ref, _ = oracle.potrs_batched(ubuf, n, lda, strideA, bbuf, 1, ldb, strideB, batch,
+                                    uplo="U")
+    for b in range(batch):
+        X = _sol(out, n, 1, ldb, strideB, b).astype(np.float64)
+        Ud = Us[b].astype(np.float64)
+        res = np.linalg.norm(Bs[b].astype(np.float64) - Ud.T @ (Ud @ X))
+        bound = checks.RECON_PER_N * n * np.linalg.norm(Ud) ** 2 * np.linalg.norm(X)
+        assert res <= bound, f"n={n} b={b}: residual {res:.3e} > {bound:.3e}"
+        s = np.linalg.svd(Ud, compute_uv=False)
+        err = np.abs(X - X_ref[b]).max() / np.abs(X_ref[b]).max()
+        assert err <= 4 * n * U * (s[0] / s[-1]) ** 2
+    pat = np.zeros(bbuf.size, dtype=bool)
+    for b in range(batch):
+        pat[b * strideB: b * strideB + n] = True
+    assert np.array_equal(out.view(np.uint32)[~pat], bbuf.view(np.uint32)[~pat])
+
+
 @pytest.mark.parametrize("n,nrhs", [(20, 3), (64, 9), (150, 4)])
 def test_upper_sposv(n, nrhs):
     import torch
