@@ -318,10 +318,11 @@ def e2e_steps(w: DeviceWorkload, steps: int, warmup: int, barrier) -> dict:
     """Same metric through the public host-buffer call (bl_spotrf_batched_host)
     on pinned host buffers, a fresh input each step. For n <= 128 the kernel
     reads the lower triangles from host memory and writes the factors back
-    there (no staging copies; the bytes crossing the host link are the lower
-    triangles and info); above, every step copies the batch to the device,
-    factors it, and copies matrices + info back, in two slices on two streams
-    so the copies of one overlap the factorization and copies of the other."""
+    there (no staging copies); above, per slice (eight on two streams) a kernel
+    copies the lower triangles to the device, the slice is factored and a
+    kernel copies the factors and info back, so one slice's copy in overlaps
+    another's factorization and copy back. Either way the bytes crossing the
+    host link are the lower triangles and info."""
     import torch
 
     import matrix_dense_linear_gb300 as bl
@@ -349,12 +350,13 @@ def e2e_steps(w: DeviceWorkload, steps: int, warmup: int, barrier) -> dict:
         torch.cuda.synchronize()
         total += e0.elapsed_time(e1)
     assert not info_h.any().item(), "e2e run reported a failed factorization"
+    tri = 4 * bt.n * (bt.n + 1) // 2 * bt.batch
     if bt.n <= 128:  # in place over the host link: the lower triangles each way
-        tri = 4 * bt.n * (bt.n + 1) // 2 * bt.batch
         return {"ms": total, "h2d": tri, "d2h": tri + 4 * bt.batch,
                 "mode": "in place on pinned host memory over the host link (no staging copies)"}
-    return {"ms": total, "h2d": bt.buf.nbytes, "d2h": bt.buf.nbytes + 4 * bt.batch,
-            "mode": "copies in, factor, copies out; two slices on two streams"}
+    return {"ms": total, "h2d": tri, "d2h": tri + 4 * bt.batch,
+            "mode": "per slice: lower triangles copied in by kernel, factor, factors and info "
+                    "copied back by kernel; eight slices on two streams"}
 
 
 def oracle_rate(bt, seconds: float = 3.0, max_matrices: int | None = None,

@@ -148,8 +148,12 @@ int bl_spotrf_kernel_info(int route, int n, int *regs, int *local_bytes, int *st
  * from cudaHostAlloc / cudaMallocHost / cudaHostRegister, e.g. a pinned torch
  * tensor) there are no copies: the one kernel of those orders reads each
  * lower-triangle element from host memory and writes its result back there,
- * on streams[0] (A_dev and info_dev are not touched). Other buffers take the
- * copy path above.
+ * on streams[0] (A_dev and info_dev are not touched). For larger n on such
+ * buffers, kernels copy only the lower triangles: per slice, host -> A_dev,
+ * the factorization, then the factors and info back (only A_dev's lower
+ * triangles are written; chunks <= 0 here means four slices per stream, and
+ * the slices are issued one after another so that copies in and out of
+ * different slices overlap). Other buffers take the copy path above.
  *
  * Returns what bl_spotrf_batched returns (argument indices as there, with the
  * device buffers checked as A and info; -11 when streams is NULL or nstreams

@@ -177,11 +177,35 @@ int bl_spotrf_batched_host(float *A_host, int n, int lda, int64_t strideA, int b
     // each element once each way), with no staging copies; on GB300 the
     // NVLink-C2C link carries that at about 1.5 times the rate of the copy
     // engines (1024 matrices of order 64: 137 against 207 us).
-    if (n <= kCtaMaxN) {
-        float *Am = mapped_host(A_host);
-        int *im = mapped_host(info_host);
-        if (Am && im)
-            return run(Am, n, lda, strideA, batch, im, streams[0], BL_ROUTE_AUTO, false, true);
+    float *Am = n > 0 ? mapped_host(A_host) : nullptr;
+    int *im = mapped_host(info_host);
+    if (n <= kCtaMaxN && Am && im)
+        return run(Am, n, lda, strideA, batch, im, streams[0], BL_ROUTE_AUTO, false, true);
+    // Larger orders on such buffers: per slice, a kernel copies the lower
+    // triangles host -> device, the slice is factored, a kernel copies the
+    // factors and info back: half the bytes of whole spans, each way. Issued
+    // slice by slice (four a stream unless chunks says otherwise), so that one
+    // stream's copy in runs while another's copy back does and the link
+    // carries both directions at once.
+    if (Am && im) {
+        if (chunks <= 0) chunks = 4 * nstreams;
+        if (chunks > batch) chunks = batch;
+        for (int c = 0; c < chunks; ++c) {
+            const int b0 = (int)((int64_t)batch * c / chunks);
+            const int b1 = (int)((int64_t)batch * (c + 1) / chunks);
+            if (b1 <= b0) continue;
+            cudaStream_t s = streams[c % nstreams];
+            const int64_t off = (int64_t)b0 * strideA;
+            if ((e = bl::launch_tri_copy(Am + off, A_dev + off, n, lda, strideA, b1 - b0, nullptr,
+                                         nullptr, s)))
+                return e;
+            if ((e = run(A_dev + off, n, lda, strideA, b1 - b0, info_dev + b0, s, BL_ROUTE_AUTO)))
+                return e;
+            if ((e = bl::launch_tri_copy(A_dev + off, Am + off, n, lda, strideA, b1 - b0,
+                                         info_dev + b0, im + b0, s)))
+                return e;
+        }
+        return 0;
     }
     const int64_t span = (int64_t)lda * n;  // floats of one matrix
     if (chunks <= 0) chunks = nstreams;

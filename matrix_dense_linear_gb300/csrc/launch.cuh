@@ -108,6 +108,11 @@ int attrs_tiles(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem);
 // returns 1 when the panels are not 16-byte aligned (the caller's FP32 path)
 int launch_cherk_tc(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
                     cudaStream_t stream);
+// lower triangles of nb matrices (and, when info_src is given, their info
+// entries) from src to dst, both in the same strided layout; either side may
+// be mapped host memory
+int launch_tri_copy(const float *src, float *dst, int n, int lda, int64_t strideA, int nb,
+                    const int *info_src, int *info_dst, cudaStream_t stream);
 // L21 = A21 L11^{-H} of the complex blocked path (lower storage, the same
 // conventions) with the block updates on the tensor cores; returns 1 when the
 // panels are not 16-byte aligned (the caller's FP32 kernel)

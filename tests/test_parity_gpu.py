@@ -192,11 +192,13 @@ def test_host_buffer_call(n, batch, chunks):
     assert_untouched(out, bt.buf, bt, what=f"host n={n}")
 
 
-@pytest.mark.parametrize("n,batch", [(20, 100), (64, 1000), (100, 30), (128, 40)])
+@pytest.mark.parametrize("n,batch", [(20, 100), (64, 1000), (100, 30), (128, 40), (129, 9),
+                                     (200, 30), (256, 64), (300, 7)])
 def test_host_call_pinned_and_pageable_agree(n, batch):
     """Pinned host buffers of n <= 128 are factored in place by the kernel over
-    the host link; pageable ones take the copy path. Both give the bits of
-    the device call."""
+    the host link, larger ones through kernels that copy only the lower
+    triangles in and out; pageable ones take the copy path. All give the bits
+    of the device call."""
     import torch
 
     import matrix_dense_linear_gb300 as bl
@@ -215,6 +217,32 @@ def test_host_call_pinned_and_pageable_agree(n, batch):
         assert np.array_equal(host.numpy().view(np.uint32), want.view(np.uint32)), pinned
     compare(bt, want, info_d.cpu().numpy(), indices=list(range(min(batch, 40))),
             what=f"host n={n}")
+
+
+@pytest.mark.parametrize("offset,chunks", [(0, 0), (1, 3), (3, 1)])
+def test_host_call_triangle_copies(offset, chunks):
+    """The triangle copies of the host-buffer call (n > 128, pinned buffers):
+    a buffer starting off a 16-byte boundary (the scalar copy), gaps between
+    the matrices and the upper triangles poisoned, several slices per stream:
+    the factors and info are the device call's bits and nothing else changes."""
+    import torch
+
+    import matrix_dense_linear_gb300 as bl
+    n, batch = 260, 11
+    bt = _gram_batch(n, batch, 905 + offset, fill="nan", strideA=n * n + 7)
+    base = torch.full((bt.buf.size + offset,), float("nan"), dtype=torch.float32).pin_memory()
+    base[offset:] = torch.from_numpy(bt.buf)
+    host = base[offset:]
+    info_h = torch.full((batch,), -7, dtype=torch.int32).pin_memory()
+    dev = torch.from_numpy(bt.buf.copy()).cuda()
+    info_d = torch.empty(batch, dtype=torch.int32, device="cuda")
+    bl.factor(dev, n, bt.lda, bt.strideA, batch, info_d)
+    want = dev.cpu().numpy()
+    bl.factor_host(host, n, bt.lda, bt.strideA, batch, info_h, chunks=chunks)
+    assert np.array_equal(info_h.numpy(), info_d.cpu().numpy())
+    assert np.array_equal(host.numpy().view(np.uint32), want.view(np.uint32))
+    assert np.isnan(base[:offset].numpy()).all()
+    assert_untouched(host.numpy(), bt.buf, bt, what=f"host triangles offset={offset}")
 
 
 def test_fma_probe():
