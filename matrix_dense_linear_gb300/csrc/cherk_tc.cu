@@ -1,5 +1,7 @@
 // Trailing update of the single-precision complex blocked path on the tensor
-// cores (lower storage):
+// cores (either storage; in the upper one an operand row is U's contiguous
+// column and the raw values are L's conjugates, so the same products give the
+// conjugated update the upper triangle stores):
 //     A22 <- A22 - L21 L21^H      (lower triangle, 128 x 128 complex tiles, k = 128)
 // in real arithmetic. With L = P + iQ (P, Q the real and imaginary parts),
 //     L_I L_K^H = (P_I P_K^T + Q_I Q_K^T) + i (Q_I P_K^T - P_I Q_K^T),
@@ -52,6 +54,7 @@ __device__ __forceinline__ uint32_t core_off(int r, int kq)
     return (uint32_t)(r >> 3) * kSbo + (uint32_t)kq * kLbo + (uint32_t)(r & 7) * 16;
 }
 
+template <bool UP>
 __global__ void __launch_bounds__(256, 2)
 cherk_tc_kernel(float2 *__restrict__ A, int n, int lda, int64_t strideA, int c0, int ntiles_col,
                 int *__restrict__ info)
@@ -87,7 +90,11 @@ cherk_tc_kernel(float2 *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     const bool stager = !(op == 1 && I == K);
     const int rp = tid & 63, kq = (tid >> 6) & 1;
     const int rbase = op ? rk : ri;
-    const float2 *src = Ab + (c1 + rbase + 2 * rp) + (int64_t)(c0 + 4 * kq) * lda;
+    // lower storage: src[c lda] holds rows 2rp, 2rp + 1 of complex column c;
+    // upper: row 2rp + i of the operand is the contiguous column
+    // c1 + rbase + 2rp + i of U, src + i lda its columns 4kq ..
+    const float2 *src = UP ? Ab + (c0 + 4 * kq) + (int64_t)(c1 + rbase + 2 * rp) * lda
+                           : Ab + (c1 + rbase + 2 * rp) + (int64_t)(c0 + 4 * kq) * lda;
     const int valid_rows = max(0, min(2, m - rbase - 2 * rp));
 
     if (tid == 0) {
@@ -110,14 +117,34 @@ cherk_tc_kernel(float2 *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     float4 cur[4], nxt[4], nxt2[4];
     auto load_slice = [&](int s, float4 (&v)[4]) {
         if (!stager) return;
+        if constexpr (UP) {
+            // U's raw values: the conjugates of L's at the transposed places, so
+            // the same products give the conjugate of the lower update, which is
+            // what the upper triangle stores
+            float4 r[2][2];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const float2 *p = src + (int64_t)(s * kKs + c) * lda;
-            if (valid_rows == 2) {
-                v[c] = *reinterpret_cast<const float4 *>(p);
-            } else {
-                const float2 a = valid_rows > 0 ? p[0] : make_float2(0.0f, 0.0f);
-                v[c] = make_float4(a.x, a.y, 0.0f, 0.0f);
+            for (int i = 0; i < 2; ++i) {
+                const float2 *p = src + (int64_t)i * lda + s * kKs;
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    r[i][h] = i < valid_rows ? *reinterpret_cast<const float4 *>(p + 2 * h)
+                                             : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float4 a = r[0][c >> 1], b = r[1][c >> 1];
+                v[c] = (c & 1) ? make_float4(a.z, a.w, b.z, b.w) : make_float4(a.x, a.y, b.x, b.y);
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float2 *p = src + (int64_t)(s * kKs + c) * lda;
+                if (valid_rows == 2) {
+                    v[c] = *reinterpret_cast<const float4 *>(p);
+                } else {
+                    const float2 a = valid_rows > 0 ? p[0] : make_float2(0.0f, 0.0f);
+                    v[c] = make_float4(a.x, a.y, 0.0f, 0.0f);
+                }
             }
         }
     };
@@ -209,26 +236,63 @@ cherk_tc_kernel(float2 *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     const int q = warp & 3, h = warp >> 2;
     const int r = 32 * q + lane;
     const int gr = ri + r;
-    float2 *Crow = Ab + (c1 + gr) + (int64_t)c1 * lda;
+    // element (r, c) of the tile: lower storage at (c1 + gr) + (c1 + gc) lda,
+    // upper at (c1 + gc) + (c1 + gr) lda (a lane's 16 columns contiguous)
+    float2 *Crow = UP ? Ab + c1 + (int64_t)(c1 + gr) * lda : Ab + (c1 + gr) + (int64_t)c1 * lda;
+    const int64_t cs = UP ? 1 : lda;
     if (ok) {
 #pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
             const int gc0 = rk + 64 * h + 16 * cc;
             float2 old[16];
+            if constexpr (UP) {
+                // a lane's 16 entries are contiguous: 16-byte accesses by pairs,
+                // a single entry where only the first of a pair is in the triangle
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int gc = gc0 + j;
-                old[j] = (gr < m && gc < m && gr >= gc) ? Crow[(int64_t)gc * lda]
-                                                       : make_float2(0.0f, 0.0f);
+                for (int j = 0; j < 16; j += 2) {
+                    const int gc = gc0 + j;
+                    const bool in0 = gr < m && gc < m && gr >= gc;
+                    const bool in1 = gr < m && gc + 1 < m && gr >= gc + 1;
+                    if (in1) {
+                        const float4 o = *reinterpret_cast<const float4 *>(Crow + gc);
+                        old[j] = make_float2(o.x, o.y);
+                        old[j + 1] = make_float2(o.z, o.w);
+                    } else {
+                        old[j] = in0 ? Crow[gc] : make_float2(0.0f, 0.0f);
+                        old[j + 1] = make_float2(0.0f, 0.0f);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int gc = gc0 + j;
+                    old[j] = (gr < m && gc < m && gr >= gc) ? Crow[(int64_t)gc * cs]
+                                                           : make_float2(0.0f, 0.0f);
+                }
             }
             float vr[16], vi[16];
             tc::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + 64 * h + 16 * cc, vr);
             tc::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + 128 + 64 * h + 16 * cc, vi);
+            if constexpr (UP) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int gc = gc0 + j;
-                if (gr < m && gc < m && gr >= gc)
-                    Crow[(int64_t)gc * lda] = make_float2(old[j].x - vr[j], old[j].y - vi[j]);
+                for (int j = 0; j < 16; j += 2) {
+                    const int gc = gc0 + j;
+                    const bool in0 = gr < m && gc < m && gr >= gc;
+                    const bool in1 = gr < m && gc + 1 < m && gr >= gc + 1;
+                    if (in1)
+                        *reinterpret_cast<float4 *>(Crow + gc) =
+                            make_float4(old[j].x - vr[j], old[j].y - vi[j], old[j + 1].x - vr[j + 1],
+                                        old[j + 1].y - vi[j + 1]);
+                    else if (in0)
+                        Crow[gc] = make_float2(old[j].x - vr[j], old[j].y - vi[j]);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int gc = gc0 + j;
+                    if (gr < m && gc < m && gr >= gc)
+                        Crow[(int64_t)gc * cs] = make_float2(old[j].x - vr[j], old[j].y - vi[j]);
+                }
             }
         }
     } else if (tid == 0) {
@@ -241,6 +305,28 @@ cherk_tc_kernel(float2 *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     if (warp == 0) tc::tmem_dealloc(tmem, 256);
 }
 
+// Returns 0 after launching, 1 when the complex panels are not 16-byte aligned
+// (the caller's FP32 kernel), -1 on a trailing matrix that is empty.
+template <bool UP>
+int launch_t(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
+             cudaStream_t stream)
+{
+    if (((reinterpret_cast<uintptr_t>(A) & 15) != 0) || (lda & 1) || (strideA & 1)) return 1;
+    const int m = n - c0 - kNb;
+    if (m <= 0) return -1;
+    static DeviceOnce attrs;
+    if (const int e = attrs.run([] {
+            return cudaFuncSetAttribute(cherk_tc_kernel<UP>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        }))
+        return e;
+    const int T = (m + 127) / 128;
+    const int64_t blocks = (int64_t)batch * (T * (T + 1) / 2);
+    if (blocks > 0x7fffffffLL) return (int)cudaErrorInvalidConfiguration;
+    return launch_pdl(cherk_tc_kernel<UP>, dim3((unsigned)blocks), dim3(256), (size_t)kSmemBytes,
+                      stream, reinterpret_cast<float2 *>(A), n, lda, strideA, c0, T, info);
+}
+
 }  // namespace
 
 int set_fail_first_wait_cherk_tc(int every)
@@ -248,25 +334,11 @@ int set_fail_first_wait_cherk_tc(int every)
     return (int)cudaMemcpyToSymbol(g_fail_first_wait, &every, sizeof every);
 }
 
-// Returns 0 after launching, 1 when the complex panels are not 16-byte aligned
-// (the caller's FP32 kernel), -1 on a trailing matrix that is empty.
 int launch_cherk_tc(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
-                    cudaStream_t stream)
+                    cudaStream_t stream, bool upper)
 {
-    if (((reinterpret_cast<uintptr_t>(A) & 15) != 0) || (lda & 1) || (strideA & 1)) return 1;
-    const int m = n - c0 - kNb;
-    if (m <= 0) return -1;
-    static DeviceOnce attrs;
-    if (const int e = attrs.run([] {
-            return cudaFuncSetAttribute(cherk_tc_kernel,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        }))
-        return e;
-    const int T = (m + 127) / 128;
-    const int64_t blocks = (int64_t)batch * (T * (T + 1) / 2);
-    if (blocks > 0x7fffffffLL) return (int)cudaErrorInvalidConfiguration;
-    return launch_pdl(cherk_tc_kernel, dim3((unsigned)blocks), dim3(256), (size_t)kSmemBytes,
-                      stream, reinterpret_cast<float2 *>(A), n, lda, strideA, c0, T, info);
+    return upper ? launch_t<true>(A, n, lda, strideA, batch, info, c0, stream)
+                 : launch_t<false>(A, n, lda, strideA, batch, info, c0, stream);
 }
 
 }  // namespace bl

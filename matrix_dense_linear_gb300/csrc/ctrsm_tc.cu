@@ -1,5 +1,7 @@
 // Panel solve of the single-precision complex blocked path with the tensor
-// cores doing the block updates (lower storage):
+// cores doing the block updates (either storage; the upper one reads and writes
+// U = L^H's raw values at the transposed places, the conjugates of L's, so the
+// same arithmetic yields the conjugated results it stores):
 //     L21 = A21 L11^{-H}      (A21: the rows below the 128 x 128 diagonal block)
 // as a blocked forward substitution over four 32-column blocks j:
 //     X_j = (A_j - sum_{i<j} X_i L_ji^H) L_jj^{-H}.
@@ -66,6 +68,7 @@ __host__ __device__ constexpr int lt_rows(int j) { return 96 - 32 * j; }
 // tid + 128, tid + 256; load() fetches them (16-byte loads: two complex rows of
 // a column), stage() writes the four operand tiles, the two rows of a piece in
 // the order that puts a quarter warp's stores on eight distinct rows.
+template <bool UP>
 struct LtPieces {
     float4 v[3][4];  // [piece][column]: (re, im) of the two rows
     __device__ __forceinline__ void load(const float2 *L11, int lda, int j, int tid)
@@ -76,10 +79,29 @@ struct LtPieces {
             const int b = tid + 128 * u;
             if (b < 8 * np) {
                 const int s = b & 1, p = (b >> 1) % np, h = (b >> 1) / np;
-                const float2 *src = L11 + (32 * (j + 1) + 2 * p) + (int64_t)(32 * j + 4 * (2 * h + s)) * lda;
+                const int r0 = 32 * (j + 1) + 2 * p, k0 = 32 * j + 4 * (2 * h + s);
+                if constexpr (UP) {
+                    // row r of the piece is U's contiguous column r: two 16-byte
+                    // loads a row, regrouped by column
+                    float4 w[2][2];
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    v[u][c] = *reinterpret_cast<const float4 *>(src + (int64_t)c * lda);
+                    for (int i = 0; i < 2; ++i) {
+                        const float2 *src = L11 + k0 + (int64_t)(r0 + i) * lda;
+                        w[i][0] = *reinterpret_cast<const float4 *>(src);
+                        w[i][1] = *reinterpret_cast<const float4 *>(src + 2);
+                    }
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const float4 a = w[0][c >> 1], bb = w[1][c >> 1];
+                        v[u][c] = (c & 1) ? make_float4(a.z, a.w, bb.z, bb.w)
+                                          : make_float4(a.x, a.y, bb.x, bb.y);
+                    }
+                } else {
+                    const float2 *src = L11 + r0 + (int64_t)k0 * lda;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        v[u][c] = *reinterpret_cast<const float4 *>(src + (int64_t)c * lda);
+                }
             }
         }
     }
@@ -117,6 +139,7 @@ struct LtPieces {
 // The diagonal block L_jj, lower part: thread tid fetches entries
 // e = tid + 128u, (row k, column t) = (e & 31, e >> 5), into registers; put()
 // writes them as Ld[32 t + k] (complex), columns contiguous.
+template <bool UP>
 struct LdPart {
     float2 v[8];
     __device__ __forceinline__ void load(const float2 *L11, int lda, int j, int tid)
@@ -124,7 +147,9 @@ struct LdPart {
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const int e = tid + 128 * u, k = e & 31, t = e >> 5;
-            v[u] = k >= t ? L11[(32 * j + k) + (int64_t)(32 * j + t) * lda] : make_float2(0.0f, 0.0f);
+            const int64_t o = UP ? (32 * j + t) + (int64_t)(32 * j + k) * lda
+                                 : (32 * j + k) + (int64_t)(32 * j + t) * lda;
+            v[u] = k >= t ? L11[o] : make_float2(0.0f, 0.0f);
         }
     }
     __device__ __forceinline__ void put(float2 *Ld, int tid) const
@@ -134,6 +159,7 @@ struct LdPart {
     }
 };
 
+template <bool UP>
 __global__ void __launch_bounds__(128, 2)
 ctrsm_tc_kernel(float2 *__restrict__ A, int n, int lda, int64_t strideA, int c0, int nrb,
                 int *__restrict__ info)
@@ -154,7 +180,10 @@ ctrsm_tc_kernel(float2 *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     const int tid = threadIdx.x, warp = tid >> 5;
     const int R = c0 + 128 + rb * 128 + tid;  // this thread's row
     const bool live = R < n;
-    const float2 *L11 = Ab + c0 + (int64_t)c0 * lda;  // L11(i, k) = L11[i + k lda]
+    // L11(i, k) = L11[i + k lda]; in the upper storage U's raw value at the
+    // transposed place, L11[k + i lda]: the conjugates of L's values, so that
+    // the same arithmetic gives the conjugated results the upper triangle keeps
+    const float2 *L11 = Ab + c0 + (int64_t)c0 * lda;
     float2 *Ld = reinterpret_cast<float2 *>(smem + kOffX);
     float *rinv = reinterpret_cast<float *>(smem + kOffRinv);
     uint8_t *Lt = smem + kOffLt;
@@ -171,18 +200,28 @@ ctrsm_tc_kernel(float2 *__restrict__ A, int n, int lda, int64_t strideA, int c0,
 
     // the first column block's off-diagonal rows, its diagonal block and the
     // reciprocal diagonal travel with the first half of the row
-    LtPieces pc;
+    LtPieces<UP> pc;
     pc.load(L11, lda, 0, tid);
-    LdPart dg;
+    LdPart<UP> dg;
     dg.load(L11, lda, 0, tid);
     const float dii = L11[tid + (int64_t)tid * lda].x;
-    const float2 *g = Ab + (live ? R + (int64_t)c0 * lda : 0);  // g[c lda] = (R, c0 + c)
+    // element (R, c0 + c): g[c lda] (lower), g[c] (upper: U's column R)
+    const float2 *g = Ab + (live ? (UP ? c0 + (int64_t)R * lda : R + (int64_t)c0 * lda) : 0);
     auto load_chunk = [&](int q, float (&re)[32], float (&im)[32]) {
+        if constexpr (UP) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-            const float2 a = live ? g[(int64_t)(32 * q + c) * lda] : make_float2(0.0f, 0.0f);
-            re[c] = -a.x;
-            im[c] = -a.y;
+            for (int c = 0; c < 32; c += 2) {
+                const float4 a = live ? *reinterpret_cast<const float4 *>(g + 32 * q + c)
+                                      : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                re[c] = -a.x; im[c] = -a.y; re[c + 1] = -a.z; im[c + 1] = -a.w;
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const float2 a = live ? g[(int64_t)(32 * q + c) * lda] : make_float2(0.0f, 0.0f);
+                re[c] = -a.x;
+                im[c] = -a.y;
+            }
         }
     };
     float xr[32], xi[32];
@@ -253,9 +292,16 @@ ctrsm_tc_kernel(float2 *__restrict__ A, int n, int lda, int64_t strideA, int c0,
             }
         }
         if (live) {
-            float2 *out = Ab + R + (int64_t)(c0 + 32 * j) * lda;
+            if constexpr (UP) {
+                float2 *out = Ab + (c0 + 32 * j) + (int64_t)R * lda;
 #pragma unroll
-            for (int t = 0; t < 32; ++t) out[(int64_t)t * lda] = make_float2(xr[t], xi[t]);
+                for (int t = 0; t < 32; t += 2)
+                    *reinterpret_cast<float4 *>(out + t) = make_float4(xr[t], xi[t], xr[t + 1], xi[t + 1]);
+            } else {
+                float2 *out = Ab + R + (int64_t)(c0 + 32 * j) * lda;
+#pragma unroll
+                for (int t = 0; t < 32; ++t) out[(int64_t)t * lda] = make_float2(xr[t], xi[t]);
+            }
         }
         if (j == 3) break;
         __syncthreads();  // every thread is done with Ld before X overwrites it
@@ -322,6 +368,26 @@ ctrsm_tc_kernel(float2 *__restrict__ A, int n, int lda, int64_t strideA, int c0,
     if (tid == 0 && sh_err) info[mat] = -1;
 }
 
+template <bool UP>
+int launch_t(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
+             cudaStream_t stream)
+{
+    if (((reinterpret_cast<uintptr_t>(A) & 15) != 0) || (lda & 1) || (strideA & 1)) return 1;
+    const int m = n - c0 - 128;
+    if (m <= 0) return -1;
+    static DeviceOnce attrs;
+    if (const int e = attrs.run([] {
+            return cudaFuncSetAttribute(ctrsm_tc_kernel<UP>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        }))
+        return e;
+    const int nrb = (m + 127) / 128;
+    const int64_t blocks = (int64_t)batch * nrb;
+    if (blocks > 0x7fffffffLL) return (int)cudaErrorInvalidConfiguration;
+    return launch_pdl(ctrsm_tc_kernel<UP>, dim3((unsigned)blocks), dim3(128), (size_t)kSmemBytes,
+                      stream, reinterpret_cast<float2 *>(A), n, lda, strideA, c0, nrb, info);
+}
+
 }  // namespace
 
 int set_fail_first_wait_ctrsm_tc(int every)
@@ -332,22 +398,10 @@ int set_fail_first_wait_ctrsm_tc(int every)
 // Returns 0 after launching, 1 when the complex panels are not 16-byte aligned
 // (the caller's FP32 kernel), -1 on an empty panel, or a cudaError_t.
 int launch_ctrsm_tc(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
-                    cudaStream_t stream)
+                    cudaStream_t stream, bool upper)
 {
-    if (((reinterpret_cast<uintptr_t>(A) & 15) != 0) || (lda & 1) || (strideA & 1)) return 1;
-    const int m = n - c0 - 128;
-    if (m <= 0) return -1;
-    static DeviceOnce attrs;
-    if (const int e = attrs.run([] {
-            return cudaFuncSetAttribute(ctrsm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        kSmemBytes);
-        }))
-        return e;
-    const int nrb = (m + 127) / 128;
-    const int64_t blocks = (int64_t)batch * nrb;
-    if (blocks > 0x7fffffffLL) return (int)cudaErrorInvalidConfiguration;
-    return launch_pdl(ctrsm_tc_kernel, dim3((unsigned)blocks), dim3(128), (size_t)kSmemBytes, stream,
-                      reinterpret_cast<float2 *>(A), n, lda, strideA, c0, nrb, info);
+    return upper ? launch_t<true>(A, n, lda, strideA, batch, info, c0, stream)
+                 : launch_t<false>(A, n, lda, strideA, batch, info, c0, stream);
 }
 
 }  // namespace bl

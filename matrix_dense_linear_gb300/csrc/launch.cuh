@@ -103,21 +103,22 @@ int launch_cpotrf_tiles(float *A, int n, int lda, int64_t strideA, int batch, in
 int launch_spotrf_tiles(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                         cudaStream_t stream, bool upper, int info_off = -1);
 int attrs_tiles(int n, cudaFuncAttributes *fa, int *threads, int *dyn_smem);
-// A22 -= L21 L21^H of the complex blocked path (lower storage, interleaved
-// complex floats, lda and strideA in complex elements) on the tensor cores;
-// returns 1 when the panels are not 16-byte aligned (the caller's FP32 path)
+// A22 -= L21 L21^H of the complex blocked path (interleaved complex floats,
+// lda and strideA in complex elements; upper: the same on U = L^H) on the
+// tensor cores; returns 1 when the panels are not 16-byte aligned (the
+// caller's FP32 path)
 int launch_cherk_tc(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
-                    cudaStream_t stream);
+                    cudaStream_t stream, bool upper);
 // lower triangles of nb matrices (and, when info_src is given, their info
 // entries) from src to dst, both in the same strided layout; either side may
 // be mapped host memory
 int launch_tri_copy(const float *src, float *dst, int n, int lda, int64_t strideA, int nb,
                     const int *info_src, int *info_dst, cudaStream_t stream);
-// L21 = A21 L11^{-H} of the complex blocked path (lower storage, the same
-// conventions) with the block updates on the tensor cores; returns 1 when the
-// panels are not 16-byte aligned (the caller's FP32 kernel)
+// L21 = A21 L11^{-H} of the complex blocked path (the same conventions) with
+// the block updates on the tensor cores; returns 1 when the panels are not
+// 16-byte aligned (the caller's FP32 kernel)
 int launch_ctrsm_tc(float *A, int n, int lda, int64_t strideA, int batch, int *info, int c0,
-                    cudaStream_t stream);
+                    cudaStream_t stream, bool upper);
 int launch_cpotrf(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                   cudaStream_t stream, bool upper);
 // A: interleaved complex double; lda and strideA in complex elements

@@ -22,10 +22,10 @@
 //                       (16 for complex);
 //   simple_syrk_kernel  its trailing update on 64 x 64 tiles on or below the
 //                       diagonal, k staged through shared memory.
-// Single-precision complex batches in the lower storage with 16-byte-aligned
-// panels take the tensor-core forms of the panel solve and the trailing update
-// instead (ctrsm_tc.cu, cherk_tc.cu), and their diagonal blocks above order 64
-// the warp-per-tile register kernel (potrf_tiles.cu).
+// Single-precision complex batches with 16-byte-aligned panels (either
+// storage) take the tensor-core forms of the panel solve and the trailing
+// update instead (ctrsm_tc.cu, cherk_tc.cu), and their diagonal blocks above
+// order 64 the warp-per-tile register kernel (potrf_tiles.cu).
 #include <mutex>
 #include <type_traits>
 
@@ -370,13 +370,12 @@ int launch_blocked_s(T *A, int n, int lda, int64_t strideA, int batch, int *info
         if (e) return e;
         const int m = n - c0 - nb;
         if (m <= 0) break;
-        // single-precision complex, lower storage, 16-byte aligned: the panel
-        // solve's block updates on the tensor cores (ctrsm_tc.cu); else the
-        // FP32 kernel
+        // single-precision complex, 16-byte aligned: the panel solve's block
+        // updates on the tensor cores (ctrsm_tc.cu); else the FP32 kernel
         e = 1;
-        if constexpr (std::is_same<T, float2>::value && !UP) {
+        if constexpr (std::is_same<T, float2>::value) {
             e = launch_ctrsm_tc(reinterpret_cast<float *>(A), n, lda, strideA, batch, info, c0,
-                                st);
+                                st, UP);
             if (e != 0 && e != 1) return e;
         }
         if (e == 1) {
@@ -385,11 +384,11 @@ int launch_blocked_s(T *A, int n, int lda, int64_t strideA, int batch, int *info
                 A, n, lda, strideA, c0, info);
             if ((e = (int)cudaGetLastError())) return e;
         }
-        // single-precision complex, lower storage, 16-byte aligned: the trailing
-        // update on the tensor cores (cherk_tc.cu); else the FP32 tiles below
-        if constexpr (std::is_same<T, float2>::value && !UP) {
+        // single-precision complex, 16-byte aligned: the trailing update on the
+        // tensor cores (cherk_tc.cu); else the FP32 tiles below
+        if constexpr (std::is_same<T, float2>::value) {
             e = launch_cherk_tc(reinterpret_cast<float *>(A), n, lda, strideA, batch, info, c0,
-                                st);
+                                st, UP);
             if (e == 0) continue;
             if (e != 1) return e;
         }

@@ -203,21 +203,24 @@ def test_cpotrf_codes():
     assert bl.cpotrf_batched(Z, 2, 1, 4, 1, info) == -3
 
 
+@pytest.mark.parametrize("uplo", ["L", "U"])
 @pytest.mark.parametrize("n", [130, 256, 384, 520])
-def test_cpotrf_tensor_core_update(n):
-    """Single-precision complex, lower storage, 16-byte-aligned batches above
-    n = 128: the panel solve's block updates and the trailing update run on the
-    tensor cores (3xTF32 real and imaginary products); several row blocks and
-    trailing tiles, ragged ones at 130 and 520."""
+def test_cpotrf_tensor_core_update(n, uplo):
+    """Single-precision complex, 16-byte-aligned batches above n = 128 (both
+    storages): the panel solve's block updates and the trailing update run on
+    the tensor cores (3xTF32 real and imaginary products); several row blocks
+    and trailing tiles, ragged ones at 130 and 520; a padded lda."""
     batch = 5
+    lda = n + 2
     mats = [_herm(n, 4000 + 10 * n + b) for b in range(batch)]
-    buf = _pack(mats, n, n, n * n, "L", diag_imag=0.75)
-    out, info = _run(buf, n, n, n * n, batch, "L")
-    _check(buf, out, info, n, n, n * n, batch, "L", f"tensor-core update n={n}")
+    buf = _pack(mats, n, lda, lda * n, uplo, diag_imag=0.75)
+    out, info = _run(buf, n, lda, lda * n, batch, uplo)
+    _check(buf, out, info, n, lda, lda * n, batch, uplo, f"tensor-core update n={n} {uplo}")
 
 
+@pytest.mark.parametrize("uplo", ["L", "U"])
 @pytest.mark.parametrize("cls", [6, 7])
-def test_cpotrf_tensor_core_give_up(cls):
+def test_cpotrf_tensor_core_give_up(cls, uplo):
     """Classes 6 and 7 of the failure injection: the complex tensor-core
     trailing update (6) or panel solve (7) gives up at its first bounded wait
     for every third matrix: those report -1, the others match the oracle,
@@ -227,25 +230,26 @@ def test_cpotrf_tensor_core_give_up(cls):
     lib = bl.library()
     n, batch = 384, 6
     mats = [_herm(n, 4500 + b) for b in range(batch)]
-    buf = _pack(mats, n, n, n * n, "L")
+    buf = _pack(mats, n, n, n * n, uplo)
     assert lib.bl_debug_fail_first_wait(cls, 3) == 0
     try:
-        out, info = _run(buf, n, n, n * n, batch, "L")
+        out, info = _run(buf, n, n, n * n, batch, uplo)
     finally:
         assert lib.bl_debug_fail_first_wait(cls, 0) == 0
     assert [int(x) for x in info] == [-1 if b % 3 == 0 else 0 for b in range(batch)], list(info)
-    pat = _pattern(n, n, n * n, batch, buf.size, "L")
+    pat = _pattern(n, n, n * n, batch, buf.size, uplo)
     assert np.array_equal(out.view(np.uint64)[~pat], buf.view(np.uint64)[~pat])
     keep = [b for b in range(batch) if b % 3]
-    sub = _pack([mats[b] for b in keep], n, n, n * n, "L")
+    sub = _pack([mats[b] for b in keep], n, n, n * n, uplo)
     sub_out = np.concatenate([out[b * n * n:(b + 1) * n * n] for b in keep])
-    _check(sub, sub_out, np.zeros(len(keep), dtype=np.int32), n, n, n * n, len(keep), "L",
+    _check(sub, sub_out, np.zeros(len(keep), dtype=np.int32), n, n, n * n, len(keep), uplo,
            "give-up: untouched matrices")
-    out2, info2 = _run(buf, n, n, n * n, batch, "L")
-    _check(buf, out2, info2, n, n, n * n, batch, "L", "after the give-up")
+    out2, info2 = _run(buf, n, n, n * n, batch, uplo)
+    _check(buf, out2, info2, n, n, n * n, batch, uplo, "after the give-up")
 
 
-def test_cpotrf_tensor_core_info():
+@pytest.mark.parametrize("uplo", ["L", "U"])
+def test_cpotrf_tensor_core_info(uplo):
     """Failed pivots in the later panels of the tensor-core complex path: the
     panel solve and the update skip a failed matrix, info is the oracle's and the
     leading block before the failure matches."""
@@ -256,7 +260,7 @@ def test_cpotrf_tensor_core_info():
         A = mats[t]
         q = (A[:k, k].conj() @ np.linalg.solve(A[:k, :k], A[:k, k])).real
         A[k, k] = q - 0.5
-    buf = _pack(mats, n, n, n * n, "L")
-    out, info = _run(buf, n, n, n * n, 6, "L")
+    buf = _pack(mats, n, n, n * n, uplo)
+    out, info = _run(buf, n, n, n * n, 6, uplo)
     assert list(info[:4]) == [k + 1 for k in ks] and info[4] == 0 and info[5] == 0, list(info)
-    _check(buf, out, info, n, n, n * n, 6, "L", "tensor-core info")
+    _check(buf, out, info, n, n, n * n, 6, uplo, "tensor-core info")
