@@ -33,6 +33,7 @@ namespace {
 
 constexpr int kLd = 36;  // leading dimension of a 32 x 32 block in shared memory
 constexpr int kWaveMaxN = 1024;  // the wavefront form: a warp per row block, 32 warps at most
+constexpr int kRegMaxN = 64;     // the register form, several right-hand sides
 
 template <int W>
 struct TrsShared {
@@ -462,6 +463,157 @@ int launch_wave(const float *L, int n, int lda, int64_t strideA, float *B, int64
 #undef BL_WAVE_ARGS
 }
 
+// ---------------------------------------------------------------------------
+// Register form (several right-hand sides, n <= 1024): one warp per (system,
+// C right-hand sides), lane = row of the current 32-row block, the two solves
+// left-looking over the row blocks like the form above, but with the L blocks
+// taken straight into registers (lane r holds row r of L_ji for the forward
+// products, column r of L_ij for the backward ones: the loads of the
+// wavefront form, coalesced or 16 bytes a lane), the next one fetched while
+// the current one is applied, and the solved blocks kept in shared memory as
+// [row][right-hand side] and read as 16-byte broadcasts. No block barrier and
+// no staging copies: a block product is 32 register values times C broadcast
+// columns. The diagonal blocks are solved by substitution with each solved
+// row broadcast by warp shuffles. It takes n <= 64, where the shared-memory
+// form's staging and barriers cost more than its two blocks of products.
+
+// acc -= lc (32 entries of this lane's row) times the solved rows S[k][0..C)
+template <int C>
+__device__ __forceinline__ void reg_product(float (&acc)[C], const float (&lc)[32], const float *S)
+{
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+        float s[C];
+        lds<C>(S + k * C, s);
+#pragma unroll
+        for (int u = 0; u < C; ++u) acc[u] = fmaf(-lc[k], s[u], acc[u]);
+    }
+}
+
+template <int C, bool UP, bool VEC>
+__global__ void __launch_bounds__(32)
+potrs_reg_kernel(const float *__restrict__ L, int n, int lda, int64_t strideA, float *__restrict__ B,
+                 int nrhs, int ldb, int64_t strideB, int G, const int *__restrict__ info)
+{
+    extern __shared__ __align__(16) float Ssm[];  // [n rounded to 32][C]
+    const int NB = (n + 31) >> 5;
+    const int64_t sys = blockIdx.x / G;
+    const int c0 = C * (int)(blockIdx.x % G);
+    pdl_wait();
+    pdl_trigger();
+    if (info != nullptr && info[sys] != 0) return;
+    const float *Lb = L + sys * strideA;
+    float *Bb = B + sys * strideB;
+    const int lane = threadIdx.x;
+    const unsigned full = 0xffffffffu;
+
+    float acc[C], lc[32], ln[32];
+    // ---------------- forward: L Y = B ----------------
+#pragma unroll 1
+    for (int j = 0; j < NB; ++j) {
+        const int row = 32 * j + lane;
+        const bool rv = row < n;
+#pragma unroll
+        for (int u = 0; u < C; ++u)
+            acc[u] = rv && c0 + u < nrhs ? Bb[row + (int64_t)(c0 + u) * ldb] : 0.0f;
+        if (j > 0) load_block<UP, VEC, true>(lc, Lb, lda, n, 32 * j, 0, lane);
+#pragma unroll 1
+        for (int i = 0; i < j; ++i) {
+            // L_j,i+1 (or the diagonal block's row after the last product)
+            load_block<UP, VEC, true>(ln, Lb, lda, n, 32 * j, 32 * (i + 1), lane);
+            reg_product<C>(acc, lc, Ssm + 32 * i * C);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) lc[k] = ln[k];
+        }
+        if (j == 0) load_block<UP, VEC, true>(lc, Lb, lda, n, 0, 0, lane);
+        // lc: row `lane` of L_jj; y_k = acc_k / l_kk from lane k, lanes r > k
+        // subtract l_rk y_k
+        const float rinv = rv ? 1.0f / Lb[lidx<UP>(row, row, lda)] : 1.0f;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+#pragma unroll
+            for (int u = 0; u < C; ++u) {
+                const float yk = __shfl_sync(full, acc[u] * rinv, k);
+                acc[u] = lane == k ? yk : (lane > k ? fmaf(-lc[k], yk, acc[u]) : acc[u]);
+            }
+        }
+        sts<C>(Ssm + row * C, acc);
+        __syncwarp();
+    }
+
+    // ---------------- backward: L^T X = Y ----------------
+#pragma unroll 1
+    for (int j = NB - 1; j >= 0; --j) {
+        const int row = 32 * j + lane;
+        const bool rv = row < n;
+        lds<C>(Ssm + row * C, acc);
+        if (j + 1 < NB) load_block<UP, VEC, false>(lc, Lb, lda, n, 32 * (j + 1), 32 * j, lane);
+#pragma unroll 1
+        for (int i = j + 1; i < NB; ++i) {
+            // L_i+1,j, or column `lane` of L_jj after the last product
+            load_block<UP, VEC, false>(ln, Lb, lda, n, i + 1 < NB ? 32 * (i + 1) : 32 * j, 32 * j,
+                                       lane);
+            reg_product<C>(acc, lc, Ssm + 32 * i * C);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) lc[k] = ln[k];
+        }
+        if (j + 1 == NB) load_block<UP, VEC, false>(lc, Lb, lda, n, 32 * j, 32 * j, lane);
+        // lc: column `lane` of L_jj; x_k = acc_k / l_kk from lane k (from the
+        // bottom), lanes r < k subtract l_kr x_k
+        const float rinv = rv ? 1.0f / Lb[lidx<UP>(row, row, lda)] : 1.0f;
+#pragma unroll
+        for (int k = 31; k >= 0; --k) {
+#pragma unroll
+            for (int u = 0; u < C; ++u) {
+                const float xk = __shfl_sync(full, acc[u] * rinv, k);
+                acc[u] = lane == k ? xk : (lane < k ? fmaf(-lc[k], xk, acc[u]) : acc[u]);
+            }
+        }
+        __syncwarp();  // every lane has read block j's Y before it is overwritten
+        sts<C>(Ssm + row * C, acc);
+        if (rv) {
+#pragma unroll
+            for (int u = 0; u < C; ++u)
+                if (c0 + u < nrhs) Bb[row + (int64_t)(c0 + u) * ldb] = acc[u];
+        }
+        __syncwarp();
+    }
+}
+
+template <int C, bool UP, bool VEC>
+int launch_reg_t(const float *L, int n, int lda, int64_t strideA, float *B, int nrhs, int ldb,
+                 int64_t strideB, int batch, const int *info, cudaStream_t stream)
+{
+    const size_t smem = (size_t)((n + 31) / 32) * 32 * C * 4;
+    static DeviceOnce attrs;
+    if (const int e = attrs.run([] {
+            return cudaFuncSetAttribute(potrs_reg_kernel<C, UP, VEC>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        kRegMaxN * C * 4);
+        }))
+        return e;
+    const int G = (nrhs + C - 1) / C;
+    const int64_t blocks = (int64_t)batch * G;
+    if (blocks > 0x7fffffffLL) return (int)cudaErrorInvalidConfiguration;
+    return launch_pdl(potrs_reg_kernel<C, UP, VEC>, dim3((unsigned)blocks), dim3(32), smem, stream,
+                      L, n, lda, strideA, B, nrhs, ldb, strideB, G, info);
+}
+
+template <int C>
+int launch_reg(const float *L, int n, int lda, int64_t strideA, float *B, int nrhs, int ldb,
+               int64_t strideB, int batch, const int *info, cudaStream_t stream, bool upper)
+{
+    const bool vec = ((reinterpret_cast<uintptr_t>(L) & 15) == 0) && (lda & 3) == 0 &&
+                     (strideA & 3) == 0;
+#define BL_REG_ARGS L, n, lda, strideA, B, nrhs, ldb, strideB, batch, info, stream
+    if (upper)
+        return vec ? launch_reg_t<C, true, true>(BL_REG_ARGS)
+                   : launch_reg_t<C, true, false>(BL_REG_ARGS);
+    return vec ? launch_reg_t<C, false, true>(BL_REG_ARGS)
+               : launch_reg_t<C, false, false>(BL_REG_ARGS);
+#undef BL_REG_ARGS
+}
+
 template <int W, int C>
 int launch_wc(const float *L, int n, int lda, int64_t strideA, float *B, int nrhs, int ldb,
               int64_t strideB, int batch, const int *info, cudaStream_t stream, bool upper)
@@ -490,6 +642,17 @@ int launch_potrs(const float *L, int n, int lda, int64_t strideA, float *B, int 
         if (NB <= 16)
             return launch_wave<16>(L, n, lda, strideA, B, strideB, batch, info, stream, upper);
         return launch_wave<32>(L, n, lda, strideA, B, strideB, batch, info, stream, upper);
+    }
+    // several right-hand sides: the register form up to n = 64, the
+    // left-looking shared-memory form above (measured on GB300: n = 64 x 1024
+    // with 8 right-hand sides 16.1 against 28.5 us, 32 with 32 19.3 against
+    // 21.0 us; from n = 128 on the register form loses, 256 x 4096 with 16
+    // 927 against 788 us: a warp's chain of block products waits on its L
+    // loads, and each group of eight right-hand sides reads L again)
+    if (n <= kRegMaxN) {
+        if (nrhs <= 2) return launch_reg<2>(BL_POTRS_ARGS);
+        if (nrhs <= 4) return launch_reg<4>(BL_POTRS_ARGS);
+        return launch_reg<8>(BL_POTRS_ARGS);
     }
     if (nrhs <= 1) return launch_wc<1, 1>(BL_POTRS_ARGS);
     if (nrhs <= 2) return launch_wc<1, 2>(BL_POTRS_ARGS);

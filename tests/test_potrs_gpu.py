@@ -150,6 +150,42 @@ def test_potrs_one_rhs_wavefront(n, aligned):
                         f"n={n} aligned={aligned} system {b}")
 
 
+@pytest.mark.parametrize("uplo", ["L", "U"])
+@pytest.mark.parametrize("n,nrhs", [(32, 2), (40, 4), (61, 9), (64, 16)])
+def test_potrs_register_form(n, nrhs, uplo):
+    """Several right-hand sides up to n = 64 run the register form (a warp per
+    system and group of up to eight right-hand sides, L blocks in registers):
+    lda and the matrix stride multiples of four floats, so the L loads that are
+    contiguous per lane take 16-byte accesses; both storages."""
+    import torch
+
+    import matrix_dense_linear_gb300 as bl
+    batch = 4
+    lda = (n + 3) // 4 * 4
+    strideA, ldb, strideB = lda * n + 8, n + 1, (n + 1) * nrhs + 3
+    lbuf, Ls = _factors(n, batch, 1800 + n, lda, strideA)
+    if uplo == "U":  # the same factors as U = L^T in the upper triangle
+        ubuf = np.full_like(lbuf, np.nan)
+        for b in range(batch):
+            for j in range(n):
+                ubuf[b * strideA + j * lda: b * strideA + j * lda + j + 1] = Ls[b][j, : j + 1]
+        lbuf = ubuf
+    bbuf, Bs = _rhs(n, nrhs, batch, 1850 + n, ldb, strideB)
+    dl = torch.from_numpy(lbuf.copy()).cuda()
+    db = torch.from_numpy(bbuf.copy()).cuda()
+    assert bl.spotrs_batched_uplo(uplo, dl, n, lda, strideA, db, nrhs, ldb, strideB, batch) == 0
+    torch.cuda.synchronize()
+    b_after = db.cpu().numpy()
+    assert np.array_equal(dl.cpu().numpy().view(np.uint32), lbuf.view(np.uint32))
+    pat = _solution_pattern(n, nrhs, ldb, strideB, batch, bbuf.size)
+    assert np.array_equal(b_after.view(np.uint32)[~pat], bbuf.view(np.uint32)[~pat])
+    X_ref, _ = oracle.potrs_batched(lbuf, n, lda, strideA, bbuf, nrhs, ldb, strideB, batch,
+                                    uplo=uplo)
+    for b in range(batch):
+        _check_solution(Ls[b], Bs[b], _view(b_after, n, nrhs, ldb, strideB, b), X_ref[b],
+                        f"n={n} nrhs={nrhs} {uplo} system {b}")
+
+
 def test_potrs_large_order():
     n, nrhs, batch = 1024, 32, 2
     lbuf, Ls = _factors(n, batch, 1100, n, n * n)
