@@ -44,8 +44,8 @@ REPLICA_CAP_BYTES = 96 << 30
 # its launches summed (the blocked route, whose `achieved` is per call too).
 TRAFFIC = {
     # workload: (source files, sha256 prefix over them, bytes, scope)
-    "n32": (('matrix_dense_linear_gb300/csrc/potrf_warp.cu', 'matrix_dense_linear_gb300/csrc/bl_common.cuh'), "3256ed3948addbed", 4219904, "per launch"),
-    "n64": (('matrix_dense_linear_gb300/csrc/potrf_warp.cu', 'matrix_dense_linear_gb300/csrc/bl_common.cuh'), "3256ed3948addbed", 12660224, "per launch"),
+    "n32": (('matrix_dense_linear_gb300/csrc/potrf_warp.cu', 'matrix_dense_linear_gb300/csrc/bl_common.cuh'), "67514fa4e72bb6b5", 4219904, "per launch"),
+    "n64": (('matrix_dense_linear_gb300/csrc/potrf_warp.cu', 'matrix_dense_linear_gb300/csrc/bl_common.cuh'), "67514fa4e72bb6b5", 12660224, "per launch"),
     "n128": (('matrix_dense_linear_gb300/csrc/potrf_cta.cu', 'matrix_dense_linear_gb300/csrc/cta_common.cuh', 'matrix_dense_linear_gb300/csrc/bl_common.cuh', 'matrix_dense_linear_gb300/csrc/tc_sm100.cuh'), "5ddde5688af11cca", 42150000, "per launch"),
     "n256": (('matrix_dense_linear_gb300/csrc/potrf_blocked.cu', 'matrix_dense_linear_gb300/csrc/potrf_cta.cu', 'matrix_dense_linear_gb300/csrc/cta_common.cuh', 'matrix_dense_linear_gb300/csrc/trsm_tc.cu', 'matrix_dense_linear_gb300/csrc/syrk_tc.cu', 'matrix_dense_linear_gb300/csrc/tc_sm100.cuh', 'matrix_dense_linear_gb300/csrc/bl_common.cuh'), "a37c800817932de5", 1708000000, "per call (4 launches)"),
     "n1024": (('matrix_dense_linear_gb300/csrc/potrf_blocked.cu', 'matrix_dense_linear_gb300/csrc/potrf_cta.cu', 'matrix_dense_linear_gb300/csrc/cta_common.cuh', 'matrix_dense_linear_gb300/csrc/trsm_tc.cu', 'matrix_dense_linear_gb300/csrc/syrk_tc.cu', 'matrix_dense_linear_gb300/csrc/tc_sm100.cuh', 'matrix_dense_linear_gb300/csrc/bl_common.cuh'), "a37c800817932de5", 5740000000, "per call (21 launches)"),

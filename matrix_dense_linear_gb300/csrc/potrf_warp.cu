@@ -132,14 +132,23 @@ potrf_warp_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int ba
         r[j] = lij;
         dm = (row == j) ? d : dm;
         // columns j+1 .. N-1 of the broadcast column, read 4 at a time
+        // by pairs of columns with the paired single-precision FMA (two
+        // fused multiply-adds, each rounded as fmaf, in one instruction); a
+        // single column where the pair straddles j
+        const float2 nw = make_float2(-w, -w);
 #pragma unroll
         for (int q = (j + 1) / 4; q < N / 4; ++q) {
             const float4 c4 = reinterpret_cast<const float4 *>(col)[q];
-            const float cv[4] = {c4.x, c4.y, c4.z, c4.w};
+            const float2 cp[2] = {make_float2(c4.x, c4.y), make_float2(c4.z, c4.w)};
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                const int k = 4 * q + t;
-                if (k > j) r[k] = fmaf(-w, cv[t], r[k]);
+            for (int h = 0; h < 2; ++h) {
+                const int k = 4 * q + 2 * h;
+                if (k > j) {
+                    const float2 t = __ffma2_rn(nw, cp[h], make_float2(r[k], r[k + 1]));
+                    r[k] = t.x; r[k + 1] = t.y;
+                } else if (k + 1 > j) {
+                    r[k + 1] = fmaf(-w, cp[h].y, r[k + 1]);
+                }
             }
         }
     }
