@@ -67,13 +67,13 @@ __device__ __forceinline__ void factor_diag_block(float *P, int ldp, int lane, i
         r[j] = lij;
 #pragma unroll
         for (int t = j % 4 + 1; t < 4; ++t) r[4 * (j / 4) + t] = fmaf(-w, fv[t], r[4 * (j / 4) + t]);
+        const float2 nw = make_float2(-w, -w);
 #pragma unroll
         for (int q = j / 4 + 1; q < 8; ++q) {
             const float4 c4 = reinterpret_cast<const float4 *>(cb)[q];
-            r[4 * q] = fmaf(-w, c4.x, r[4 * q]);
-            r[4 * q + 1] = fmaf(-w, c4.y, r[4 * q + 1]);
-            r[4 * q + 2] = fmaf(-w, c4.z, r[4 * q + 2]);
-            r[4 * q + 3] = fmaf(-w, c4.w, r[4 * q + 3]);
+            float2 t0 = __ffma2_rn(nw, make_float2(c4.x, c4.y), make_float2(r[4 * q], r[4 * q + 1]));
+            float2 t1 = __ffma2_rn(nw, make_float2(c4.z, c4.w), make_float2(r[4 * q + 2], r[4 * q + 3]));
+            r[4 * q] = t0.x; r[4 * q + 1] = t0.y; r[4 * q + 2] = t1.x; r[4 * q + 3] = t1.y;
         }
     }
 #pragma unroll
@@ -88,7 +88,8 @@ __device__ __forceinline__ void factor_diag_block(float *P, int ldp, int lane, i
 
 // Step 2: row a (>= 32, panel coordinates) of panel p: x <- x L11^{-T}, with
 // L11 the panel's factored diagonal block and sinv its reciprocal diagonal;
-// the solved row is stored back and left in x.
+// the solved row is stored back and left in x. Here and in step 1 the updates
+// go by pairs of columns through the paired single-precision FMA.
 __device__ __forceinline__ void trsm_row_x(float *P, int ldp, int a, const float *sinv,
                                            float (&x)[32])
 {
@@ -100,14 +101,20 @@ __device__ __forceinline__ void trsm_row_x(float *P, int ldp, int a, const float
         if (j % 4 == 0) s4 = reinterpret_cast<const float4 *>(sinv)[j / 4];
         x[j] *= (j % 4 == 0) ? s4.x : (j % 4 == 1) ? s4.y : (j % 4 == 2) ? s4.z : s4.w;
         const float *Lj = P + j * ldp;  // column j of L11, rows 0..31
+        const float2 nx = make_float2(-x[j], -x[j]);
 #pragma unroll
         for (int q = (j + 1) / 4; q < 8; ++q) {
             const float4 l4 = reinterpret_cast<const float4 *>(Lj)[q];
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+            const float2 lp[2] = {make_float2(l4.x, l4.y), make_float2(l4.z, l4.w)};
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                const int k = 4 * q + t;
-                if (k > j) x[k] = fmaf(-x[j], lv[t], x[k]);
+            for (int h = 0; h < 2; ++h) {
+                const int k = 4 * q + 2 * h;
+                if (k > j) {
+                    const float2 t = __ffma2_rn(nx, lp[h], make_float2(x[k], x[k + 1]));
+                    x[k] = t.x; x[k + 1] = t.y;
+                } else if (k + 1 > j) {
+                    x[k + 1] = fmaf(-x[j], lp[h].y, x[k + 1]);
+                }
             }
         }
     }

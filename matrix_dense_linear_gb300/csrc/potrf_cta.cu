@@ -40,7 +40,9 @@ using namespace cta;
 __device__ int g_fail_first_wait;
 
 // Step 3: one 4 x 4 tile (I, K), I >= K, of the trailing lower triangle that
-// starts at c1 = c0 + 32; L21 is panel p's rows c1.. .
+// starts at c1 = c0 + 32; L21 is panel p's rows c1.. . Pairs of rows go through
+// the paired single-precision FMA (two fused multiply-adds, each rounded as
+// fmaf, in one instruction).
 template <int NB>
 __device__ __forceinline__ void syrk_tile(float *S, const float *P, int ldp, int c0, int c1,
                                           int I, int K)
@@ -50,11 +52,11 @@ __device__ __forceinline__ void syrk_tile(float *S, const float *P, int ldp, int
     const int q = gk >> 5;
     const int ldq = Gm::ld(q);
     float *C = S + Gm::off(q) + (gi - 32 * q) + (gk - 32 * q) * ldq;
-    float acc[4][4];
+    float2 acc[4][2];  // acc[b][h]: rows 2h, 2h + 1 of tile column b
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
         const float4 c4 = *reinterpret_cast<const float4 *>(C + b * ldq);
-        acc[b][0] = c4.x; acc[b][1] = c4.y; acc[b][2] = c4.z; acc[b][3] = c4.w;
+        acc[b][0] = make_float2(c4.x, c4.y); acc[b][1] = make_float2(c4.z, c4.w);
     }
     const float *Li = P + (gi - c0);
     const float *Lk = P + (gk - c0);
@@ -62,17 +64,19 @@ __device__ __forceinline__ void syrk_tile(float *S, const float *P, int ldp, int
     for (int k = 0; k < 32; ++k) {
         const float4 a4 = *reinterpret_cast<const float4 *>(Li + k * ldp);
         const float4 b4 = *reinterpret_cast<const float4 *>(Lk + k * ldp);
-        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+        const float2 ap[2] = {make_float2(a4.x, a4.y), make_float2(a4.z, a4.w)};
         const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
-        for (int b = 0; b < 4; ++b)
+        for (int b = 0; b < 4; ++b) {
+            const float2 nb = make_float2(-bv[b], -bv[b]);
 #pragma unroll
-            for (int a = 0; a < 4; ++a) acc[b][a] = fmaf(-av[a], bv[b], acc[b][a]);
+            for (int h = 0; h < 2; ++h) acc[b][h] = __ffma2_rn(nb, ap[h], acc[b][h]);
+        }
     }
 #pragma unroll
     for (int b = 0; b < 4; ++b)
         *reinterpret_cast<float4 *>(C + b * ldq) =
-            make_float4(acc[b][0], acc[b][1], acc[b][2], acc[b][3]);
+            make_float4(acc[b][0].x, acc[b][0].y, acc[b][1].x, acc[b][1].y);
 }
 
 __device__ __forceinline__ void tri_index(int t, int &I, int &K)
