@@ -530,7 +530,8 @@ def run_ours(args, rank: int, world: int, barrier) -> dict | None:
                 rows.append({"workload": name, "n": n, "batch": batch,
                              "ms_per_call": per_call, "matrices_per_s": batch / (per_call / 1e3),
                              "gflops": batch * flops_per_matrix(n) / (per_call / 1e3) / 1e9,
-                             "roofline": {**{k: rf[k] for k in ("bound", "frac", "roof_ms")},
+                             "roofline": {**{k: rf[k] for k in ("bound", "frac", "roof_ms",
+                                                                "frac_sector_rounded") if k in rf},
                                           "traffic": roof["traffic"],
                                           "traffic_scope": roof["traffic_scope"]},
                              "launches_per_call": nl, "e2e": out["e2e"],
