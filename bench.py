@@ -47,8 +47,8 @@ TRAFFIC = {
     "n32": (('matrix_dense_linear_gb300/csrc/potrf_warp.cu', 'matrix_dense_linear_gb300/csrc/bl_common.cuh'), "67514fa4e72bb6b5", 4219904, "per launch"),
     "n64": (('matrix_dense_linear_gb300/csrc/potrf_warp.cu', 'matrix_dense_linear_gb300/csrc/bl_common.cuh'), "67514fa4e72bb6b5", 12660224, "per launch"),
     "n128": (('matrix_dense_linear_gb300/csrc/potrf_cta.cu', 'matrix_dense_linear_gb300/csrc/cta_common.cuh', 'matrix_dense_linear_gb300/csrc/bl_common.cuh', 'matrix_dense_linear_gb300/csrc/tc_sm100.cuh'), "7edaae49fb143436", 42140000, "per launch"),
-    "n256": (('matrix_dense_linear_gb300/csrc/potrf_blocked.cu', 'matrix_dense_linear_gb300/csrc/potrf_cta.cu', 'matrix_dense_linear_gb300/csrc/cta_common.cuh', 'matrix_dense_linear_gb300/csrc/trsm_tc.cu', 'matrix_dense_linear_gb300/csrc/syrk_tc.cu', 'matrix_dense_linear_gb300/csrc/tc_sm100.cuh', 'matrix_dense_linear_gb300/csrc/bl_common.cuh'), "2b9c4910ca0059e1", 1708000000, "per call (4 launches)"),
-    "n1024": (('matrix_dense_linear_gb300/csrc/potrf_blocked.cu', 'matrix_dense_linear_gb300/csrc/potrf_cta.cu', 'matrix_dense_linear_gb300/csrc/cta_common.cuh', 'matrix_dense_linear_gb300/csrc/trsm_tc.cu', 'matrix_dense_linear_gb300/csrc/syrk_tc.cu', 'matrix_dense_linear_gb300/csrc/tc_sm100.cuh', 'matrix_dense_linear_gb300/csrc/bl_common.cuh'), "2b9c4910ca0059e1", 5740000000, "per call (21 launches)"),
+    "n256": (('matrix_dense_linear_gb300/csrc/potrf_blocked.cu', 'matrix_dense_linear_gb300/csrc/potrf_cta.cu', 'matrix_dense_linear_gb300/csrc/cta_common.cuh', 'matrix_dense_linear_gb300/csrc/trsm_tc.cu', 'matrix_dense_linear_gb300/csrc/syrk_tc.cu', 'matrix_dense_linear_gb300/csrc/tc_sm100.cuh', 'matrix_dense_linear_gb300/csrc/bl_common.cuh'), "42f7d5f3f7ba33c0", 1708000000, "per call (4 launches)"),
+    "n1024": (('matrix_dense_linear_gb300/csrc/potrf_blocked.cu', 'matrix_dense_linear_gb300/csrc/potrf_cta.cu', 'matrix_dense_linear_gb300/csrc/cta_common.cuh', 'matrix_dense_linear_gb300/csrc/trsm_tc.cu', 'matrix_dense_linear_gb300/csrc/syrk_tc.cu', 'matrix_dense_linear_gb300/csrc/tc_sm100.cuh', 'matrix_dense_linear_gb300/csrc/bl_common.cuh'), "42f7d5f3f7ba33c0", 6120000000, "per call (22 launches)"),
 }
 
 
@@ -83,16 +83,22 @@ def sector_bytes_per_matrix(n: int) -> int:
 
 def launches_per_call(n: int, batch: int = 0) -> int:
     """Kernels one lower-storage call on a 16-byte-aligned batch launches: one
-    for n <= 128; above, per 128-wide panel the diagonal factor, the panel
-    solve and the trailing update, except that the last panel has only its
-    factor and a one-tile trailing matrix is updated inside the panel solve
-    when the call holds at most 2048 matrices and no delayed update is pending
-    (the blocked driver's schedule)."""
+    for n <= 128; above, on large batches the left-looking order (per panel
+    its update, factor and solve), else per 128-wide panel the diagonal factor,
+    the panel solve and the trailing update, except that the last panel has
+    only its factor and a one-tile trailing matrix is updated inside the panel
+    solve when the call holds at most 2048 matrices and no delayed update is
+    pending (the blocked driver's schedule)."""
     if n <= 128:
         return 1
     panels = (n + 127) // 128
     count, pending = 0, False
     sms = 152
+    if n > 256 and batch * ((n - 1) // 128) >= 10 * sms:
+        # the left-looking order of large batches: per panel its update by the
+        # earlier panels (not the first), its diagonal factor, its panel solve
+        # (not the last)
+        return 3 * panels - 2
     for p in range(panels):
         count += 1  # diagonal factor
         m = n - 128 * (p + 1)
@@ -241,6 +247,7 @@ class DeviceWorkload:
 
     uplo = "L"
     work = None  # a device workspace: the call is bl_spotrf_batched_ws
+    route = 0    # a forced route (bl_spotrf_batched_ex / _uplo_ex), 0: the automatic one
 
     def use_workspace(self) -> None:
         import torch
@@ -252,7 +259,10 @@ class DeviceWorkload:
     def call(self, i: int, stream) -> None:
         import matrix_dense_linear_gb300 as bl
         bt = self.bt
-        if self.work is not None:
+        if self.route:
+            code = bl.spotrf_batched_uplo(self.uplo, self.rep[i].data_ptr(), bt.n, bt.lda,
+                                          bt.strideA, bt.batch, self.info, stream, self.route)
+        elif self.work is not None:
             code = bl.spotrf_batched_ws(self.rep[i].data_ptr(), bt.n, bt.lda, bt.strideA,
                                         bt.batch, self.info, self.work, stream=stream,
                                         uplo=self.uplo)
@@ -682,6 +692,7 @@ def run_shapes(args) -> list:
         bt = type(base)(buf=buf, n=n, lda=n, strideA=n * n, batch=batch, fill=base.fill)
         w = DeviceWorkload(bt, args.steps, dev)
         w.uplo = args.uplo
+        w.route = args.route
         if args.ws:
             w.use_workspace()
         for i in range(min(args.warmup, w.nrep)):
@@ -692,7 +703,8 @@ def run_shapes(args) -> list:
         ms = statistics.median(time_steps(w, k, lambda: None) / k for _ in range(3))
         assert not w.info.cpu().numpy().any()
         rf = roofline_entry("shape", n, batch, ms, pk, sms)
-        row = {"shape": spec, "uplo": args.uplo, "workspace": bool(args.ws), "n": n,
+        row = {"shape": spec, "uplo": args.uplo, "workspace": bool(args.ws), "route": args.route,
+               "n": n,
                "batch": batch, "ms_per_call": ms,
                "us_per_call": ms * 1e3, "matrices_per_s": batch / (ms / 1e3),
                "tflops": flops_per_matrix(n) * batch / (ms / 1e3) / 1e12,
@@ -942,6 +954,9 @@ def main():
                          "factorization for --shapes")
     ap.add_argument("--ws", action="store_true",
                     help="--shapes through bl_spotrf_batched_ws (a caller workspace)")
+    ap.add_argument("--route", type=int, default=0,
+                    help="--shapes: force a route (bl_spotrf_batched_ex): 3 the right-looking "
+                         "blocked schedule, 5 the left-looking one; 0 the automatic choice")
     ap.add_argument("--uplo", choices=["L", "U"], default="L",
                     help="storage of the factor for --shapes (U: upper triangle)")
     args = ap.parse_args()

@@ -56,6 +56,9 @@ extern "C" {
                                panel triangular solve, lower-only trailing update, any n */
 #define BL_ROUTE_TMEM 4     /* K2t: one thread block per matrix, the matrix resident in tensor
                                memory, trailing updates on the tensor cores, n <= 128 */
+#define BL_ROUTE_LEFT 5     /* K3's kernels in the left-looking order: per panel, its columns
+                               updated by every earlier panel at once, then its diagonal
+                               factor and panel solve; n > 128 (unaligned batches: K3) */
 
 /*
  * bl_spotrf_batched - factor a strided batch in place.
@@ -98,7 +101,8 @@ int bl_spotrf_batched(float *A, int n, int lda, int64_t strideA, int batch, int 
  * bl_spotrf_batched_ex - as bl_spotrf_batched, with the kernel class forced
  * (route = BL_ROUTE_*; BL_ROUTE_AUTO selects by n like bl_spotrf_batched).
  * Returns -8 when the forced route cannot factor this n (WARP: n > 64;
- * CTA or TMEM: n > 128), after the checks above. For tests and measurement.
+ * CTA or TMEM: n > 128; LEFT: n <= 128), after the checks above. For tests
+ * and measurement.
  */
 int bl_spotrf_batched_ex(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                          cudaStream_t stream, int route);

@@ -12,14 +12,14 @@ import ctypes
 import os
 from typing import Optional
 
-__all__ = ["ROUTE_AUTO", "ROUTE_WARP", "ROUTE_CTA", "ROUTE_BLOCKED", "ROUTE_TMEM", "MAX_N",
+__all__ = ["ROUTE_AUTO", "ROUTE_WARP", "ROUTE_CTA", "ROUTE_BLOCKED", "ROUTE_TMEM", "ROUTE_LEFT", "MAX_N",
            "BLError",
            "library", "library_path", "spotrf_batched", "spotrf_batched_ex", "route",
            "kernel_info", "version", "factor", "factor_host", "spotrs_batched",
            "workspace_bytes", "spotrf_batched_ws",
            "sposv_batched", "solve", "factor_solve"]
 
-ROUTE_AUTO, ROUTE_WARP, ROUTE_CTA, ROUTE_BLOCKED, ROUTE_TMEM = 0, 1, 2, 3, 4
+ROUTE_AUTO, ROUTE_WARP, ROUTE_CTA, ROUTE_BLOCKED, ROUTE_TMEM, ROUTE_LEFT = 0, 1, 2, 3, 4, 5
 MAX_N = 4096
 _PKG = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_PKG, "libbl_spotrf.so")

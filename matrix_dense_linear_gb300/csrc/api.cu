@@ -58,6 +58,7 @@ bool route_can_run(int route, int n, bool upper)
     case BL_ROUTE_CTA: return n <= kCtaMaxN;
     case BL_ROUTE_TMEM: return n <= kCtaMaxN && !upper;
     case BL_ROUTE_BLOCKED: return true;
+    case BL_ROUTE_LEFT: return n > kCtaMaxN;
     default: return false;
     }
 }
@@ -81,6 +82,7 @@ int run(float *A, int n, int lda, int64_t strideA, int batch, int *info, cudaStr
                               host_mapped);
     case BL_ROUTE_TMEM:
         return bl::launch_tmem(A, n, lda, strideA, batch, info, stream, bl::InfoMode{-1});
+    case BL_ROUTE_LEFT: return bl::launch_left(A, n, lda, strideA, batch, info, stream, upper);
     default: return bl::launch_blocked(A, n, lda, strideA, batch, info, stream, upper, W);
     }
 }
@@ -385,7 +387,7 @@ int bl_spotrf_batched_uplo_ex(char uplo, float *A, int n, int lda, int64_t strid
 {
     const int u = parse_uplo(uplo);
     if (u < 0) return -1;
-    if (route < BL_ROUTE_AUTO || route > BL_ROUTE_TMEM) return -9;
+    if (route < BL_ROUTE_AUTO || route > BL_ROUTE_LEFT) return -9;
     return shift_arg(run(A, n, lda, strideA, batch, info, stream, route, u == 1));
 }
 
@@ -399,7 +401,7 @@ int bl_spotrf_batched(float *A, int n, int lda, int64_t strideA, int batch, int 
 int bl_spotrf_batched_ex(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                          cudaStream_t stream, int route)
 {
-    if (route < BL_ROUTE_AUTO || route > BL_ROUTE_TMEM) return -8;
+    if (route < BL_ROUTE_AUTO || route > BL_ROUTE_LEFT) return -8;
     return run(A, n, lda, strideA, batch, info, stream, route);
 }
 

@@ -52,6 +52,9 @@ int launch_tmem(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                 cudaStream_t stream, InfoMode mode);
 // W: the caller's workspace for the inverse-based panel solve (kInvBytes per
 // matrix, 16-byte aligned), or nullptr (substitution only)
+// the left-looking schedule of the same kernels (BL_ROUTE_LEFT)
+int launch_left(float *A, int n, int lda, int64_t strideA, int batch, int *info,
+                cudaStream_t stream, bool upper);
 int launch_blocked(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                    cudaStream_t stream, bool upper, float *W = nullptr);
 constexpr size_t kInvBytes = 128 * 128 * sizeof(float);

@@ -18,6 +18,10 @@
 // driver on "kernelbot-cholesky-930185", whose measured defect (a full-square
 // trailing update costing 2n^3/3) the lower-only tiling avoids.
 //
+// Large batches of more than two panels take the left-looking order of the
+// same kernels instead (launch_left, below): per panel its columns updated by
+// every earlier panel at once, then its diagonal factor and panel solve.
+//
 // A matrix whose info is already nonzero after a panel is skipped by every
 // later launch.
 #include <mutex>
@@ -334,6 +338,21 @@ static bool delay_pays(int m, int batch, int sms)
     return (int64_t)batch * (T * (T + 1) / 2) >= 8 * 2 * (int64_t)sms;
 }
 
+// Whether the left-looking schedule pays: its per-panel update launch covers
+// batch x (row tiles of the panel) tiles with k growing by 128 a panel, so it
+// wins once the first of them spans about five waves (two tiles an SM): on
+// GB300, 1024 x 512 2.43 against 2.58 ms, 1024 x 1024 4.61 against 5.01,
+// 1536 x 256 3.63 against 3.95, 2048 x 128 4.18 against 4.41; it loses below
+// (2048 x 64 2.58 against 2.49 ms, 3072 x 16 3.09 against 2.44, one matrix of
+// order 1024 0.45 against 0.33), where the longer updates sit on the panel
+// chain. Two panels (n <= 256) keep the right-looking order, which fuses a
+// one-tile update into the panel solve (200 x 4096: 0.65 against 0.69 ms).
+static bool left_pays(int n, int batch, int sms)
+{
+    const int64_t rows_below = (n - 1) / kTile;  // row tiles below the first panel
+    return n > 2 * kTile && (int64_t)batch * rows_below >= 10 * (int64_t)sms;
+}
+
 int launch_blocked(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                    cudaStream_t stream, bool upper, float *W)
 {
@@ -346,6 +365,11 @@ int launch_blocked(float *A, int n, int lda, int64_t strideA, int batch, int *in
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return (int)cudaGetLastError();
+    // large batches of aligned panels (no workspace): the left-looking order
+    const bool aligned = ((reinterpret_cast<uintptr_t>(A) & 15) == 0) && (lda & 3) == 0 &&
+                         (strideA & 3) == 0;
+    if (W == nullptr && aligned && left_pays(n, batch, sms))
+        return launch_left(A, n, lda, strideA, batch, info, stream, upper);
     for (int c0 = 0; c0 < n; c0 += kNb) {
         const int nb = n - c0 < kNb ? n - c0 : kNb;
         int e = launch_cta(A + c0 + (int64_t)c0 * lda, nb, lda, strideA, batch, info, stream,
@@ -413,6 +437,35 @@ int launch_blocked(float *A, int n, int lda, int64_t strideA, int batch, int *in
             }
         }
         if (e) return e;
+    }
+    return 0;
+}
+
+// The left-looking schedule of the same kernels (a forced route, measured
+// against the right-looking one): per panel p, its columns are first updated
+// by every earlier panel at once, A[c0:, c0:c0+128] -= L[c0:, :c0] L[c0:c0+128, :c0]^T
+// (the tensor-core update in its one-tile-column form with k = c0), then its
+// diagonal block is factored and its rows below solved. Each element of the
+// panel is written once per panel instead of once per earlier panel, but the
+// update's k, and so its latency, grows with p. Unaligned batches take the
+// right-looking driver.
+int launch_left(float *A, int n, int lda, int64_t strideA, int batch, int *info,
+                cudaStream_t stream, bool upper)
+{
+    if (((reinterpret_cast<uintptr_t>(A) & 15) != 0) || (lda & 3) || (strideA & 3))
+        return launch_blocked(A, n, lda, strideA, batch, info, stream, upper, nullptr);
+    for (int c0 = 0; c0 < n; c0 += kNb) {
+        const int nb = n - c0 < kNb ? n - c0 : kNb;
+        int e = 0;
+        if (c0 > 0 &&
+            (e = launch_syrk_tc(A, n, lda, strideA, batch, info, 0, c0, true, stream, upper)))
+            return e;
+        if ((e = launch_cta(A + c0 + (int64_t)c0 * lda, nb, lda, strideA, batch, info, stream,
+                            InfoMode{c0 == 0 ? -1 : c0}, upper)))
+            return e;
+        if (n - c0 - nb <= 0) break;
+        if ((e = launch_trsm_tc(A, n, lda, strideA, batch, info, c0, stream, upper, false)))
+            return e;
     }
     return 0;
 }

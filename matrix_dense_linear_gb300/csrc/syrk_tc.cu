@@ -341,7 +341,7 @@ int launch_syrk_tc(float *A, int n, int lda, int64_t strideA, int batch, int *in
                    int nk, bool narrow, cudaStream_t stream, bool upper)
 {
     if (((reinterpret_cast<uintptr_t>(A) & 15) != 0) || (lda & 3) || (strideA & 3)) return 1;
-    if ((nk != kNbTc && nk != 2 * kNbTc) || n - c0 - nk <= 0) return -1;
+    if (nk <= 0 || nk % kKs != 0 || n - c0 - nk <= 0) return -1;
     return upper ? launch_u<true>(A, n, lda, strideA, batch, info, c0, nk, narrow, stream)
                  : launch_u<false>(A, n, lda, strideA, batch, info, c0, nk, narrow, stream);
 }

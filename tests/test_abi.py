@@ -186,7 +186,8 @@ def test_forced_route_that_cannot_run(bl):
     assert lib.bl_spotrf_batched_ex(8, 65, 65, 65 * 65, 1, 8, None, bl.ROUTE_WARP) == -8
     assert lib.bl_spotrf_batched_ex(8, 129, 129, 129 * 129, 1, 8, None, bl.ROUTE_CTA) == -8
     assert lib.bl_spotrf_batched_ex(8, 129, 129, 129 * 129, 1, 8, None, bl.ROUTE_TMEM) == -8
-    assert lib.bl_spotrf_batched_ex(8, 4, 4, 16, 1, 8, None, bl.ROUTE_TMEM + 1) == -8
+    assert lib.bl_spotrf_batched_ex(8, 4, 4, 16, 1, 8, None, bl.ROUTE_LEFT + 1) == -8
+    assert lib.bl_spotrf_batched_ex(8, 128, 128, 128 * 128, 1, 8, None, bl.ROUTE_LEFT) == -8
     assert lib.bl_spotrf_batched_ex(8, 4, 4, 16, 1, 8, None, 9) == -8
     assert lib.bl_spotrf_batched_ex(8, 4, 4, 16, 1, 8, None, -1) == -8
     # argument errors come first

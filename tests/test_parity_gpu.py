@@ -17,7 +17,7 @@ from tests.gpu_helpers import assert_untouched, compare, run_gpu
 
 pytestmark = pytest.mark.gpu
 
-WARP, CTA, BLOCKED, TMEM = 1, 2, 3, 4
+WARP, CTA, BLOCKED, TMEM, LEFT = 1, 2, 3, 4, 5
 
 
 def _routes(n):
@@ -26,6 +26,8 @@ def _routes(n):
         r.append(WARP)
     if n <= 128:
         r += [CTA, TMEM]
+    else:
+        r.append(LEFT)
     return sorted(set(r))
 
 
@@ -51,12 +53,13 @@ def test_orders_every_route(n):
         assert_untouched(out, bt.buf, bt, what=f"n={n} route={route}")
 
 
+@pytest.mark.parametrize("route", [0, LEFT])
 @pytest.mark.parametrize("n", [1000, 1024])
-def test_large_orders(n):
+def test_large_orders(n, route):
     bt = _gram_batch(n, 2, 300 + n, fill="nan")
-    out, info = run_gpu(bt)
-    compare(bt, out, info, what=f"n={n}")
-    assert_untouched(out, bt.buf, bt, what=f"n={n}")
+    out, info = run_gpu(bt, route)
+    compare(bt, out, info, what=f"n={n} route={route}")
+    assert_untouched(out, bt.buf, bt, what=f"n={n} route={route}")
 
 
 @pytest.mark.parametrize("n", [2048, 3000, 4096])

@@ -110,6 +110,8 @@ def _routes(n):
         r.append(WARP)
     if n <= 128:
         r.append(CTA)
+    else:
+        r.append(5)  # the left-looking schedule
     return sorted(set(r))
 
 
