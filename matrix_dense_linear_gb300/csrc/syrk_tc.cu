@@ -44,8 +44,9 @@ namespace {
 
 constexpr int kNbTc = 128;                 // panel width
 constexpr int kKs = 16;                    // k columns per shared-memory slice
-constexpr uint32_t kLbo = 128;             // K-adjacent core matrices
-constexpr uint32_t kSbo = (kKs / 4) * 128 + 16;  // row-group stride, +16 B: no bank conflicts
+constexpr uint32_t kLbo = 144;             // K-adjacent core matrices, +16 B: the upper storage's
+                                           // staging stores (a row's four k quads) on distinct banks
+constexpr uint32_t kSbo = (kKs / 4) * kLbo + 16;  // row-group stride, +16 B: no bank conflicts
 constexpr uint32_t kTileBytes = 16 * kSbo;  // 128 rows
 constexpr uint32_t kStageBytes = 4 * kTileBytes;  // A hi, A lo, B hi, B lo
 constexpr int kStages = 3;                 // operand buffers in the ring
