@@ -157,15 +157,30 @@ trsm_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0, i
     }
     cp_async_commit();
 
-    // -A21 rows, this thread's row: column chunks of 32 (16-byte loads along the
-    // row in the upper storage, one column at a time in the lower)
+    // -A21 rows, this thread's row: column chunks of 32 (one column at a time in
+    // the lower storage). In the upper storage a row is contiguous: the warp
+    // reads its 32 rows four at a time, a quarter warp a row's 128 bytes, and
+    // passes them through its slice of the X region (free until the first
+    // X operand is staged), so that every load is a whole line
     const float *g = Ab + (live ? lidx<UP>(R, c0, lda) : 0);  // g[c * xs] = (R, c0 + c)
+    const int Rw = c0 + 128 + rb * 128 + 32 * warp;            // the warp's first row
+    float *tb = reinterpret_cast<float *>(smem + kOffX) + warp * (32 * 36);  // [32][36]
     auto load_chunk = [&](int q, float (&v)[32]) {
         if constexpr (UP) {
+            __syncwarp();  // the slice's previous contents are read
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = 4 * i + (lane >> 3), cq = lane & 7;
+                const float4 a = Rw + r < n
+                    ? *reinterpret_cast<const float4 *>(Ab + (c0 + 32 * q + 4 * cq) +
+                                                        (int64_t)(Rw + r) * lda)
+                    : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                *reinterpret_cast<float4 *>(tb + r * 36 + 4 * cq) = a;
+            }
+            __syncwarp();
 #pragma unroll
             for (int c = 0; c < 32; c += 4) {
-                const float4 a = live ? *reinterpret_cast<const float4 *>(g + 32 * q + c)
-                                      : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                const float4 a = *reinterpret_cast<const float4 *>(tb + lane * 36 + c);
                 v[c] = -a.x; v[c + 1] = -a.y; v[c + 2] = -a.z; v[c + 3] = -a.w;
             }
         } else {
@@ -242,17 +257,26 @@ trsm_tc_kernel(float *__restrict__ A, int n, int lda, int64_t strideA, int c0, i
                 }
             }
         }
-        if (live) {
-            float *out = Ab + lidx<UP>(R, c0 + 32 * j, lda);
-            if constexpr (UP) {
+        if constexpr (UP) {
+            // through the warp's slice of the X region (the MMAs of block j - 1
+            // that read it are complete), a quarter warp writing a row's 128 bytes
 #pragma unroll
-                for (int t = 0; t < 32; t += 4)
-                    *reinterpret_cast<float4 *>(out + t) =
-                        make_float4(x[t], x[t + 1], x[t + 2], x[t + 3]);
-            } else {
+            for (int t = 0; t < 32; t += 4)
+                *reinterpret_cast<float4 *>(tb + lane * 36 + t) =
+                    make_float4(x[t], x[t + 1], x[t + 2], x[t + 3]);
+            __syncwarp();
 #pragma unroll
-                for (int t = 0; t < 32; ++t) out[(int64_t)t * xs] = x[t];
+            for (int i = 0; i < 8; ++i) {
+                const int r = 4 * i + (lane >> 3), cq = lane & 7;
+                if (Rw + r < n)
+                    *reinterpret_cast<float4 *>(Ab + (c0 + 32 * j + 4 * cq) + (int64_t)(Rw + r) * lda) =
+                        *reinterpret_cast<const float4 *>(tb + r * 36 + 4 * cq);
             }
+            __syncthreads();  // every warp is done with its slice before X is staged
+        } else if (live) {
+            float *out = Ab + lidx<UP>(R, c0 + 32 * j, lda);
+#pragma unroll
+            for (int t = 0; t < 32; ++t) out[(int64_t)t * xs] = x[t];
         }
         if (j == 3 && !FUSED) break;
         // X_j as the A operand (K-major, hi/lo)
