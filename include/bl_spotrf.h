@@ -109,8 +109,11 @@ int bl_spotrf_batched_ex(float *A, int n, int lda, int64_t strideA, int batch, i
 
 /*
  * bl_spotrf_route - the route bl_spotrf_batched takes for (n, batch). Host
- * only, needs no GPU. Returns BL_ROUTE_WARP/CTA/BLOCKED, or 0 when nothing
- * would be launched (n <= 0 or batch <= 0).
+ * only, needs no GPU. Returns BL_ROUTE_WARP/CTA/BLOCKED, BL_ROUTE_LEFT where
+ * the blocked route takes its left-looking order (large batches above n = 256,
+ * for 16-byte-aligned batches; judged by the current device's SM count, 152
+ * when no device is visible), or 0 when nothing would be launched (n <= 0 or
+ * batch <= 0).
  */
 int bl_spotrf_route(int n, int batch);
 

@@ -408,7 +408,11 @@ int bl_spotrf_batched_ex(float *A, int n, int lda, int64_t strideA, int batch, i
 int bl_spotrf_route(int n, int batch)
 {
     if (n <= 0 || batch <= 0) return 0;
-    return route_for(n);
+    const int r = route_for(n);
+    if (r == BL_ROUTE_BLOCKED && n <= BL_SPOTRF_MAX_N &&
+        bl::left_pays(n, batch, bl::sm_count_or_default()))
+        return BL_ROUTE_LEFT;
+    return r;
 }
 
 int bl_spotrf_kernel_info(int route, int n, int *regs, int *local_bytes, int *static_smem,

@@ -52,6 +52,11 @@ int launch_tmem(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                 cudaStream_t stream, InfoMode mode);
 // W: the caller's workspace for the inverse-based panel solve (kInvBytes per
 // matrix, 16-byte aligned), or nullptr (substitution only)
+// whether the automatic blocked route takes the left-looking order (aligned
+// panels, no workspace), and the SM count it judges by (152 when no device is
+// visible)
+bool left_pays(int n, int batch, int sms);
+int sm_count_or_default();
 // the left-looking schedule of the same kernels (BL_ROUTE_LEFT)
 int launch_left(float *A, int n, int lda, int64_t strideA, int batch, int *info,
                 cudaStream_t stream, bool upper);

@@ -347,7 +347,7 @@ static bool delay_pays(int m, int batch, int sms)
 // order 1024 0.45 against 0.33), where the longer updates sit on the panel
 // chain. Two panels (n <= 256) keep the right-looking order, which fuses a
 // one-tile update into the panel solve (200 x 4096: 0.65 against 0.69 ms).
-static bool left_pays(int n, int batch, int sms)
+bool left_pays(int n, int batch, int sms)
 {
     const int64_t rows_below = (n - 1) / kTile;  // row tiles below the first panel
     return n > 2 * kTile && (int64_t)batch * rows_below >= 10 * (int64_t)sms;
@@ -441,9 +441,24 @@ int launch_blocked(float *A, int n, int lda, int64_t strideA, int batch, int *in
     return 0;
 }
 
-// The left-looking schedule of the same kernels (a forced route, measured
-// against the right-looking one): per panel p, its columns are first updated
-// by every earlier panel at once, A[c0:, c0:c0+128] -= L[c0:, :c0] L[c0:c0+128, :c0]^T
+// The SM count of the current device; 152 (a GB300's) when none is visible,
+// so that the route query answers on a host without a GPU.
+int sm_count_or_default()
+{
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= 0) {
+        cudaGetLastError();  // no device visible: clear the error
+        return 152;
+    }
+    return sms;
+}
+
+// The left-looking schedule of the same kernels (the blocked driver's choice
+// where left_pays holds, and a forced route above order 128): per panel p, its
+// columns are first updated by every earlier panel at once,
+// A[c0:, c0:c0+128] -= L[c0:, :c0] L[c0:c0+128, :c0]^T
 // (the tensor-core update in its one-tile-column form with k = c0), then its
 // diagonal block is factored and its rows below solved. Each element of the
 // panel is written once per panel instead of once per earlier panel, but the

@@ -201,7 +201,13 @@ def test_route_selection(bl):
     for n in (65, 100, 128):
         assert bl.route(n, 1024) == bl.ROUTE_CTA
     for n in (129, 256, 1024, 4096):
-        assert bl.route(n, 512) == bl.ROUTE_BLOCKED
+        assert bl.route(n, 8) == bl.ROUTE_BLOCKED
+    # large batches above n = 256: the left-looking order (152 SMs assumed
+    # without a device: batch x row tiles below the first panel >= 1520)
+    assert bl.route(256, 4096) == bl.ROUTE_BLOCKED
+    assert bl.route(1024, 512) == bl.ROUTE_LEFT
+    assert bl.route(1024, 128) == bl.ROUTE_BLOCKED
+    assert bl.route(2048, 128) == bl.ROUTE_LEFT
 
 
 def test_no_stack_no_spill(bl):
