@@ -136,9 +136,16 @@ def kernel_source(n: int) -> str:
     return os.path.join(d, "syrk_tc.cu")
 
 
-def traffic_for(name: str, n: int):
+def traffic_for(name: str, n: int, batch: int | None = None):
+    """The captured DRAM bytes of workload `name`, or None when its sources
+    changed since the capture or the run's batch is not the workload's own
+    (the figure was taken at that batch)."""
     ent = TRAFFIC.get(name)
     if not ent:
+        return None
+    import synth
+    wl = synth.WORKLOADS.get(name)
+    if wl is None or n != wl.n or (batch is not None and batch != wl.batch):
         return None
     srcs, sha, nbytes, _ = ent
     h = hashlib.sha256()
@@ -497,7 +504,7 @@ def run_ours(args, rank: int, world: int, barrier) -> dict | None:
     rf = roofline_entry(args.workload, n, batch, per_call, pk, sms)
     nl = launches_per_call(n, batch)
     roof = {"bound": rf["bound"], "achieved": rf["achieved"], "peak": rf["peak"],
-            "unit": rf["unit"], "frac": rf["frac"], "traffic": traffic_for(args.workload, n),
+            "unit": rf["unit"], "frac": rf["frac"], "traffic": traffic_for(args.workload, n, batch),
             "traffic_scope": TRAFFIC[args.workload][3] if args.workload in TRAFFIC else None,
             "kernel": dominant_kernel(n), "peak_source": pk["source"],
             "peak_note": ("HBM: measured copy bandwidth" if rf["bound"] == "hbm" else
@@ -572,7 +579,7 @@ def run_ours(args, rank: int, world: int, barrier) -> dict | None:
                    "roofline": {k: r2[k] for k in ("bound", "frac", "roof_ms",
                                                    "frac_sector_rounded") if k in r2},
                    "launches_per_call": launches_per_call(b2.n, b2.batch)}
-            row["roofline"]["traffic"] = traffic_for(name, b2.n)
+            row["roofline"]["traffic"] = traffic_for(name, b2.n, b2.batch)
             row["roofline"]["traffic_scope"] = TRAFFIC[name][3] if name in TRAFFIC else None
             # the same workload end to end through the host-buffer call
             e2 = e2e_steps(w2, min(args.steps, 5), 2, lambda: None)

@@ -72,3 +72,14 @@ def test_traffic_is_null_once_its_sources_change(monkeypatch):
     monkeypatch.setitem(bench.TRAFFIC, "n64", (srcs, "0" * 16, nbytes, scope))
     assert bench.traffic_for("n64", 64) is None
     assert bench.traffic_for("no-such-workload", 64) is None
+
+
+def test_traffic_is_null_off_the_captured_batch():
+    # the figures were captured on each workload's own batch; another batch
+    # (bench.py --batch) does not rescale them
+    for name, (_, _, nbytes, _) in bench.TRAFFIC.items():
+        n = int(name[1:])
+        batch = {"n32": 1024, "n64": 1024, "n128": 1024, "n256": 4096, "n1024": 512}[name]
+        assert bench.traffic_for(name, n, batch) == nbytes
+        assert bench.traffic_for(name, n, batch // 2) is None
+        assert bench.traffic_for(name, n + 1, batch) is None
