@@ -47,8 +47,8 @@ TRAFFIC = {
     "n32": (('matrix_dense_linear_gb300/csrc/potrf_warp.cu', 'matrix_dense_linear_gb300/csrc/bl_common.cuh'), "67514fa4e72bb6b5", 4219904, "per launch"),
     "n64": (('matrix_dense_linear_gb300/csrc/potrf_warp.cu', 'matrix_dense_linear_gb300/csrc/bl_common.cuh'), "67514fa4e72bb6b5", 12660224, "per launch"),
     "n128": (('matrix_dense_linear_gb300/csrc/potrf_cta.cu', 'matrix_dense_linear_gb300/csrc/cta_common.cuh', 'matrix_dense_linear_gb300/csrc/bl_common.cuh', 'matrix_dense_linear_gb300/csrc/tc_sm100.cuh'), "7edaae49fb143436", 42140000, "per launch"),
-    "n256": (('matrix_dense_linear_gb300/csrc/potrf_blocked.cu', 'matrix_dense_linear_gb300/csrc/potrf_cta.cu', 'matrix_dense_linear_gb300/csrc/cta_common.cuh', 'matrix_dense_linear_gb300/csrc/trsm_tc.cu', 'matrix_dense_linear_gb300/csrc/syrk_tc.cu', 'matrix_dense_linear_gb300/csrc/tc_sm100.cuh', 'matrix_dense_linear_gb300/csrc/bl_common.cuh'), "30122f956b728464", 1708000000, "per call (4 launches)"),
-    "n1024": (('matrix_dense_linear_gb300/csrc/potrf_blocked.cu', 'matrix_dense_linear_gb300/csrc/potrf_cta.cu', 'matrix_dense_linear_gb300/csrc/cta_common.cuh', 'matrix_dense_linear_gb300/csrc/trsm_tc.cu', 'matrix_dense_linear_gb300/csrc/syrk_tc.cu', 'matrix_dense_linear_gb300/csrc/tc_sm100.cuh', 'matrix_dense_linear_gb300/csrc/bl_common.cuh'), "30122f956b728464", 6120000000, "per call (22 launches)"),
+    "n256": (('matrix_dense_linear_gb300/csrc/potrf_blocked.cu', 'matrix_dense_linear_gb300/csrc/potrf_cta.cu', 'matrix_dense_linear_gb300/csrc/cta_common.cuh', 'matrix_dense_linear_gb300/csrc/trsm_tc.cu', 'matrix_dense_linear_gb300/csrc/syrk_tc.cu', 'matrix_dense_linear_gb300/csrc/tc_sm100.cuh', 'matrix_dense_linear_gb300/csrc/bl_common.cuh'), "5039563aab3a57de", 1708000000, "per call (4 launches)"),
+    "n1024": (('matrix_dense_linear_gb300/csrc/potrf_blocked.cu', 'matrix_dense_linear_gb300/csrc/potrf_cta.cu', 'matrix_dense_linear_gb300/csrc/cta_common.cuh', 'matrix_dense_linear_gb300/csrc/trsm_tc.cu', 'matrix_dense_linear_gb300/csrc/syrk_tc.cu', 'matrix_dense_linear_gb300/csrc/tc_sm100.cuh', 'matrix_dense_linear_gb300/csrc/bl_common.cuh'), "5039563aab3a57de", 6120000000, "per call (22 launches)"),
 }
 
 

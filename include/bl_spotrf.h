@@ -53,7 +53,8 @@ extern "C" {
                                resident, bulk copies) for n <= 64 and the aligned orders
                                96 and 128, else a warp per 32 x 32 tile in registers */
 #define BL_ROUTE_BLOCKED 3  /* K3: right-looking blocked, 128-wide panels: diagonal factor,
-                               panel triangular solve, lower-only trailing update, any n */
+                               panel triangular solve, lower-only trailing update, any n
+                               (forced: the right-looking order at any batch) */
 #define BL_ROUTE_TMEM 4     /* K2t: one thread block per matrix, the matrix resident in tensor
                                memory, trailing updates on the tensor cores, n <= 128 */
 #define BL_ROUTE_LEFT 5     /* K3's kernels in the left-looking order: per panel, its columns
@@ -99,7 +100,9 @@ int bl_spotrf_batched(float *A, int n, int lda, int64_t strideA, int batch, int 
 
 /*
  * bl_spotrf_batched_ex - as bl_spotrf_batched, with the kernel class forced
- * (route = BL_ROUTE_*; BL_ROUTE_AUTO selects by n like bl_spotrf_batched).
+ * (route = BL_ROUTE_*; BL_ROUTE_AUTO selects like bl_spotrf_batched: by n, and
+ * above n = 256 by batch between BL_ROUTE_BLOCKED and BL_ROUTE_LEFT, as
+ * bl_spotrf_route reports).
  * Returns -8 when the forced route cannot factor this n (WARP: n > 64;
  * CTA or TMEM: n > 128; LEFT: n <= 128), after the checks above. For tests
  * and measurement.

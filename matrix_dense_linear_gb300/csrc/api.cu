@@ -68,7 +68,17 @@ int run(float *A, int n, int lda, int64_t strideA, int batch, int *info, cudaStr
 {
     int e = check_args(A, n, lda, strideA, batch, info);
     if (e) return e;
-    if (route == BL_ROUTE_AUTO) route = route_for(n);
+    if (route == BL_ROUTE_AUTO) {
+        route = route_for(n);
+        // large batches of 16-byte-aligned matrices without a workspace: the
+        // blocked route's kernels in the left-looking order (a forced
+        // BL_ROUTE_BLOCKED keeps the right-looking one)
+        const bool aligned = ((reinterpret_cast<uintptr_t>(A) & 15) == 0) && (lda & 3) == 0 &&
+                             (strideA & 3) == 0;
+        if (route == BL_ROUTE_BLOCKED && W == nullptr && aligned &&
+            bl::left_pays(n, batch, bl::sm_count_or_default()))
+            route = BL_ROUTE_LEFT;
+    }
     if (!route_can_run(route, n, upper)) return -8;
     if (batch == 0) return 0;
     if (n == 0) return (int)cudaMemsetAsync(info, 0, sizeof(int) * (size_t)batch, stream);

@@ -18,9 +18,10 @@
 // driver on "kernelbot-cholesky-930185", whose measured defect (a full-square
 // trailing update costing 2n^3/3) the lower-only tiling avoids.
 //
-// Large batches of more than two panels take the left-looking order of the
-// same kernels instead (launch_left, below): per panel its columns updated by
-// every earlier panel at once, then its diagonal factor and panel solve.
+// On large batches of more than two panels the automatic route takes the
+// left-looking order of the same kernels instead (launch_left, below): per
+// panel its columns updated by every earlier panel at once, then its diagonal
+// factor and panel solve.
 //
 // A matrix whose info is already nonzero after a panel is skipped by every
 // later launch.
@@ -338,7 +339,8 @@ static bool delay_pays(int m, int batch, int sms)
     return (int64_t)batch * (T * (T + 1) / 2) >= 8 * 2 * (int64_t)sms;
 }
 
-// Whether the left-looking schedule pays: its per-panel update launch covers
+// Whether the left-looking schedule pays (the automatic route's choice for
+// 16-byte-aligned batches without a workspace): its per-panel update launch covers
 // batch x (row tiles of the panel) tiles with k growing by 128 a panel, so it
 // wins once the first of them spans about five waves (two tiles an SM): on
 // GB300, 1024 x 512 2.43 against 2.58 ms, 1024 x 1024 4.61 against 5.01,
@@ -365,11 +367,6 @@ int launch_blocked(float *A, int n, int lda, int64_t strideA, int batch, int *in
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return (int)cudaGetLastError();
-    // large batches of aligned panels (no workspace): the left-looking order
-    const bool aligned = ((reinterpret_cast<uintptr_t>(A) & 15) == 0) && (lda & 3) == 0 &&
-                         (strideA & 3) == 0;
-    if (W == nullptr && aligned && left_pays(n, batch, sms))
-        return launch_left(A, n, lda, strideA, batch, info, stream, upper);
     for (int c0 = 0; c0 < n; c0 += kNb) {
         const int nb = n - c0 < kNb ? n - c0 : kNb;
         int e = launch_cta(A + c0 + (int64_t)c0 * lda, nb, lda, strideA, batch, info, stream,
@@ -455,7 +452,7 @@ int sm_count_or_default()
     return sms;
 }
 
-// The left-looking schedule of the same kernels (the blocked driver's choice
+// The left-looking schedule of the same kernels (the automatic route's choice
 // where left_pays holds, and a forced route above order 128): per panel p, its
 // columns are first updated by every earlier panel at once,
 // A[c0:, c0:c0+128] -= L[c0:, :c0] L[c0:c0+128, :c0]^T
