@@ -256,3 +256,43 @@ def test_workspace_argument_codes(bl):
                                          None) == -10
     assert lib.bl_spotrf_batched_uplo_ws(b"Q", 16, 512, 512, 512 * 512, 2, 16, 4096, need,
                                          None) == -1
+
+
+def test_host_call_argument_codes(bl):
+    """bl_spotrf_batched_host checks its device buffers as A and info, then
+    the host buffers (-1, -6), then the streams (-11), all before any copy."""
+    import ctypes
+    lib = bl.library()
+    one = (ctypes.c_void_p * 1)(None)
+    st = ctypes.addressof(one)
+    # (A_host, n, lda, strideA, batch, info_host, A_dev, info_dev, streams, nstreams)
+    cases = [
+        ((16, 4, 4, 16, 2, 16, None, 16, st, 1), -1),
+        ((16, 4, 4, 16, 2, 16, 16, None, st, 1), -6),
+        ((16, 4, 3, 16, 2, 16, 16, 16, st, 1), -3),
+        ((16, -1, 4, 16, 2, 16, 16, 16, st, 1), -2),
+        ((16, 4, 4, 16, -1, 16, 16, 16, st, 1), -5),
+        ((None, 4, 4, 16, 2, 16, 16, 16, st, 1), -1),
+        ((16, 4, 4, 16, 2, None, 16, 16, st, 1), -6),
+        ((16, 4, 4, 16, 2, 16, 16, 16, None, 1), -11),
+        ((16, 4, 4, 16, 2, 16, 16, 16, st, 0), -11),
+        ((None, 4, 4, 16, 0, None, None, None, st, 1), 0),  # batch == 0: nothing to do
+    ]
+    for (Ah, n, lda, sA, batch, ih, Ad, idv, streams, ns), code in cases:
+        got = lib.bl_spotrf_batched_host(Ah, n, lda, sA, batch, ih, Ad, idv, 0, streams, ns)
+        assert got == code, (n, lda, batch, got, code)
+
+
+def test_static_call_scratch_limit(bl):
+    """bl_spotrf_batched_static: the argument codes first, then -10 when the
+    scratch the call would need passes the library's fixed array (checked on
+    the host before anything is looked up or launched)."""
+    lib = bl.library()
+    per = bl.workspace_bytes(512, 1)
+    fits = (16 << 20) // per  # matrices of order > 128 the 16 MB array holds
+    assert fits == 256
+    assert lib.bl_spotrf_batched_static(16, 512, 512, 512 * 512, fits + 1, 16, None) == -10
+    assert lib.bl_spotrf_batched_static(16, 4096, 4096, 4096 * 4096, 1000, 16, None) == -10
+    assert lib.bl_spotrf_batched_static(16, 512, 511, 512 * 512, fits + 1, 16, None) == -3
+    assert lib.bl_spotrf_batched_static(16, 512, 512, 512 * 512, fits + 1, None, None) == -6
+    assert lib.bl_spotrf_batched_static(None, 4, 4, 16, 0, None, None) == 0
